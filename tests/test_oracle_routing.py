@@ -1,0 +1,129 @@
+"""Pins of the oracle's routing (CPU only).
+
+Routing kinds of the spark_model MoE pages: softmax top-K (moe/init.rs `moe_topk_softmax`
+handles), sigmoid scoring with a correction bias used for selection only (moe/mod.rs
+`correction_bias_dev` field doc), static hash routing through tid2eid (moe/init.rs
+`new_with_hash` doc).  Checked against brute force over every k-subset, closed forms and the
+weight-sum invariant.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+from block_quantized_moe_router_gb300 import synth
+
+
+def _bf16(a):
+    import torch
+    return synth.bf16_bits(torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16))
+
+
+def _brute_topk(v, k):
+    """Best k-subset by brute force: the one whose minimum beats every unselected score."""
+    E = len(v)
+    best = None
+    for sub in itertools.combinations(range(E), k):
+        rest = [e for e in range(E) if e not in sub]
+        if not rest or min(v[list(sub)]) > max(v[rest]):
+            assert best is None, "ties in test data"
+            best = set(sub)
+    return best
+
+
+@pytest.mark.parametrize("scoring", [0, 1])
+@pytest.mark.parametrize("E,k", [(6, 2), (8, 3), (10, 4), (5, 5)])
+def test_topk_matches_brute_force(orc, scoring, E, k):
+    rng = np.random.default_rng(E * 10 + k + scoring)
+    T = 6
+    logits = rng.standard_normal((T, E)).astype(np.float32) * 2
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    r = orc.route(T=T, E=E, k=k, scoring=scoring, renorm=True, scaling=2.5 if scoring else 1.0,
+                  logits_in=logits, bias=bias)
+    for t in range(T):
+        l = logits[t].astype(np.float64)
+        v = l if scoring == 0 else 1 / (1 + np.exp(-l)) + bias
+        assert set(r["ids"][t]) == _brute_topk(v, k)
+        # descending selection score
+        sel = v[r["ids"][t]]
+        assert np.all(np.diff(sel) < 0)
+
+
+def test_softmax_weights_closed_form(orc):
+    rng = np.random.default_rng(3)
+    T, E, k = 5, 16, 4
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    r = orc.route(T=T, E=E, k=k, scoring=0, renorm=True, logits_in=logits)
+    r_nr = orc.route(T=T, E=E, k=k, scoring=0, renorm=False, logits_in=logits)
+    for t in range(T):
+        l = logits[t].astype(np.float64)
+        ids = r["ids"][t]
+        # renormalised top-k of softmax == softmax over the selected logits
+        sm_sel = np.exp(l[ids]) / np.exp(l[ids]).sum()
+        assert np.allclose(r["w"][t], sm_sel, rtol=0, atol=1e-15)
+        p = np.exp(l - l.max()) / np.exp(l - l.max()).sum()
+        assert np.allclose(r_nr["w"][t], p[ids], rtol=0, atol=1e-15)
+        assert abs(r["w"][t].sum() - 1.0) < 1e-12
+
+
+def test_sigmoid_bias_selects_but_does_not_weight(orc):
+    E, k = 4, 2
+    logits = np.array([[2.0, 1.0, 0.0, -1.0]], np.float32)
+    bias = np.array([0.0, 0.0, 0.5, 0.0], np.float32)
+    r = orc.route(T=1, E=E, k=k, scoring=1, renorm=True, scaling=2.5, logits_in=logits, bias=bias)
+    # scores: s = sigmoid(l) = .881, .731, .5, .269; +bias: .881, .731, 1.0, .269
+    assert list(r["ids"][0]) == [2, 0]
+    s = 1 / (1 + np.exp(-np.array([0.0, 2.0])))
+    assert np.allclose(r["w"][0], s / s.sum() * 2.5, atol=1e-15)
+    r_nr = orc.route(T=1, E=E, k=k, scoring=1, renorm=False, scaling=1.0, logits_in=logits, bias=bias)
+    assert np.allclose(r_nr["w"][0], s, atol=1e-15)
+
+
+@pytest.mark.parametrize("scoring,scaling", [(0, 1.0), (1, 2.5)])
+def test_weight_sum_invariant(orc, scoring, scaling):
+    rng = np.random.default_rng(11)
+    T, E, k = 64, 256, 8
+    logits = rng.standard_normal((T, E)).astype(np.float32) * 1.7
+    r = orc.route(T=T, E=E, k=k, scoring=scoring, renorm=True, scaling=scaling, logits_in=logits,
+                  bias=rng.uniform(-0.1, 0.1, E).astype(np.float32))
+    assert np.allclose(r["w"].sum(1), scaling, rtol=0, atol=1e-12)
+    for t in range(T):
+        assert len(set(r["ids"][t])) == k
+        assert r["ids"][t].min() >= 0 and r["ids"][t].max() < E
+
+
+def test_ties_break_to_lower_index(orc):
+    logits = np.array([[1.0, 3.0, 3.0, 2.0, 3.0]], np.float32)
+    r = orc.route(T=1, E=5, k=3, scoring=0, logits_in=logits)
+    assert list(r["ids"][0]) == [1, 2, 4]
+
+
+def test_router_gemm_fp64(orc):
+    rng = np.random.default_rng(5)
+    T, E, H = 3, 7, 64
+    x = rng.standard_normal((T, H)).astype(np.float32)
+    w = (rng.standard_normal((E, H)) * 0.02).astype(np.float32)
+    xb, wb = _bf16(x), _bf16(w)
+    r = orc.route(T=T, E=E, k=2, scoring=0, x_bf16=xb, w_router_bf16=wb)
+    xf = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    wf = (wb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.allclose(r["logits"], xf @ wf.T, rtol=0, atol=1e-14)
+
+
+def test_hash_routing_and_bad_ids(orc):
+    tid2eid = np.array([[0, 3], [2, 1], [5, 0], [1, -1]], np.int64)   # rows 2 and 3 hold bad ids
+    tok = np.array([1, 0, 2, 3, 7], np.int32)                          # token 7 is out of vocab
+    r = orc.route(T=5, E=4, k=2, scoring=2, tid2eid=tid2eid, token_ids=tok, vocab=4)
+    assert r["ids"].tolist() == [[2, 1], [0, 3], [-1, 0], [1, -1], [-1, -1]]
+    assert np.allclose(r["w"], [[.5, .5], [.5, .5], [0, .5], [.5, 0], [0, 0]])
+    assert r["status"] == (1 | 2)
+
+
+def test_nonfinite_logits_rank_last(orc):
+    logits = np.array([[np.nan, 0.5, np.inf, -1.0, 0.2]], np.float32)
+    r = orc.route(T=1, E=5, k=3, scoring=0, logits_in=logits)
+    assert list(r["ids"][0]) == [1, 4, 3]
+    assert r["status"] == 4
+    r = orc.route(T=1, E=5, k=4, scoring=1, scaling=1.0, logits_in=logits)
+    assert list(r["ids"][0])[:3] == [1, 4, 3] and r["w"][0][3] == 0.0
