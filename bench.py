@@ -1,0 +1,442 @@
+"""Benchmark of the MoE FFN block (router -> top-K -> NVFP4/MXFP4 experts -> combine).
+
+One step = one MoE layer forward (moe_route + moe_ffn_forward) over one batch of T synthetic
+tokens.  Steps cycle through L replicas of the layer's weights (distinct device copies, as the
+layers of a model would be) with L * touched-bytes >= 4 * L2, so every step streams its expert
+weights from HBM.  Each step is one CUDA-graph replay; the timed region is exactly K steps
+between a barrier + device synchronisation on both sides, timed with CUDA events on the
+launching stream, max over ranks.
+
+Prints one JSON line: MoE-layer tokens/s (whole job), the roofline of the dominant kernel
+(algorithmic bytes / its CUDA-event duration measured inside the timed region), the clocks
+seen during the timed region, an end-to-end figure through the public API with host buffers,
+and the CPU oracle's throughput on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config dec1] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from block_quantized_moe_router_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and achieved HBM GB/s or FP4 TFLOP/s vs GB300 peak"
+DEFAULT_CONFIG = "dec1"
+FALLBACK_HBM_GBS = 6800.0
+
+# ncu DRAM traffic (read + write bytes per launch) of the dominant kernel, keyed by workload,
+# with the hash of the kernel source it was captured on; reported only while the hash matches.
+TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("ffn.cu", "common.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "block_quantized_moe_router_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+            if key in d:
+                return float(d[key]), "measured"
+    except Exception:
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------------
+# workload accounting
+# ------------------------------------------------------------------------------------------
+def proj_bytes(N, K, fmt):
+    sv = 16 if fmt == synth.FMT_NVFP4 else 32
+    return N * K // 2 + N * K // sv + (4 if fmt == synth.FMT_NVFP4 else 0)
+
+
+def step_bytes(cfg, n_touched):
+    """Algorithmic HBM bytes of one layer step (touched experts only)."""
+    H, I, Is = cfg.H, cfg.I, cfg.I_shared
+    gate_up = 2 * proj_bytes(I, H, cfg.fmt)
+    down = proj_bytes(H, I, cfg.fmt)
+    sh_gate_up = 2 * proj_bytes(Is, H, cfg.shared_fmt) if Is else 0
+    sh_down = proj_bytes(H, Is, cfg.shared_fmt) if Is else 0
+    router = cfg.E * H * 2 if cfg.scoring != synth.SCORE_HASH else cfg.T * cfg.k * 8
+    acts = cfg.T * H * 2 * 2
+    return {"gate_up": n_touched * gate_up + sh_gate_up + cfg.T * H * 2,
+            "total": n_touched * (gate_up + down) + sh_gate_up + sh_down + router + acts}
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ------------------------------------------------------------------------------------------
+def oracle_step(cfg, inp_np, tokens, n_threads=0):
+    """One oracle layer pass over `tokens` (route + expert FFN + combine)."""
+    import oracle
+    x = inp_np["x"][tokens]
+    if cfg.scoring == synth.SCORE_HASH:
+        r = oracle.route(T=len(tokens), E=cfg.E, k=cfg.k, scoring=2, scaling=cfg.scaling,
+                         tid2eid=inp_np["tid2eid"], token_ids=inp_np["token_ids"][tokens],
+                         vocab=cfg.vocab, nthreads=n_threads)
+    else:
+        r = oracle.route(T=len(tokens), E=cfg.E, k=cfg.k, scoring=cfg.scoring, renorm=cfg.renorm,
+                         scaling=cfg.scaling, x_bf16=x, w_router_bf16=inp_np["w_router"],
+                         bias=inp_np.get("bias"), nthreads=n_threads)
+    return oracle.moe_ffn(T=len(tokens), E=cfg.E, H=cfg.H, I=cfg.I, k=cfg.k, gate=inp_np["gate"],
+                          up=inp_np["up"], down=inp_np["down"], x_bf16=x, ids=r["ids"], w=r["w"],
+                          sh_I=cfg.I_shared, sh_gate=inp_np.get("sh_gate"), sh_up=inp_np.get("sh_up"),
+                          sh_down=inp_np.get("sh_down"), act_mode=cfg.act, nthreads=n_threads)
+
+
+def host_inputs(cfg, seed):
+    inp = synth.make_inputs(cfg, seed=seed, device="cuda" if torch.cuda.is_available() else "cpu")
+    d = {"x": synth.bf16_bits(inp["x"])}
+    if "w_router" in inp:
+        d["w_router"] = synth.bf16_bits(inp["w_router"])
+    for key in ("bias", "tid2eid", "token_ids"):
+        if key in inp:
+            d[key] = inp[key].cpu().numpy()
+    for key in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
+        if key in inp:
+            d[key] = synth.to_numpy_proj(inp[key])
+    return inp, d
+
+
+def cpu_baseline(cfg, inp_np, budget_s=10.0):
+    """Oracle tokens/s on the host cores over a bounded sample of the workload."""
+    import oracle
+    oracle.build()
+    threads = oracle.hardware_threads()
+    # one of the workload's tokens per host thread (the oracle threads over tokens)
+    n_tok = max(1, threads)
+    tokens = np.arange(n_tok) % cfg.T
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        oracle_step(cfg, inp_np, tokens)
+        done += len(tokens)
+        if time.perf_counter() - t0 >= budget_s or done >= 64 * cfg.T:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": min(threads, len(tokens)), "kind": "oracle",
+            "sample": f"{done} tokens of workload {cfg.name} in batches of {n_tok}, {dt:.1f} s"}
+
+
+def run_reference(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    _, inp_np = host_inputs(cfg, seed=0)
+    tokens_all = np.arange(cfg.T)
+    # size each step's sample so that warmup + steps fit in about two minutes
+    t0 = time.perf_counter()
+    oracle_step(cfg, inp_np, tokens_all[:1])
+    t_tok = time.perf_counter() - t0
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n_tok = int(max(1, min(cfg.T, per_step_budget // max(t_tok, 1e-6))))
+    sample = tokens_all[:n_tok]
+    for _ in range(args.warmup):
+        oracle_step(cfg, inp_np, sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(cfg, inp_np, sample)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n_tok / dt
+    threads = min(oracle.hardware_threads(), n_tok)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 * cfg.T / n_tok, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                       "top_k": cfg.k, "I_shared": cfg.I_shared},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n_tok} of {cfg.T} tokens per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------
+def run_ours(args, cfg):
+    from block_quantized_moe_router_gb300 import build, capi
+    from block_quantized_moe_router_gb300.layer import MoeLayer
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    capi.load_library()
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 0) or 128 * 2 ** 20
+
+    inp = synth.make_inputs(cfg, seed=rank, device="cuda")
+    base = MoeLayer.from_inputs(inp)
+    x = inp["x"].cuda()
+    tok = inp["token_ids"].cuda() if "token_ids" in inp else None
+    T = cfg.T
+    ids0, _, _ = base.route(x, token_ids=tok)
+    torch.cuda.synchronize()
+    touched = int(torch.unique(ids0[ids0 >= 0]).numel())
+    nbytes = step_bytes(cfg, touched)
+    replicas = max(1, math.ceil(4 * l2 / nbytes["total"]))
+    if args.replicas:
+        replicas = args.replicas
+
+    layers = [base]
+    for _ in range(replicas - 1):
+        clone = {k: ({kk: (vv.clone() if isinstance(vv, torch.Tensor) else vv)
+                      for kk, vv in v.items()} if isinstance(v, dict) else v)
+                 for k, v in inp.items()}
+        layers.append(MoeLayer.from_inputs(clone))
+    bufs = []
+    for layer in layers:
+        layer.workspace(T)
+        bufs.append(dict(ids=torch.empty((T, cfg.k), dtype=torch.int32, device="cuda"),
+                         w=torch.empty((T, cfg.k), dtype=torch.float32, device="cuda"),
+                         logits=torch.empty((T, cfg.E), dtype=torch.float32, device="cuda"),
+                         out=torch.empty((T, cfg.H), dtype=torch.bfloat16, device="cuda")))
+        capi.moe_profile_enable(layer.handle, 1 << capi.PHASE_GATE_UP)
+
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for layer, b in zip(layers, bufs):   # one eager pass per replica before capture
+            layer.route(x, token_ids=tok, topk_ids=b["ids"], topk_w=b["w"],
+                        logits_out=None if tok is not None else b["logits"])
+            layer.ffn(x, b["ids"], b["w"], out=b["out"])
+        stream.synchronize()
+        for layer, b in zip(layers, bufs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                layer.route(x, token_ids=tok, topk_ids=b["ids"], topk_w=b["w"],
+                            logits_out=None if tok is not None else b["logits"])
+                layer.ffn(x, b["ids"], b["w"], out=b["out"])
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % replicas].replay()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[(args.warmup + i) % replicas].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    # dominant kernel: the last execution of the gate+up GEMM of each replica, all inside the
+    # timed region when steps >= replicas
+    dom = [capi.moe_profile_read(l.handle)[capi.PHASE_GATE_UP] for l in layers]
+    dom_ms = float(np.mean(dom))
+    if dist is not None:
+        t = torch.tensor([ms, dom_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, dom_ms = float(t[0]), float(t[1])
+    ok = all(torch.equal(bufs[0]["out"], b["out"]) for b in bufs[1:])
+
+    # end to end through the public API with host buffers: H2D of x, route + FFN, D2H of out
+    e2e_s = float("nan")
+    x_host = inp["x"].pin_memory()
+    out_host = torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    tok_host = inp["token_ids"].pin_memory() if tok is not None else None
+    x_dev = torch.empty_like(x)
+    tok_dev = torch.empty_like(tok) if tok is not None else None
+    e2e_steps = max(3, min(args.steps, 200)) if args.e2e else 0
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps + args.warmup if args.e2e else 0):
+            if i == args.warmup:
+                barrier()
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            layer = layers[i % replicas]
+            x_dev.copy_(x_host, non_blocking=True)
+            if tok_dev is not None:
+                tok_dev.copy_(tok_host, non_blocking=True)
+            o = layer.forward(x_dev, token_ids=tok_dev)
+            out_host.copy_(o, non_blocking=True)
+            stream.synchronize()
+    if args.e2e:
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t[0])
+    h2d = T * cfg.H * 2 + (T * 4 if tok is not None else 0)
+    d2h = T * cfg.H * 2
+
+    if rank == 0:
+        peak, peak_kind = measured_peaks()
+        achieved = nbytes["gate_up"] / (dom_ms * 1e-3) / 1e9
+        layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
+        src = kernel_source_hash()
+        tr = TRAFFIC.get(cfg.name)
+        traffic = tr[0] if tr and tr[1] == src else None
+        line = {
+            "metric": METRIC, "value": T * world / (ms * 1e-3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 weights, f16 mma / f32 accumulate" if cfg.act == synth.ACT_BF16
+            else "nvfp4 weights and activations, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "T": T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                       "top_k": cfg.k, "I_shared": cfg.I_shared, "replicas": replicas,
+                       "l2_policy": f"inputs larger than L2: {replicas} weight replicas cycled, "
+                                    f"{replicas * nbytes['total'] / 1e6:.0f} MB touched per cycle",
+                       "touched_experts": touched},
+            "gpu_launches": args.steps * launches_per_step(cfg),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "expert_mma_kernel<gate+up>",
+                         "bytes_per_launch": nbytes["gate_up"], "launch_ms": dom_ms,
+                         "peak_source": peak_kind},
+            "layer_roofline": {"achieved": layer_gbs, "peak": peak, "unit": "GB/s",
+                               "frac": layer_gbs / peak, "bytes_per_step": nbytes["total"]},
+            "clocks": clk,
+            "e2e": {"value": T * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+            "replica_outputs_equal": ok,
+            "kernel_source": src,
+        }
+        if args.cpu_baseline:
+            _, inp_np = host_inputs_from(inp)
+            line["cpu_baseline"] = cpu_baseline(cfg, inp_np, budget_s=args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    for layer in layers:
+        layer.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def host_inputs_from(inp):
+    d = {"x": synth.bf16_bits(inp["x"])}
+    if "w_router" in inp:
+        d["w_router"] = synth.bf16_bits(inp["w_router"])
+    for key in ("bias", "tid2eid", "token_ids"):
+        if key in inp:
+            d[key] = inp[key].cpu().numpy()
+    for key in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
+        if key in inp:
+            d[key] = synth.to_numpy_proj(inp[key])
+    return inp, d
+
+
+def launches_per_step(cfg):
+    """Kernels one step launches: router GEMM + top-K (or the hash lookup), then dispatch,
+    gate+up GEMM, down GEMM and combine."""
+    route = 1 if cfg.scoring == synth.SCORE_HASH else 2
+    return route + 4
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(synth.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--replicas", type=int, default=0,
+                    help="weight replicas to cycle (default: enough to exceed 4x L2)")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,276 @@
+// api.cu -- the C ABI declared in include/moe.h: argument validation, the prepared-weights
+// handle and the launch sequence.  Argument checks follow the construction-time checks of
+// the spark_model MoE layer (moe/init.rs, `MoeLayer::new_with_hash`: 1 <= top_k <= E, and
+// top_k / E bounded by the routing kernels' fixed per-warp storage).
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using namespace moe;
+
+bool pow2_positive(float g) {
+    if (!(g > 0.f) || !std::isfinite(g)) return false;
+    int ex = 0;
+    return std::frexp(g, &ex) == 0.5f;
+}
+
+bool valid_fmt(int f) { return f == MOE_FMT_NVFP4 || f == MOE_FMT_MXFP4; }
+
+bool valid_qtensor(const moe_qtensor& t) {
+    if (!t.packed || !t.scales || !valid_fmt(t.fmt)) return false;
+    if (t.fmt == MOE_FMT_NVFP4 && !t.globals) return false;
+    return true;
+}
+
+struct PreparedProj {
+    ProjView view{};
+    int32_t* mx_off = nullptr;  // owned
+    float* mx_post = nullptr;   // owned
+};
+
+struct Handle {
+    uint32_t magic = 0x4D4F4531u;  // "MOE1"
+    moe_ffn_desc desc{};
+    PreparedProj gate, up, down, sh_gate, sh_up, sh_down;
+    uint32_t profile_mask = 0;
+    PhaseEvents events{};  // owned; created by moe_profile_enable
+};
+
+void destroy_events(Handle* h) {
+    for (int i = 0; i < 4; ++i) {
+        if (h->events.begin[i]) cudaEventDestroy(h->events.begin[i]);
+        if (h->events.end[i]) cudaEventDestroy(h->events.end[i]);
+        h->events.begin[i] = h->events.end[i] = nullptr;
+    }
+    h->profile_mask = 0;
+}
+
+moe_status_t prepare_proj(const moe_qtensor& t, int E, int64_t N, int64_t K, PreparedProj& out,
+                          cudaStream_t st) {
+    out.view.packed = static_cast<const uint8_t*>(t.packed);
+    out.view.scales = static_cast<const uint8_t*>(t.scales);
+    out.view.fmt = t.fmt;
+    if (t.fmt == MOE_FMT_NVFP4) {
+        out.view.post = t.globals;
+        out.view.mx_off = nullptr;
+        return MOE_OK;
+    }
+    if (cudaMalloc(&out.mx_off, sizeof(int32_t) * E) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMalloc(&out.mx_post, sizeof(float) * E) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_mx_offsets(out.view.scales, E, N * (K / 32), out.mx_off, out.mx_post, st) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    out.view.post = out.mx_post;
+    out.view.mx_off = out.mx_off;
+    return MOE_OK;
+}
+
+void free_proj(PreparedProj& p) {
+    if (p.mx_off) cudaFree(p.mx_off);
+    if (p.mx_post) cudaFree(p.mx_post);
+    p.mx_off = nullptr;
+    p.mx_post = nullptr;
+}
+
+moe_status_t validate_ffn_desc(const moe_ffn_desc* d) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->E < 1 || d->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (d->top_k < 1 || d->top_k > d->E || d->top_k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+    if (d->H < 128 || d->H % 128 || d->I < 128 || d->I % 128) return MOE_ERR_INVALID_ARG;
+    if (d->I_shared < 0 || d->I_shared % 128) return MOE_ERR_INVALID_ARG;
+    if (!valid_qtensor(d->gate) || !valid_qtensor(d->up) || !valid_qtensor(d->down))
+        return MOE_ERR_INVALID_ARG;
+    if (d->gate.fmt != d->up.fmt || d->gate.fmt != d->down.fmt) return MOE_ERR_UNSUPPORTED;
+    if (d->I_shared > 0) {
+        if (!valid_qtensor(d->sh_gate) || !valid_qtensor(d->sh_up) || !valid_qtensor(d->sh_down))
+            return MOE_ERR_INVALID_ARG;
+        if (d->sh_gate.fmt != d->sh_up.fmt || d->sh_gate.fmt != d->sh_down.fmt)
+            return MOE_ERR_UNSUPPORTED;
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: argument out of range";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: combination not implemented";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA call or kernel launch failed";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small";
+    }
+    return "unknown moe_status_t";
+}
+
+moe_status_t moe_route(const moe_route_desc* d, const void* x_bf16, const float* logits_in,
+                       float* logits_out, int32_t* topk_ids, float* topk_w, int32_t* dev_status,
+                       void* stream) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->E < 1 || d->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (d->top_k < 1 || d->top_k > d->E || d->top_k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+    if (!std::isfinite(d->routed_scaling)) return MOE_ERR_INVALID_ARG;
+    if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID &&
+        d->scoring != MOE_SCORE_HASH)
+        return MOE_ERR_INVALID_ARG;
+    if (d->scoring == MOE_SCORE_HASH && d->vocab < 1) return MOE_ERR_INVALID_ARG;
+    if (d->scoring != MOE_SCORE_HASH && !logits_in && (d->H < 32 || d->H % 32))
+        return MOE_ERR_INVALID_ARG;
+    if (d->T == 0) return MOE_OK;
+    if (!topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (d->scoring == MOE_SCORE_HASH) {
+        if (!d->tid2eid || !d->token_ids) return MOE_ERR_INVALID_ARG;
+        return launch_hash_route(d->tid2eid, d->token_ids, d->vocab, d->T, d->E, d->top_k,
+                                 d->routed_scaling, topk_ids, topk_w, dev_status, st) == cudaSuccess
+                   ? MOE_OK : MOE_ERR_CUDA;
+    }
+    const float* logits = logits_in;
+    if (!logits) {
+        if (!d->w_router || !x_bf16 || !logits_out) return MOE_ERR_INVALID_ARG;
+        if (launch_router_logits(x_bf16, d->w_router, logits_out, d->T, d->E, d->H, st) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        logits = logits_out;
+    }
+    const float* bias = d->scoring == MOE_SCORE_SIGMOID ? d->correction_bias : nullptr;
+    return launch_topk(logits, bias, d->T, d->E, d->top_k, d->scoring, d->renormalize ? 1 : 0,
+                       d->routed_scaling, topk_ids, topk_w, dev_status, st) == cudaSuccess
+               ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_workspace_size(const moe_ffn_desc* d, int32_t T, int32_t act, size_t* bytes) {
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    moe_status_t v = validate_ffn_desc(d);
+    if (v != MOE_OK) return v;
+    if (T < 0 || (act != MOE_ACT_BF16 && act != MOE_ACT_NVFP4)) return MOE_ERR_INVALID_ARG;
+    *bytes = Workspace::plan(d->E, d->H, d->I, d->I_shared, d->top_k, T, act).total;
+    return MOE_OK;
+}
+
+moe_status_t moe_prepare_weights(const moe_ffn_desc* d, void** handle_out, void* stream) {
+    if (!handle_out) return MOE_ERR_INVALID_ARG;
+    *handle_out = nullptr;
+    moe_status_t v = validate_ffn_desc(d);
+    if (v != MOE_OK) return v;
+    Handle* h = new (std::nothrow) Handle();
+    if (!h) return MOE_ERR_CUDA;
+    h->desc = *d;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    moe_status_t s = MOE_OK;
+    const int E = d->E, H = d->H, I = d->I, Is = d->I_shared;
+    if (s == MOE_OK) s = prepare_proj(d->gate, E, I, H, h->gate, st);
+    if (s == MOE_OK) s = prepare_proj(d->up, E, I, H, h->up, st);
+    if (s == MOE_OK) s = prepare_proj(d->down, E, H, I, h->down, st);
+    if (Is > 0) {
+        if (s == MOE_OK) s = prepare_proj(d->sh_gate, 1, Is, H, h->sh_gate, st);
+        if (s == MOE_OK) s = prepare_proj(d->sh_up, 1, Is, H, h->sh_up, st);
+        if (s == MOE_OK) s = prepare_proj(d->sh_down, 1, H, Is, h->sh_down, st);
+    }
+    if (s == MOE_OK && cudaStreamSynchronize(st) != cudaSuccess) s = MOE_ERR_CUDA;
+    if (s != MOE_OK) {
+        moe_release_weights(h);
+        return s;
+    }
+    *handle_out = h;
+    return MOE_OK;
+}
+
+moe_status_t moe_release_weights(void* handle) {
+    Handle* h = static_cast<Handle*>(handle);
+    if (!h || h->magic != 0x4D4F4531u) return MOE_ERR_INVALID_ARG;
+    free_proj(h->gate); free_proj(h->up); free_proj(h->down);
+    free_proj(h->sh_gate); free_proj(h->sh_up); free_proj(h->sh_down);
+    destroy_events(h);
+    h->magic = 0;
+    delete h;
+    return MOE_OK;
+}
+
+moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g_act1,
+                             float g_act2, const void* x_bf16, const int32_t* topk_ids,
+                             const float* topk_w, void* out_bf16, void* workspace,
+                             size_t ws_bytes, int32_t* dev_status, void* stream) {
+    const Handle* h = static_cast<const Handle*>(handle);
+    if (!h || h->magic != 0x4D4F4531u) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || (act != MOE_ACT_BF16 && act != MOE_ACT_NVFP4)) return MOE_ERR_INVALID_ARG;
+    if (act == MOE_ACT_NVFP4 && (!pow2_positive(g_act1) || !pow2_positive(g_act2)))
+        return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !topk_ids || !topk_w || !out_bf16 || !workspace) return MOE_ERR_INVALID_ARG;
+    const moe_ffn_desc& d = h->desc;
+    const Workspace ws = Workspace::plan(d.E, d.H, d.I, d.I_shared, d.top_k, T, act);
+    if (ws_bytes < ws.total) return MOE_ERR_WORKSPACE;
+    char* base = static_cast<char*>(workspace);
+    FfnLaunch L{};
+    L.T = T; L.E = d.E; L.H = d.H; L.I = d.I; L.k = d.top_k; L.I_shared = d.I_shared;
+    L.act = act; L.g1 = g_act1; L.g2 = g_act2;
+    L.x = x_bf16; L.ids = topk_ids; L.w = topk_w; L.out = out_bf16; L.status = dev_status;
+    L.gate = h->gate.view; L.up = h->up.view; L.down = h->down.view;
+    L.sh_gate = h->sh_gate.view; L.sh_up = h->sh_up.view; L.sh_down = h->sh_down.view;
+    L.counts = reinterpret_cast<int32_t*>(base + ws.counts);
+    L.offsets = reinterpret_cast<int32_t*>(base + ws.offsets);
+    L.active = reinterpret_cast<int32_t*>(base + ws.active);
+    L.meta = reinterpret_cast<int32_t*>(base + ws.meta);
+    L.sorted_pair = reinterpret_cast<int32_t*>(base + ws.sorted_pair);
+    L.pos_of_pair = reinterpret_cast<int32_t*>(base + ws.pos_of_pair);
+    L.x16 = reinterpret_cast<__half*>(base + ws.x16);
+    L.xq = reinterpret_cast<uint8_t*>(base + ws.xq);
+    L.xs = reinterpret_cast<uint8_t*>(base + ws.xs);
+    L.h16 = reinterpret_cast<__half*>(base + ws.h16);
+    L.hq = reinterpret_cast<uint8_t*>(base + ws.hq);
+    L.hs = reinterpret_cast<uint8_t*>(base + ws.hs);
+    L.y = reinterpret_cast<float*>(base + ws.y);
+    return launch_ffn(L, static_cast<cudaStream_t>(stream), h->profile_mask ? &h->events : nullptr) ==
+                   cudaSuccess
+               ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_profile_enable(void* handle, uint32_t mask) {
+    Handle* h = static_cast<Handle*>(handle);
+    if (!h || h->magic != 0x4D4F4531u || (mask & ~0xFu)) return MOE_ERR_INVALID_ARG;
+    destroy_events(h);
+    for (int i = 0; i < 4; ++i) {
+        if (!(mask & (1u << i))) continue;
+        if (cudaEventCreate(&h->events.begin[i]) != cudaSuccess ||
+            cudaEventCreate(&h->events.end[i]) != cudaSuccess) {
+            destroy_events(h);
+            return MOE_ERR_CUDA;
+        }
+    }
+    h->profile_mask = mask;
+    return MOE_OK;
+}
+
+moe_status_t moe_profile_read(void* handle, float* ms_out) {
+    Handle* h = static_cast<Handle*>(handle);
+    if (!h || h->magic != 0x4D4F4531u || !ms_out) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i) {
+        ms_out[i] = -1.f;
+        if (!(h->profile_mask & (1u << i))) continue;
+        if (cudaEventSynchronize(h->events.end[i]) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaEventElapsedTime(&ms_out[i], h->events.begin[i], h->events.end[i]) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+moe_status_t moe_quantize_act_nvfp4(const void* x_bf16, int64_t rows, int64_t K, float g,
+                                    uint8_t* packed, uint8_t* scales, void* stream) {
+    if (rows < 0 || K < 16 || K % 16 || !(g > 0.f) || !std::isfinite(g))
+        return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!x_bf16 || !packed || !scales) return MOE_ERR_INVALID_ARG;
+    return launch_quantize_act(x_bf16, rows, K, g, packed, scales, nullptr,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

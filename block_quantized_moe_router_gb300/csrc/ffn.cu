@@ -1,0 +1,525 @@
+// ffn.cu -- expert dispatch and the grouped expert FFN on the warp-level tensor-core path.
+//
+// Structure (spark_model MoE pages, moe/mod.rs module doc and `MoeLayer` field docs):
+//   1. dispatch: histogram of the routed (token, slot) pairs per expert, offsets, the list of
+//      experts that received tokens, and the permutation grouping pairs by expert
+//      (`moe_sort_by_expert`, `moe_build_tile_worklist` handles);
+//   2. gate+up projection of every routed pair and of the shared expert, SiLU(gate)*up fused
+//      into its epilogue (`moe_expert_gate_up_shared`);
+//   3. down projection, the routing weight applied in its epilogue
+//      (`moe_expert_silu_down_shared`);
+//   4. top-K weighted sum plus the shared expert (`moe_weighted_sum_blend`).
+//
+// Weight formats (moe/mod.rs, `MoeLayer::experts_scale_kind` field doc): NVFP4 = E2M1 codes,
+// FP8-E4M3 scale per 16, f32 per-tensor global; MXFP4 = E2M1 codes, E8M0 scale per 32.
+//
+// The grouped GEMM: each warp owns 16 output rows of one expert and streams their packed
+// weight rows with 16-byte loads (32 E2M1 codes per lane per step).  Codes are converted to
+// f16 with the hardware E2M1->f16x2 conversion and multiplied by the f16 block scale (both
+// exact: an E2M1 value times an E4M3 value has at most 6 significant bits and lies within
+// [2^-10, 2688]); the per-tensor global is applied in fp32 at the end.  The columns are the
+// expert's routed pairs (8 per m16n8k16 MMA tile), so each weight row is read once per
+// launch whatever the number of tokens routed to the expert.  Activations enter as f16
+// (bf16 tokens converted once; the NVFP4-quantized tokens and h are exact in f16).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
+
+// ------------------------------------------------------------------------------------------
+// The NVFP4 activation quantizer on 16 fp32 values: writes 8 packed bytes, one E4M3 scale
+// byte and (optionally) the 16 exact dequantized values as f16.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void quant16(const float (&v)[16], float g, uint8_t* packed,
+                                        uint8_t* scale, __half* deq) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    float qs = amax / 6.0f;
+    qs = qs / g;
+    const uint32_t s = f32_to_e4m3(qs);
+    const float denom = e4m3_to_f32(s) * g;
+    uint32_t bytes[8];
+    float dq[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t b = 0;
+        if (denom != 0.f) b = f32x2_to_e2m1x2(v[2 * i] / denom, v[2 * i + 1] / denom);
+        bytes[i] = b;
+        dq[2 * i] = e2m1_to_f32(b & 0xF) * denom;
+        dq[2 * i + 1] = e2m1_to_f32(b >> 4) * denom;
+    }
+    uint2 pk;
+    pk.x = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+    pk.y = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+    *reinterpret_cast<uint2*>(packed) = pk;
+    *scale = (uint8_t)s;
+    if (deq) {
+        uint4 a, b;
+        a.x = pack_half2(dq[0], dq[1]);   a.y = pack_half2(dq[2], dq[3]);
+        a.z = pack_half2(dq[4], dq[5]);   a.w = pack_half2(dq[6], dq[7]);
+        b.x = pack_half2(dq[8], dq[9]);   b.y = pack_half2(dq[10], dq[11]);
+        b.z = pack_half2(dq[12], dq[13]); b.w = pack_half2(dq[14], dq[15]);
+        reinterpret_cast<uint4*>(deq)[0] = a;
+        reinterpret_cast<uint4*>(deq)[1] = b;
+    }
+}
+
+__device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v)[16]) {
+    const uint4 a = ldg_cached128(src), b = ldg_cached128(src + 8);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Dispatch (block 0) + activation conversion/quantization (blocks 1..).
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(512) prep_kernel(FfnLaunch L) {
+    const int tid = threadIdx.x;
+    if (blockIdx.x == 0) {
+        __shared__ int s_cnt[kMaxExperts];
+        __shared__ int s_cur[kMaxExperts];
+        const int E = L.E, P = L.T * L.k;
+        for (int e = tid; e < E; e += blockDim.x) s_cnt[e] = 0;
+        __syncthreads();
+        int bad = 0;
+        for (int p = tid; p < P; p += blockDim.x) {
+            const int e = L.ids[p];
+            if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+            else if (e != -1) bad = 1;
+        }
+        if (bad) status_or(L.status, MOE_DEV_BAD_EXPERT_ID);
+        __syncthreads();
+        if (tid < 32) {
+            const int lane = tid;
+            const int per = (E + 31) / 32;
+            const int lo = min(E, lane * per), hi = min(E, lo + per);
+            int sum = 0, nz = 0;
+            for (int e = lo; e < hi; ++e) { sum += s_cnt[e]; nz += s_cnt[e] > 0; }
+            int isum = sum, inz = nz;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, isum, o);
+                const int b = __shfl_up_sync(0xffffffffu, inz, o);
+                if (lane >= o) { isum += a; inz += b; }
+            }
+            int off = isum - sum, act = inz - nz;
+            for (int e = lo; e < hi; ++e) {
+                const int c = s_cnt[e];
+                L.offsets[e] = off;
+                L.counts[e] = c;
+                s_cur[e] = off;
+                if (c > 0) L.active[act++] = e;
+                off += c;
+            }
+            if (lane == 31) {
+                L.offsets[E] = isum;
+                L.meta[0] = inz;  // number of experts with at least one pair
+                L.meta[1] = isum; // number of valid routed pairs
+            }
+        }
+        __syncthreads();
+        for (int p = tid; p < P; p += blockDim.x) {
+            const int e = L.ids[p];
+            if (e >= 0 && e < E) {
+                const int pos = atomicAdd(&s_cur[e], 1);
+                L.sorted_pair[pos] = p;
+                L.pos_of_pair[p] = pos;
+            } else {
+                L.pos_of_pair[p] = -1;
+            }
+        }
+        return;
+    }
+    // activation conversion: one thread per 16 elements of x
+    const int64_t n16 = (int64_t)L.T * L.H / 16;
+    const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
+    const auto* x = static_cast<const __nv_bfloat16*>(L.x);
+    for (int64_t i = (int64_t)(blockIdx.x - 1) * blockDim.x + tid; i < n16; i += stride) {
+        float v[16];
+        load_bf16x16(x + i * 16, v);
+        if (L.act == MOE_ACT_NVFP4) {
+            quant16(v, L.g1, L.xq + i * 8, L.xs + i, L.x16 + i * 16);
+        } else {
+            uint4 a, b;
+            a.x = pack_half2(v[0], v[1]);   a.y = pack_half2(v[2], v[3]);
+            a.z = pack_half2(v[4], v[5]);   a.w = pack_half2(v[6], v[7]);
+            b.x = pack_half2(v[8], v[9]);   b.y = pack_half2(v[10], v[11]);
+            b.z = pack_half2(v[12], v[13]); b.w = pack_half2(v[14], v[15]);
+            reinterpret_cast<uint4*>(L.x16 + i * 16)[0] = a;
+            reinterpret_cast<uint4*>(L.x16 + i * 16)[1] = b;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Grouped expert GEMM on m16n8k16 f16 MMAs.
+// ------------------------------------------------------------------------------------------
+// Block-scale of the 16-byte chunk (32 codes) a lane holds, as f16x2 pairs for the chunk's
+// first and second 16 elements.
+template <int FMT>
+__device__ __forceinline__ void chunk_scales(const uint8_t* srow, int step, int q, int mxbias,
+                                             uint32_t& lo, uint32_t& hi) {
+    if constexpr (FMT == MOE_FMT_NVFP4) {
+        const uint32_t s2 = ldg_u16(srow + step * 8 + 2 * q);
+        const uint32_t h = e4m3x2_to_f16x2(s2);
+        lo = __byte_perm(h, h, 0x1010);
+        hi = __byte_perm(h, h, 0x3232);
+    } else {
+        const int b = (int)ldg_u8(srow + step * 4 + q);
+        const int field = min(30, max(0, b - mxbias));
+        const uint32_t bits = (uint32_t)field << 10;
+        lo = hi = bits | (bits << 16);
+    }
+}
+
+struct ChunkA {
+    uint4 r0, r1;       // packed codes of rows g and g+8
+    uint32_t s0lo, s0hi, s1lo, s1hi;
+};
+
+template <int FMT>
+__device__ __forceinline__ void load_chunk(ChunkA& c, const uint8_t* p0, const uint8_t* p1,
+                                           const uint8_t* s0, const uint8_t* s1, int step, int q,
+                                           int mxbias) {
+    c.r0 = ldg_stream128(p0 + step * 64);
+    c.r1 = ldg_stream128(p1 + step * 64);
+    chunk_scales<FMT>(s0, step, q, mxbias, c.s0lo, c.s0hi);
+    chunk_scales<FMT>(s1, step, q, mxbias, c.s1lo, c.s1hi);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// A fragment of MMA step i (0..7) from a chunk: rows g / g+8, k-slots (2q,2q+1) = chunk
+// elements 4i, 4i+1 and k-slots (2q+8, 2q+9) = chunk elements 4i+2, 4i+3.
+template <int I>
+__device__ __forceinline__ void frag_a(const ChunkA& c, uint32_t (&a)[4]) {
+    const uint32_t w0 = word_of(c.r0, I >> 1), w1 = word_of(c.r1, I >> 1);
+    const uint32_t sc0 = (I < 4) ? c.s0lo : c.s0hi;
+    const uint32_t sc1 = (I < 4) ? c.s1lo : c.s1hi;
+    constexpr int SEL = (I & 1) * 2;
+    a[0] = hmul2(e2m1x2_to_f16x2<SEL>(w0), sc0);
+    a[1] = hmul2(e2m1x2_to_f16x2<SEL>(w1), sc1);
+    a[2] = hmul2(e2m1x2_to_f16x2<SEL + 1>(w0), sc0);
+    a[3] = hmul2(e2m1x2_to_f16x2<SEL + 1>(w1), sc1);
+}
+
+template <int MODE, int NT, int FMT>
+__device__ __forceinline__ void expert_rows(const FfnLaunch& L, bool shared, int e, int row0,
+                                            int cnt, int N, int K, int n0) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int sv = (FMT == MOE_FMT_NVFP4) ? 16 : 32;
+    const ProjView& PA = MODE == MODE_GATEUP ? (shared ? L.sh_gate : L.gate)
+                                             : (shared ? L.sh_down : L.down);
+    const ProjView& PB = shared ? L.sh_up : L.up;
+    const size_t rowA = (size_t)e * N + n0 + g;
+    const uint8_t* pa0 = PA.packed + rowA * (K / 2) + 16 * q;
+    const uint8_t* pa1 = pa0 + (size_t)8 * (K / 2);
+    const uint8_t* sa0 = PA.scales + rowA * (K / sv);
+    const uint8_t* sa1 = sa0 + (size_t)8 * (K / sv);
+    const uint8_t *pb0 = nullptr, *pb1 = nullptr, *sb0 = nullptr, *sb1 = nullptr;
+    if (MODE == MODE_GATEUP) {
+        pb0 = PB.packed + rowA * (K / 2) + 16 * q;
+        pb1 = pb0 + (size_t)8 * (K / 2);
+        sb0 = PB.scales + rowA * (K / sv);
+        sb1 = sb0 + (size_t)8 * (K / sv);
+    }
+    const int mxa = (FMT == MOE_FMT_MXFP4) ? 112 + PA.mx_off[e] : 0;
+    const int mxb = (FMT == MOE_FMT_MXFP4 && MODE == MODE_GATEUP) ? 112 + PB.mx_off[e] : 0;
+    const float postA = PA.post[e];
+    const float postB = (MODE == MODE_GATEUP) ? PB.post[e] : 1.f;
+    const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
+    const int P = L.T * L.k;
+    const int steps = K / 128;
+
+    for (int c0 = 0; c0 < cnt; c0 += 8 * NT) {
+        // B operand rows (one column per lane group g)
+        const __half* brow[NT];
+        bool bval[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = c0 + nt * 8 + g;
+            bval[nt] = col < cnt;
+            const int cc = bval[nt] ? col : 0;
+            if (MODE == MODE_GATEUP) {
+                const int tok = shared ? cc : L.sorted_pair[row0 + cc] / L.k;
+                brow[nt] = L.x16 + (size_t)tok * L.H + 32 * q;
+            } else {
+                const int r = shared ? P + cc : row0 + cc;
+                brow[nt] = L.h16 + (size_t)r * Imax + 32 * q;
+            }
+        }
+        float accA[NT][4], accB[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { accA[nt][i] = 0.f; accB[nt][i] = 0.f; }
+
+        ChunkA ca, cb;
+        load_chunk<FMT>(ca, pa0, pa1, sa0, sa1, 0, q, mxa);
+        if (MODE == MODE_GATEUP) load_chunk<FMT>(cb, pb0, pb1, sb0, sb1, 0, q, mxb);
+        for (int s = 0; s < steps; ++s) {
+            ChunkA na = ca, nb = cb;
+            if (s + 1 < steps) {
+                load_chunk<FMT>(na, pa0, pa1, sa0, sa1, s + 1, q, mxa);
+                if (MODE == MODE_GATEUP) load_chunk<FMT>(nb, pb0, pb1, sb0, sb1, s + 1, q, mxb);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (c0 + nt * 8 >= cnt) break;  // warp-uniform
+                uint4 b[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    b[j] = bval[nt] ? ldg_cached128(brow[nt] + s * 128 + 8 * j)
+                                    : make_uint4(0, 0, 0, 0);
+#define MOE_STEP(I)                                                                   \
+    {                                                                                 \
+        uint32_t fa[4];                                                               \
+        frag_a<I>(ca, fa);                                                            \
+        const uint32_t b0 = word_of(b[I >> 1], (I & 1) * 2);                          \
+        const uint32_t b1 = word_of(b[I >> 1], (I & 1) * 2 + 1);                      \
+        mma_f16_16816(accA[nt], fa[0], fa[1], fa[2], fa[3], b0, b1);                  \
+        if (MODE == MODE_GATEUP) {                                                    \
+            uint32_t fb[4];                                                           \
+            frag_a<I>(cb, fb);                                                        \
+            mma_f16_16816(accB[nt], fb[0], fb[1], fb[2], fb[3], b0, b1);              \
+        }                                                                             \
+    }
+                MOE_STEP(0) MOE_STEP(1) MOE_STEP(2) MOE_STEP(3)
+                MOE_STEP(4) MOE_STEP(5) MOE_STEP(6) MOE_STEP(7)
+#undef MOE_STEP
+            }
+            ca = na;
+            cb = nb;
+        }
+
+        // ---- epilogue ----
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            if (c0 + nt * 8 >= cnt) break;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = c0 + nt * 8 + 2 * q + j;
+                const bool valid = col < cnt;
+                const int r = shared ? P + col : row0 + col;
+                if (MODE == MODE_GATEUP) {
+                    const float h0 = silu_f32(accA[nt][j] * postA) * (accB[nt][j] * postB);
+                    const float h1 = silu_f32(accA[nt][2 + j] * postA) * (accB[nt][2 + j] * postB);
+                    if (L.act == MOE_ACT_NVFP4) {
+                        // quantize h over the 16 consecutive rows n0..n0+15 of this column
+                        float amax = fmaxf(fabsf(h0), fabsf(h1));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+                        float qs = amax / 6.0f;
+                        qs = qs / L.g2;
+                        const uint32_t sbyte = f32_to_e4m3(qs);
+                        const float denom = e4m3_to_f32(sbyte) * L.g2;
+                        uint32_t c0b = 0, c1b = 0;
+                        if (denom != 0.f) {
+                            c0b = f32x2_to_e2m1x2(h0 / denom, 0.f) & 0xF;
+                            c1b = f32x2_to_e2m1x2(h1 / denom, 0.f) & 0xF;
+                        }
+                        const uint32_t n0c = __shfl_down_sync(0xffffffffu, c0b, 4);
+                        const uint32_t n1c = __shfl_down_sync(0xffffffffu, c1b, 4);
+                        if (valid) {
+                            __half* hrow = L.h16 + (size_t)r * Imax + n0;
+                            hrow[g] = __float2half_rn(e2m1_to_f32(c0b) * denom);
+                            hrow[g + 8] = __float2half_rn(e2m1_to_f32(c1b) * denom);
+                            uint8_t* qrow = L.hq + (size_t)r * (Imax / 2) + n0 / 2;
+                            if ((g & 1) == 0) {
+                                qrow[g / 2] = (uint8_t)(c0b | (n0c << 4));
+                                qrow[(g + 8) / 2] = (uint8_t)(c1b | (n1c << 4));
+                            }
+                            if (g == 0) L.hs[(size_t)r * (Imax / 16) + n0 / 16] = (uint8_t)sbyte;
+                        }
+                    } else if (valid) {
+                        __half* hrow = L.h16 + (size_t)r * Imax + n0;
+                        hrow[g] = __float2half_rn(h0);
+                        hrow[g + 8] = __float2half_rn(h1);
+                    }
+                } else if (valid) {
+                    const float wcol = shared ? 1.f : L.w[L.sorted_pair[row0 + col]];
+                    float* yrow = L.y + (size_t)r * L.H + n0;
+                    yrow[g] = accA[nt][j] * postA * wcol;
+                    yrow[g + 8] = accA[nt][2 + j] * postA * wcol;
+                }
+            }
+        }
+    }
+}
+
+template <int MODE, int NT, int WARPS, int FMT_R, int FMT_S>
+__global__ void __launch_bounds__(WARPS * 32)
+expert_mma_kernel(FfnLaunch L, int max_routed_slots) {
+    const int slot = blockIdx.y;
+    const bool shared = slot == max_routed_slots;
+    int e, row0, cnt;
+    if (shared) {
+        e = 0;
+        row0 = 0;
+        cnt = L.T;
+    } else {
+        if (slot >= L.meta[0]) return;
+        e = L.active[slot];
+        row0 = L.offsets[e];
+        cnt = L.offsets[e + 1] - row0;
+    }
+    const int Iexp = shared ? L.I_shared : L.I;
+    const int N = MODE == MODE_GATEUP ? Iexp : L.H;
+    const int K = MODE == MODE_GATEUP ? L.H : Iexp;
+    const int n0 = (blockIdx.x * WARPS + (threadIdx.x >> 5)) * 16;
+    if (n0 >= N) return;
+    if (shared) expert_rows<MODE, NT, FMT_S>(L, true, e, row0, cnt, N, K, n0);
+    else expert_rows<MODE, NT, FMT_R>(L, false, e, row0, cnt, N, K, n0);
+}
+
+// ------------------------------------------------------------------------------------------
+// Combine: out[t] = sum_j y[pos(t,j)] + y[shared row t], fixed j order, bf16 output.
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(FfnLaunch L) {
+    const int H8 = L.H / 8;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)L.T * H8) return;
+    const int t = (int)(idx / H8), c = (int)(idx - (int64_t)t * H8);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    auto add_row = [&](int r) {
+        const float4* src = reinterpret_cast<const float4*>(L.y + (size_t)r * L.H + c * 8);
+        const float4 a = src[0], b = src[1];
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    };
+    for (int j = 0; j < L.k; ++j) {
+        const int pos = L.pos_of_pair[t * L.k + j];
+        if (pos >= 0) add_row(pos);
+    }
+    if (L.I_shared > 0) add_row(L.T * L.k + t);
+    uint4 o;
+    __nv_bfloat162 v;
+    v = __floats2bfloat162_rn(acc[0], acc[1]); o.x = *reinterpret_cast<uint32_t*>(&v);
+    v = __floats2bfloat162_rn(acc[2], acc[3]); o.y = *reinterpret_cast<uint32_t*>(&v);
+    v = __floats2bfloat162_rn(acc[4], acc[5]); o.z = *reinterpret_cast<uint32_t*>(&v);
+    v = __floats2bfloat162_rn(acc[6], acc[7]); o.w = *reinterpret_cast<uint32_t*>(&v);
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(L.out) + (size_t)t * L.H)[c] = o;
+}
+
+// ------------------------------------------------------------------------------------------
+__global__ void quantize_act_kernel(const __nv_bfloat16* __restrict__ x, int64_t n16, float g,
+                                    uint8_t* __restrict__ packed, uint8_t* __restrict__ scales,
+                                    __half* deq16) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n16) return;
+    float v[16];
+    load_bf16x16(x + i * 16, v);
+    quant16(v, g, packed + i * 8, scales + i, deq16 ? deq16 + i * 16 : nullptr);
+}
+
+__global__ void mx_offsets_kernel(const uint8_t* __restrict__ scales, int64_t per_expert,
+                                  int32_t* __restrict__ off, float* __restrict__ post) {
+    const int e = blockIdx.x;
+    const uint8_t* s = scales + (size_t)e * per_expert;
+    int m = 0;
+    for (int64_t i = threadIdx.x; i < per_expert; i += blockDim.x) m = max(m, (int)s[i]);
+    __shared__ int red[32];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int mm = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) mm = max(mm, red[w]);
+        if (mm == 255) mm = 254;  // 0xFF is NaN in E8M0; never produced by an encoder
+        // f16 scale = 2^(byte - 127 - o) with o = max - 139: the largest block scale maps to
+        // 2^12, so 6 * scale stays below the f16 maximum; post = 2^o restores the magnitude.
+        const int o = mm - 139;
+        off[e] = o;
+        post[e] = ldexpf(1.0f, o);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Records a timing event on `st`; inside stream capture it becomes an event-record node.
+static cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
+    if (!ev) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t err = cudaStreamIsCapturing(st, &cs);
+    if (err != cudaSuccess) return err;
+    return cs == cudaStreamCaptureStatusActive
+               ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+               : cudaEventRecord(ev, st);
+}
+
+template <int MODE, int NT, int FR, int FS>
+static void launch_expert_gemm(const FfnLaunch& L, int slots_r, cudaStream_t st) {
+    constexpr int WARPS = 4;
+    const int slots = slots_r + (L.I_shared > 0 ? 1 : 0);
+    const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
+    const int N = MODE == MODE_GATEUP ? Imax : L.H;
+    dim3 grid((N / 16 + WARPS - 1) / WARPS, slots);
+    expert_mma_kernel<MODE, NT, WARPS, FR, FS><<<grid, WARPS * 32, 0, st>>>(L, slots_r);
+}
+
+template <int MODE, int NT>
+static void launch_expert_gemm_fmt(const FfnLaunch& L, int slots_r, cudaStream_t st) {
+    const int fr = L.gate.fmt;
+    const int fs = L.I_shared > 0 ? L.sh_gate.fmt : fr;
+    if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_NVFP4)
+        launch_expert_gemm<MODE, NT, MOE_FMT_NVFP4, MOE_FMT_NVFP4>(L, slots_r, st);
+    else if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_MXFP4)
+        launch_expert_gemm<MODE, NT, MOE_FMT_NVFP4, MOE_FMT_MXFP4>(L, slots_r, st);
+    else if (fr == MOE_FMT_MXFP4 && fs == MOE_FMT_NVFP4)
+        launch_expert_gemm<MODE, NT, MOE_FMT_MXFP4, MOE_FMT_NVFP4>(L, slots_r, st);
+    else
+        launch_expert_gemm<MODE, NT, MOE_FMT_MXFP4, MOE_FMT_MXFP4>(L, slots_r, st);
+}
+
+template <int MODE>
+static void launch_expert_phase(const FfnLaunch& L, int slots_r, cudaStream_t st) {
+    if (L.T <= 8) launch_expert_gemm_fmt<MODE, 1>(L, slots_r, st);
+    else launch_expert_gemm_fmt<MODE, 4>(L, slots_r, st);
+}
+
+cudaError_t launch_ffn(const FfnLaunch& L, cudaStream_t st, const PhaseEvents* ev) {
+    cudaError_t err = cudaSuccess;
+#define MOE_PHASE(i, body)                                                  \
+    if (ev && (err = record_event(ev->begin[i], st)) != cudaSuccess) return err; \
+    body;                                                                  \
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;             \
+    if (ev && (err = record_event(ev->end[i], st)) != cudaSuccess) return err;
+    const int64_t n16 = (int64_t)L.T * L.H / 16;
+    int conv_blocks = (int)((n16 + 511) / 512);
+    if (conv_blocks > 4 * 152) conv_blocks = 4 * 152;
+    if (conv_blocks < 1) conv_blocks = 1;
+    const int slots_r = L.E < L.T * L.k ? L.E : L.T * L.k;
+    const int64_t nthreads = (int64_t)L.T * (L.H / 8);
+    MOE_PHASE(0, (prep_kernel<<<1 + conv_blocks, 512, 0, st>>>(L)))
+    MOE_PHASE(1, launch_expert_phase<MODE_GATEUP>(L, slots_r, st))
+    MOE_PHASE(2, launch_expert_phase<MODE_DOWN>(L, slots_r, st))
+    MOE_PHASE(3, (combine_kernel<<<(unsigned)((nthreads + 255) / 256), 256, 0, st>>>(L)))
+#undef MOE_PHASE
+    return cudaSuccess;
+}
+
+cudaError_t launch_quantize_act(const void* x, int64_t rows, int64_t K, float g, uint8_t* packed,
+                                uint8_t* scales, __half* deq16, cudaStream_t st) {
+    const int64_t n16 = rows * K / 16;
+    quantize_act_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), n16, g, packed, scales, deq16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mx_offsets(const uint8_t* scales, int E, int64_t per_expert, int32_t* off,
+                              float* post, cudaStream_t st) {
+    mx_offsets_kernel<<<E, 256, 0, st>>>(scales, per_expert, off, post);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,238 @@
+// route.cu -- router GEMM (bf16 x bf16 -> fp32 logits) and the top-K routing kernels.
+//
+// Routing kinds (spark_model MoE pages):
+//   softmax top-K           -- moe/init.rs, the `moe_topk_softmax` handles;
+//   sigmoid + correction bias (selection on sigmoid+bias, weights from the unbiased sigmoid,
+//     renormalised and scaled) -- moe/mod.rs, `correction_bias_dev` field doc;
+//   static hash routing through tid2eid [vocab, top_k] -- moe/init.rs, `new_with_hash` doc.
+// The router keeps fp32 logits (moe/mod.rs, `dense_gemm_f32out` field doc: an fp32-output
+// router GEMM feeding an fp32-input top-K).  Ids and weights stay on the device.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------------------------------
+// Router logits: logits[t][e] = sum_h x[t][h] * Wr[e][h].
+// One CTA computes 16 experts x (8*NT) tokens; its KSPLIT warps split H and reduce through
+// shared memory.  Each warp runs bf16 m16n8k16 MMAs with fp32 accumulation.  Within a warp
+// the K order of the fragments is permuted so that every lane reads 16 contiguous bytes of
+// its expert row and of its token row per 32-element step (both operands use the same
+// permutation, so the dot product is unchanged).
+// ------------------------------------------------------------------------------------------
+template <int NT, int KSPLIT>
+__global__ void __launch_bounds__(KSPLIT * 32)
+router_logits_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wr,
+                     float* __restrict__ logits, int T, int E, int H) {
+    __shared__ float red[KSPLIT][NT * 4][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int e0 = blockIdx.x * 16;
+    const int t0 = blockIdx.y * 8 * NT;
+    const int steps = H / 32;                       // 32 K-elements per warp step
+    const int per = (steps + KSPLIT - 1) / KSPLIT;
+    const int s_begin = warp * per;
+    const int s_end = min(steps, s_begin + per);
+
+    const int ea = e0 + g, eb = e0 + g + 8;
+    const bool va = ea < E, vb = eb < E;
+    const __nv_bfloat16* wa = wr + (size_t)(va ? ea : 0) * H + 8 * q;
+    const __nv_bfloat16* wb = wr + (size_t)(vb ? eb : 0) * H + 8 * q;
+    const __nv_bfloat16* xp[NT];
+    bool vt[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int t = t0 + nt * 8 + g;
+        vt[nt] = t < T;
+        xp[nt] = x + (size_t)(vt[nt] ? t : 0) * H + 8 * q;
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+
+    for (int s = s_begin; s < s_end; ++s) {
+        const int kofs = s * 32;
+        uint4 A0 = va ? ldg_stream128(wa + kofs) : make_uint4(0, 0, 0, 0);
+        uint4 A1 = vb ? ldg_stream128(wb + kofs) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            uint4 B = vt[nt] ? ldg_cached128(xp[nt] + kofs) : make_uint4(0, 0, 0, 0);
+            mma_bf16_16816(acc[nt], A0.x, A1.x, A0.y, A1.y, B.x, B.y);
+            mma_bf16_16816(acc[nt], A0.z, A1.z, A0.w, A1.w, B.z, B.w);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) red[warp][nt * 4 + i][lane] = acc[nt][i];
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < NT * 4 * 32; idx += blockDim.x) {
+        const int slot = idx >> 5, ln = idx & 31;
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < KSPLIT; ++w) sum += red[w][slot][ln];
+        const int nt = slot >> 2, i = slot & 3;
+        const int gg = ln >> 2, qq = ln & 3;
+        const int e = e0 + gg + ((i & 2) ? 8 : 0);
+        const int t = t0 + nt * 8 + 2 * qq + (i & 1);
+        if (e < E && t < T) logits[(size_t)t * E + e] = sum;
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Top-K over fp32 logits: one warp per token.  Lane l holds experts l, l+32, ...  K rounds
+// of a warp arg-max on (score, -index) pick the experts in descending score order with ties
+// to the lower index.  Non-finite logits rank below every finite score and get weight 0.
+// ------------------------------------------------------------------------------------------
+constexpr int kEPL = kMaxExperts / 32;  // experts per lane (max)
+
+__global__ void __launch_bounds__(128)
+topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
+            int k, int scoring, int renorm, float scaling, int32_t* __restrict__ ids,
+            float* __restrict__ wout, int32_t* __restrict__ status) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 4 + warp;
+    if (t >= T) return;
+    const float* row = logits + (size_t)t * E;
+    float lg[kEPL], v[kEPL];
+    bool nonfinite = false;
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kEPL; ++j) {
+        const int e = lane + 32 * j;
+        lg[j] = -INFINITY;
+        v[j] = -INFINITY;
+        if (e < E) {
+            const float l = row[e];
+            if (!isfinite(l)) {
+                nonfinite = true;
+            } else {
+                lg[j] = l;
+                lmax = fmaxf(lmax, l);
+                v[j] = (scoring == MOE_SCORE_SOFTMAX) ? l
+                                                      : 1.0f / (1.0f + expf(-l)) + (bias ? bias[e] : 0.f);
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, nonfinite) && lane == 0) status_or(status, MOE_DEV_NONFINITE);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+
+    uint32_t taken = 0;  // bit j: expert lane+32j already selected
+    int my_e = -1;       // lane j < k keeps the j-th selection
+    float my_l = -INFINITY;
+    for (int r = 0; r < k; ++r) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < kEPL; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && !((taken >> j) & 1u)) {
+                if (v[j] > bv || (v[j] == bv && e < be)) { bv = v[j]; be = e; }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        // logit of the winner, fetched from its owner lane
+        float wl = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kEPL; ++j)
+            if (lane + 32 * j == be) wl = lg[j];
+        wl = __shfl_sync(0xffffffffu, wl, be & 31);
+        if (lane == r) { my_e = be; my_l = wl; }
+    }
+    // weights
+    float num = 0.f;
+    if (lane < k && isfinite(my_l)) {
+        num = (scoring == MOE_SCORE_SOFTMAX) ? expf(my_l - lmax) : 1.0f / (1.0f + expf(-my_l));
+    }
+    float den = 0.f;
+    if (renorm) {
+        den = num;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    } else if (scoring == MOE_SCORE_SOFTMAX) {
+        float z = 0.f;
+#pragma unroll
+        for (int j = 0; j < kEPL; ++j)
+            if (isfinite(lg[j])) z += expf(lg[j] - lmax);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        den = z;
+    } else {
+        den = 1.f;
+    }
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = my_e;
+        wout[(size_t)t * k + lane] = (den > 0.f ? num / den : 0.f) * scaling;
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Hash routing: ids = tid2eid[token_ids[t]] (table order), weight = scaling / k.
+// ------------------------------------------------------------------------------------------
+__global__ void hash_route_kernel(const int64_t* __restrict__ tid2eid,
+                                  const int32_t* __restrict__ token_ids, int64_t vocab, int T,
+                                  int E, int k, float scaling, int32_t* __restrict__ ids,
+                                  float* __restrict__ wout, int32_t* __restrict__ status) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= T * k) return;
+    const int t = idx / k, j = idx - t * k;
+    const int64_t tok = token_ids[t];
+    int32_t e = -1;
+    float w = 0.f;
+    if (tok < 0 || tok >= vocab) {
+        status_or(status, MOE_DEV_BAD_TOKEN_ID);
+    } else {
+        const int64_t te = tid2eid[tok * k + j];
+        if (te < 0 || te >= E) {
+            status_or(status, MOE_DEV_BAD_EXPERT_ID);
+        } else {
+            e = (int32_t)te;
+            w = scaling / (float)k;
+        }
+    }
+    ids[idx] = e;
+    wout[idx] = w;
+}
+
+// ------------------------------------------------------------------------------------------
+cudaError_t launch_router_logits(const void* x, const void* wr, float* logits, int T, int E,
+                                 int H, cudaStream_t st) {
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    const auto* wb = static_cast<const __nv_bfloat16*>(wr);
+    if (T <= 8) {
+        dim3 grid((E + 15) / 16, (T + 7) / 8);
+        router_logits_kernel<1, 16><<<grid, 16 * 32, 0, st>>>(xb, wb, logits, T, E, H);
+    } else {
+        dim3 grid((E + 15) / 16, (T + 31) / 32);
+        router_logits_kernel<4, 8><<<grid, 8 * 32, 0, st>>>(xb, wb, logits, T, E, H);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int scoring,
+                        int renorm, float scaling, int32_t* ids, float* w, int32_t* status,
+                        cudaStream_t st) {
+    topk_kernel<<<(T + 3) / 4, 128, 0, st>>>(logits, bias, T, E, k, scoring, renorm, scaling,
+                                             ids, w, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_hash_route(const int64_t* tid2eid, const int32_t* token_ids, int64_t vocab,
+                              int T, int E, int k, float scaling, int32_t* ids, float* w,
+                              int32_t* status, cudaStream_t st) {
+    const int n = T * k;
+    hash_route_kernel<<<(n + 255) / 256, 256, 0, st>>>(tid2eid, token_ids, vocab, T, E, k,
+                                                        scaling, ids, w, status);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,164 @@
+/* moe.h -- C ABI of the GB300 (sm_103a) MoE FFN block library (libmoe_gb300.so).
+ *
+ * The library computes the Mixture-of-Experts FFN block of an LLM serving engine:
+ *   router GEMM -> top-K routing (softmax, sigmoid + correction bias, or a static hash
+ *   table) -> per-expert token dispatch -> block-quantized expert FFN
+ *   (gate+up projection, SiLU(gate)*up, down projection) -> top-K weighted sum plus an
+ *   optional shared expert.
+ * Sources: the spark_model MoE pages -- moe/mod.rs (module doc: two fused expert launches,
+ * routing ids and weights stay on the device with no device-to-host synchronisation; the
+ * `MoeLayer` field docs for the weight formats, the correction bias and the tid2eid table)
+ * and moe/init.rs (`MoeLayer::new_with_hash`: argument checks at construction).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers marked [device] must point to device memory of the current CUDA device;
+ *     pointers marked [host] to host memory.  The caller owns every buffer it passes.
+ *     The library owns only the prepared-weights handle and the buffers behind it.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Every call is asynchronous on that stream: no host synchronisation, no device-to-host
+ *     copy and no memory allocation happen inside moe_route / moe_ffn_forward /
+ *     moe_quantize_act_nvfp4.
+ *   - Errors detectable on the host return a nonzero moe_status_t BEFORE anything is
+ *     launched.  A failed launch returns MOE_ERR_CUDA.  Problems found in the data on the
+ *     device are OR-ed into the caller's int32 device status word (MOE_DEV_* bits); the
+ *     kernels then skip or zero the affected work instead of trapping.
+ *   - Layouts are row-major.  Block-quantized tensors are stacked over experts:
+ *       packed  [E][N][K/2] uint8 -- E2M1 codes, element 2i in the LOW nibble of byte i,
+ *                                   bit 3 of a code is its sign;
+ *       scales  [E][N][K/16] uint8 FP8-E4M3 (NVFP4) or [E][N][K/32] uint8 E8M0 (MXFP4);
+ *       globals [E] float32 per-tensor global (NVFP4, multiplies) or NULL (MXFP4).
+ *     Value of element (e, n, k) = e2m1(code) * scale(e, n, k / block) * global(e).
+ *     gate and up have N = I, K = H; down has N = H, K = I.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* a size, pointer or enum is out of its documented range  */
+    MOE_ERR_UNSUPPORTED = 2,   /* a valid combination this build does not implement       */
+    MOE_ERR_CUDA = 3,          /* a CUDA runtime call or a kernel launch failed            */
+    MOE_ERR_WORKSPACE = 4      /* the workspace passed is smaller than moe_workspace_size */
+} moe_status_t;
+
+/* Bits of the caller-owned int32 device status word (atomically OR-ed by the kernels). */
+#define MOE_DEV_BAD_EXPERT_ID 0x1 /* a tid2eid entry outside [0,E): that pair is dropped     */
+#define MOE_DEV_BAD_TOKEN_ID 0x2  /* a token id outside [0,vocab): the token's pairs dropped */
+#define MOE_DEV_NONFINITE 0x4     /* a NaN/Inf router logit: ranked below every finite one   */
+#define MOE_DEV_TIMEOUT 0x8       /* a bounded device-side wait gave up                      */
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1, MOE_SCORE_HASH = 2 } moe_scoring_t;
+typedef enum { MOE_FMT_NVFP4 = 0, MOE_FMT_MXFP4 = 1 } moe_fmt_t;
+/* Activation precision of the expert GEMMs.  BF16: W4A16 (bf16 tokens, dequantized
+ * weights).  NVFP4: W4A4 -- tokens and the intermediate h are quantized to NVFP4 (per 16
+ * elements, E4M3 scale, static power-of-two f32 global) before the block-scaled FP4 MMA. */
+typedef enum { MOE_ACT_BF16 = 0, MOE_ACT_NVFP4 = 1 } moe_act_t;
+
+/* One block-quantized projection, stacked over experts (layout in the header comment). */
+typedef struct {
+    const void* packed;    /* [device] uint8 [E][N][K/2]                                  */
+    const void* scales;    /* [device] uint8 [E][N][K/16] (NVFP4) or [E][N][K/32] (MXFP4) */
+    const float* globals;  /* [device] float [E] (NVFP4) or NULL (MXFP4)                   */
+    int32_t fmt;           /* moe_fmt_t                                                     */
+} moe_qtensor;
+
+/* The expert weights of one MoE layer.  Constraints (checked): 1 <= E <= 512;
+ * H, I, I_shared multiples of 128; I_shared == 0 means no shared expert.
+ * A shared expert is one expert (E = 1 in its tensors) added with weight 1. */
+typedef struct {
+    int32_t E, H, I, top_k, I_shared;
+    moe_qtensor gate, up, down;
+    moe_qtensor sh_gate, sh_up, sh_down;
+} moe_ffn_desc;
+
+/* Routing of T tokens.  Constraints (checked): 1 <= E <= 512, 1 <= top_k <= min(E, 32);
+ * softmax/sigmoid: H a multiple of 32 when the router GEMM runs;
+ * hash: tid2eid and token_ids non-NULL, vocab >= 1. */
+typedef struct {
+    int32_t T, E, H, top_k;
+    int32_t scoring;           /* moe_scoring_t                                            */
+    int32_t renormalize;       /* 1: weights renormalised over the selected experts        */
+    float routed_scaling;      /* multiplies every routing weight (1.0 for plain top-K)    */
+    const void* w_router;      /* [device] bf16 [E][H], or NULL when logits are supplied   */
+    const float* correction_bias; /* [device] float [E] (sigmoid selection only) or NULL  */
+    const int64_t* tid2eid;    /* [device] int64 [vocab][top_k] (hash only)               */
+    int64_t vocab;
+    const int32_t* token_ids;  /* [device] int32 [T] (hash only)                          */
+} moe_route_desc;
+
+/* Router GEMM + top-K.
+ *   Softmax: p = softmax(logits) over all E; the top_k largest are selected; weight =
+ *     p / sum(selected p) when renormalize, else p; times routed_scaling.
+ *   Sigmoid: s = sigmoid(logits); selection ranks s + correction_bias; weight = s /
+ *     sum(selected s) when renormalize, else s; times routed_scaling.  (moe/mod.rs,
+ *     `correction_bias_dev` field doc.)
+ *   Hash: ids = tid2eid[token_ids[t]] in table order; weight = routed_scaling / top_k.
+ *     (moe/init.rs, `new_with_hash` doc.)
+ * Ids are written in descending selection-score order, ties to the lower expert index.
+ * x_bf16      [device] bf16 [T][H]; used when w_router != NULL.
+ * logits_in   [device] float [T][E] or NULL: precomputed router logits (then w_router and
+ *             x_bf16 are ignored).
+ * logits_out  [device] float [T][E]; required when the router GEMM runs, else may be NULL.
+ * topk_ids    [device] int32 [T][top_k]; -1 marks a dropped pair.
+ * topk_w      [device] float [T][top_k].
+ * dev_status  [device] int32 [1]; bits are OR-ed in, never cleared by the library.
+ * T == 0 is a valid no-op. */
+moe_status_t moe_route(const moe_route_desc* desc, const void* x_bf16, const float* logits_in,
+                       float* logits_out, int32_t* topk_ids, float* topk_w, int32_t* dev_status,
+                       void* stream);
+
+/* Bytes of device workspace moe_ffn_forward needs for T tokens in activation mode act. */
+moe_status_t moe_workspace_size(const moe_ffn_desc* desc, int32_t T, int32_t act, size_t* bytes);
+
+/* One-time weight preparation: validates the descriptor, derives per-tensor post-scales
+ * (the NVFP4 globals; for MXFP4 a power-of-two exponent offset) and the scale-factor
+ * tiles of the FP4 tensor-core path.  The weight buffers must stay alive and unchanged until
+ * moe_release_weights.  Allocates device memory and synchronises `stream` before returning. */
+moe_status_t moe_prepare_weights(const moe_ffn_desc* desc, void** handle_out, void* stream);
+moe_status_t moe_release_weights(void* handle);
+
+/* Expert FFN + weighted combine:
+ *   out[t] = sum_j topk_w[t][j] * FFN_{topk_ids[t][j]}(x[t]) + FFN_shared(x[t]),
+ *   FFN_e(a) = W_down,e (SiLU(W_gate,e a) * (W_up,e a)).
+ * act = MOE_ACT_NVFP4 quantizes x with global g_act1 and h with global g_act2 (each a
+ * power of two) before the FP4 products; MOE_ACT_BF16 ignores both.
+ * x_bf16 [device] bf16 [T][H]; topk_ids/topk_w as written by moe_route;
+ * out_bf16 [device] bf16 [T][H]; workspace [device], ws_bytes >= moe_workspace_size.
+ * T == 0 is a valid no-op. */
+moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g_act1,
+                             float g_act2, const void* x_bf16, const int32_t* topk_ids,
+                             const float* topk_w, void* out_bf16, void* workspace,
+                             size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* The NVFP4 activation quantizer on its own (the `quantize_bf16_to_nvfp4` step of the
+ * FP4 x FP4 recipe, qwen3_attention/init.rs handle list): per 16 consecutive elements of
+ * each row, s = E4M3(amax / 6 / g) (round to nearest even, saturating), code =
+ * E2M1(v / (e4m3(s) * g)) (round to nearest even, saturating at 6), all-zero codes when s
+ * decodes to 0.  x_bf16 [device] bf16 [rows][K]; packed [device] uint8 [rows][K/2];
+ * scales [device] uint8 [rows][K/16]; K a multiple of 16. */
+moe_status_t moe_quantize_act_nvfp4(const void* x_bf16, int64_t rows, int64_t K, float g,
+                                    uint8_t* packed, uint8_t* scales, void* stream);
+
+/* Kernel timing for benchmarks.  moe_profile_enable(handle, mask) makes the handle record
+ * a pair of CUDA timing events around each kernel phase selected by `mask` in every later
+ * moe_ffn_forward on that handle (as external event nodes when the stream is being captured
+ * into a CUDA graph); mask 0 stops it.  Phases: bit 0 dispatch + activation conversion,
+ * bit 1 gate+up GEMM, bit 2 down GEMM, bit 3 combine.  moe_profile_read waits for the last
+ * recorded end event and writes the duration in milliseconds of each phase's most recent
+ * execution to ms_out[0..3] (-1 for phases not timed).  Not thread-safe per handle. */
+moe_status_t moe_profile_enable(void* handle, uint32_t mask);
+moe_status_t moe_profile_read(void* handle, float* ms_out);
+
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,136 @@
+"""End-to-end GPU parity of the MoE block through the C ABI (moe_route + moe_ffn_forward).
+
+Expert FFN per pair -- gate+up, SiLU(gate)*up, down -- and the top-K weighted sum plus the
+shared expert (spark_model MoE pages, moe/mod.rs module doc), over NVFP4 / MXFP4 weights
+(moe/mod.rs, `experts_scale_kind` doc), with bf16 activations or NVFP4-quantized
+activations (the FP4 x FP4 recipe, moe/mod.rs `moe_fused_gate_up_t_k64_fp4` doc).
+Tolerance: max|gpu - ref| <= 1e-2 * max|ref| + 1e-3 and relative RMS error < 1e-2.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import parity
+from block_quantized_moe_router_gb300 import capi, synth
+from block_quantized_moe_router_gb300.layer import MoeLayer
+
+pytestmark = pytest.mark.gpu
+
+S = synth
+SMALL = {
+    "tiny": S.CONFIGS["tiny"],
+    "tiny_a4": dataclasses.replace(S.CONFIGS["tiny"], name="tiny_a4", act=S.ACT_NVFP4),
+    "ragged": S.MoeConfig("ragged", T=13, H=384, I=256, E=10, k=3, scoring=S.SCORE_SOFTMAX,
+                          I_shared=128),
+    "ragged_a4": S.MoeConfig("ragged_a4", T=13, H=384, I=256, E=10, k=3, scoring=S.SCORE_SOFTMAX,
+                             I_shared=128, act=S.ACT_NVFP4),
+    "mx_routed": S.MoeConfig("mx_routed", T=9, H=256, I=384, E=12, k=4, scoring=S.SCORE_SIGMOID,
+                             scaling=2.5, I_shared=256, fmt=S.FMT_MXFP4, shared_fmt=S.FMT_NVFP4),
+    "mx_shared": S.MoeConfig("mx_shared", T=11, H=256, I=128, E=6, k=2, scoring=S.SCORE_SOFTMAX,
+                             I_shared=384, fmt=S.FMT_NVFP4, shared_fmt=S.FMT_MXFP4),
+    "mx_all_a4": S.MoeConfig("mx_all_a4", T=40, H=512, I=256, E=16, k=4, scoring=S.SCORE_SIGMOID,
+                             scaling=2.5, I_shared=256, fmt=S.FMT_MXFP4, shared_fmt=S.FMT_MXFP4,
+                             act=S.ACT_NVFP4),
+    "many_tokens": S.MoeConfig("many", T=100, H=256, I=256, E=8, k=2, scoring=S.SCORE_SOFTMAX,
+                               I_shared=128),
+    "hash_small": S.MoeConfig("hash_small", T=20, H=256, I=128, E=16, k=3, scoring=S.SCORE_HASH,
+                              I_shared=128, fmt=S.FMT_MXFP4, vocab=100),
+}
+
+
+def _run(cfg, inp):
+    layer = MoeLayer.from_inputs(inp)
+    x = inp["x"].cuda()
+    tok = inp["token_ids"].cuda() if "token_ids" in inp else None
+    ids, w, _ = layer.route(x, token_ids=tok)
+    out = layer.ffn(x, ids, w)
+    torch.cuda.synchronize()
+    status = int(layer.status.item())
+    layer.close()
+    return ids, w, out, status
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_configs(cuda_lib, name):
+    cfg = SMALL[name]
+    inp, _ = parity.make_case(cfg, seed=1, device="cpu")
+    ref_r = parity.oracle_route(cfg, inp)
+    ids, w, out, status = _run(cfg, inp)
+    assert status == 0
+    parity.assert_routing(cfg, ref_r, ids, w)
+    ref = parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"])
+    parity.assert_close(out, ref, name)
+
+
+FULL = {
+    "dec1": (S.CONFIGS["dec1"], None),
+    "dec8": (S.CONFIGS["dec8"], None),
+    "hash64": (S.CONFIGS["hash64"], [0, 1, 17, 38, 62, 63]),
+    "pre4096": (S.CONFIGS["pre4096"], [0, 1, 2047, 4095]),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_configs(cuda_lib, name):
+    cfg, sample = FULL[name]
+    inp, _ = parity.make_case(cfg, seed=0, device="cuda")
+    ref_r = parity.oracle_route(cfg, inp)
+    ids, w, out, status = _run(cfg, inp)
+    assert status == 0
+    parity.assert_routing(cfg, ref_r, ids, w)
+    ref = parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"], tokens=sample)
+    got = out if sample is None else out[sample]
+    parity.assert_close(got, ref, name)
+    # every output row is finite and the unsampled rows are not left untouched
+    assert torch.isfinite(out.float()).all()
+    assert (out.float().abs().amax(1) > 0).all()
+
+
+def test_dropped_pairs_and_zero_tokens(cuda_lib):
+    cfg = SMALL["hash_small"]
+    inp, _ = parity.make_case(cfg, seed=2, device="cpu")
+    tab = inp["tid2eid"].clone()
+    tok = inp["token_ids"]
+    tab[int(tok[3]), 1] = 99     # bad id: that pair is dropped
+    inp["tid2eid"] = tab
+    ref_r = parity.oracle_route(cfg, inp)
+    ids, w, out, status = _run(cfg, inp)
+    assert status == capi.MOE_DEV_BAD_EXPERT_ID
+    parity.assert_routing(cfg, ref_r, ids, w)
+    parity.assert_close(out, parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"]), "dropped")
+    # T == 0 is a no-op through both entry points
+    layer = MoeLayer.from_inputs(inp)
+    x0 = torch.zeros((0, cfg.H), dtype=torch.bfloat16, device="cuda")
+    out0 = layer.ffn(x0, torch.zeros((0, cfg.k), dtype=torch.int32, device="cuda"),
+                     torch.zeros((0, cfg.k), device="cuda"))
+    torch.cuda.synchronize()
+    assert out0.shape == (0, cfg.H)
+    layer.close()
+
+
+def test_quantizer_matches_oracle(cuda_lib):
+    import oracle
+    rng = np.random.default_rng(0)
+    rows, K = 64, 512
+    v = rng.standard_normal((rows, K)).astype(np.float32) * rng.uniform(1e-4, 300, (rows, 1)).astype(np.float32)
+    v[3, :16] = 0.0                               # all-zero block
+    v[4, :16] = [3, -1.5, 0.75, 0.25, 6, 5, -3.5, 0, 1.25, -2.5, 0.5, 1.75, -6, 2, 4, -0.1]
+    xb = torch.from_numpy(v).to(torch.bfloat16)
+    vb = xb.float().numpy()
+    for g in (1.0, 0.25, 8.0):
+        packed = torch.zeros((rows, K // 2), dtype=torch.uint8, device="cuda")
+        scales = torch.zeros((rows, K // 16), dtype=torch.uint8, device="cuda")
+        capi.moe_quantize_act_nvfp4(xb.cuda(), g, packed, scales)
+        torch.cuda.synchronize()
+        p_ref, s_ref, d_ref = oracle.quant_nvfp4(vb, g)
+        assert np.array_equal(scales.cpu().numpy(), s_ref)
+        # compare decoded values (a code of -0 and +0 decode alike)
+        d_gpu = oracle.dequant(packed.cpu().numpy(), scales.cpu().numpy(), g, 0)
+        assert np.array_equal(d_gpu, d_ref)
+        # and the raw nibbles wherever the value is nonzero
+        nz = d_ref != 0
+        codes_gpu = np.stack([packed.cpu().numpy() & 15, packed.cpu().numpy() >> 4], -1).reshape(rows, K)
+        codes_ref = np.stack([p_ref & 15, p_ref >> 4], -1).reshape(rows, K)
+        assert np.array_equal(codes_gpu[nz], codes_ref[nz])
