@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ncu DRAM traffic (read + write bytes per launch) of the dominant kernel, keyed by workload,
 # with the hash of the kernel source it was captured on; reported only while the hash matches.
-TRAFFIC = {}
+TRAFFIC = {"dec1": (14213376, "1be2f2ccf2feb1fc")}  # profiles/expert_mma_dec1.md
 
 
 def kernel_source_hash() -> str:
