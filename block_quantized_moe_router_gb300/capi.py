@@ -24,8 +24,8 @@ MOE_ACT_BF16, MOE_ACT_NVFP4 = 0, 1
 
 # Every symbol include/moe.h declares.
 EXPORTED = ["moe_route", "moe_workspace_size", "moe_prepare_weights", "moe_release_weights",
-            "moe_ffn_forward", "moe_quantize_act_nvfp4", "moe_profile_enable", "moe_profile_read",
-            "moe_status_string"]
+            "moe_ffn_forward", "moe_ffn_forward_noalloc", "moe_quantize_act_nvfp4",
+            "moe_profile_enable", "moe_profile_read", "moe_status_string"]
 
 
 class MoeError(RuntimeError):
@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_release_weights.restype = ctypes.c_int
     lib.moe_ffn_forward.argtypes = [vp, i32, i32, f32, f32, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.moe_ffn_forward.restype = ctypes.c_int
+    lib.moe_ffn_forward_noalloc.argtypes = [vp, i32, i32, f32, f32, vp, vp, vp, vp, vp, vp]
+    lib.moe_ffn_forward_noalloc.restype = ctypes.c_int
     lib.moe_quantize_act_nvfp4.argtypes = [vp, i64, i64, f32, vp, vp, vp]
     lib.moe_quantize_act_nvfp4.restype = ctypes.c_int
     lib.moe_profile_enable.argtypes = [vp, ctypes.c_uint32]
@@ -173,6 +175,17 @@ def moe_ffn_forward(handle: int, T: int, act: int, g_act1: float, g_act2: float,
         _dptr(workspace, torch.uint8, "workspace"), workspace.numel(),
         _dptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check(st, "moe_ffn_forward")
+
+
+def moe_ffn_forward_noalloc(handle: int, T: int, act: int, g_act1: float, g_act2: float, x,
+                            topk_ids, topk_w, out, dev_status=None, stream=None):
+    """moe_ffn_forward with the library's static device workspace (no caller allocation)."""
+    st = load_library().moe_ffn_forward_noalloc(
+        ctypes.c_void_p(handle), int(T), int(act), float(g_act1), float(g_act2),
+        _dptr(x, torch.bfloat16, "x"), _dptr(topk_ids, torch.int32, "topk_ids"),
+        _dptr(topk_w, torch.float32, "topk_w"), _dptr(out, torch.bfloat16, "out"),
+        _dptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(st, "moe_ffn_forward_noalloc")
 
 
 def moe_quantize_act_nvfp4(x, g: float, packed, scales, stream=None):

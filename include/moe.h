@@ -146,6 +146,24 @@ moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g
 moe_status_t moe_quantize_act_nvfp4(const void* x_bf16, int64_t rows, int64_t K, float g,
                                     uint8_t* packed, uint8_t* scales, void* stream);
 
+/* moe_ffn_forward without a caller-provided workspace.  The paper has no counterpart: this is
+ * for callers that cannot give the library device memory -- a host that freezes its device
+ * memory plan at start-up and must see no cudaMalloc afterwards (cudaMalloc can synchronise
+ * the device), or a plugin interface that passes tensors but no workspace or allocator.
+ * Same arguments and result as moe_ffn_forward, minus workspace/ws_bytes.  The scratch is a
+ * static 8 MiB device array inside the library (held on every GPU that loads it until the
+ * process exits); a call whose workspace plan (moe_workspace_size) exceeds 8 MiB returns
+ * MOE_ERR_WORKSPACE without launching (8 MiB holds up to 27 tokens at H 7168, I 2048, top-8
+ * with a shared expert).  Allocates nothing.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls on a device share the one array, so calls whose
+ * kernels overlap on the GPU race and must be serialised by the caller; no part of the array
+ * needs clearing between calls. */
+moe_status_t moe_ffn_forward_noalloc(const void* handle, int32_t T, int32_t act, float g_act1,
+                                     float g_act2, const void* x_bf16, const int32_t* topk_ids,
+                                     const float* topk_w, void* out_bf16, int32_t* dev_status,
+                                     void* stream);
+
 /* Kernel timing for benchmarks.  moe_profile_enable(handle, mask) makes the handle record
  * a pair of CUDA timing events around each kernel phase selected by `mask` in every later
  * moe_ffn_forward on that handle (as external event nodes when the stream is being captured
