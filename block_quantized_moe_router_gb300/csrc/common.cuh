@@ -130,11 +130,37 @@ __device__ __forceinline__ void status_or(int32_t* status, int32_t bits) {
     if (status && bits) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch: wait until the preceding kernel on the stream has finished
+// and its writes are visible; allow the next kernel on the stream to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 }  // namespace moe
 
 // ---- host-side launch helpers ----------------------------------------------------------------
 namespace moe {
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Launch with programmatic stream serialization: the kernel may be scheduled while its
+// predecessor on the stream is still running and must call pdl_wait() before reading
+// anything that predecessor writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Workspace carve-up shared by moe_workspace_size and moe_ffn_forward.
 struct Workspace {
@@ -160,7 +186,12 @@ struct Workspace {
         w.x16 = take(sizeof(__half) * (size_t)T * H);
         w.xq = take(act == MOE_ACT_NVFP4 ? (size_t)T * H / 2 : 0);
         w.xs = take(act == MOE_ACT_NVFP4 ? (size_t)T * H / 16 : 0);
-        w.h16 = take(sizeof(__half) * R * Imax);
+        // few-token path: h is token-major per expert slot, [slots][8][Imax]
+        const size_t dec_rows =
+            (T <= 8 && T * top_k <= 64)
+                ? ((size_t)(E < T * top_k ? E : T * top_k) + (I_shared > 0 ? 1 : 0)) * 8
+                : 0;
+        w.h16 = take(sizeof(__half) * (R > dec_rows ? R : dec_rows) * Imax);
         w.hq = take(act == MOE_ACT_NVFP4 ? R * Imax / 2 : 0);
         w.hs = take(act == MOE_ACT_NVFP4 ? R * Imax / 16 : 0);
         w.y = take(sizeof(float) * R * H);

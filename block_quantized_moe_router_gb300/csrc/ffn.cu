@@ -22,6 +22,7 @@
 // launch whatever the number of tokens routed to the expert.  Activations enter as f16
 // (bf16 tokens converted once; the NVFP4-quantized tokens and h are exact in f16).
 #include "common.cuh"
+#include "frag.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -161,57 +162,6 @@ __global__ void __launch_bounds__(512) prep_kernel(FfnLaunch L) {
 // ------------------------------------------------------------------------------------------
 // Grouped expert GEMM on m16n8k16 f16 MMAs.
 // ------------------------------------------------------------------------------------------
-// Block-scale of the 16-byte chunk (32 codes) a lane holds, as f16x2 pairs for the chunk's
-// first and second 16 elements.
-template <int FMT>
-__device__ __forceinline__ void chunk_scales(const uint8_t* srow, int step, int q, int mxbias,
-                                             uint32_t& lo, uint32_t& hi) {
-    if constexpr (FMT == MOE_FMT_NVFP4) {
-        const uint32_t s2 = ldg_u16(srow + step * 8 + 2 * q);
-        const uint32_t h = e4m3x2_to_f16x2(s2);
-        lo = __byte_perm(h, h, 0x1010);
-        hi = __byte_perm(h, h, 0x3232);
-    } else {
-        const int b = (int)ldg_u8(srow + step * 4 + q);
-        const int field = min(30, max(0, b - mxbias));
-        const uint32_t bits = (uint32_t)field << 10;
-        lo = hi = bits | (bits << 16);
-    }
-}
-
-struct ChunkA {
-    uint4 r0, r1;       // packed codes of rows g and g+8
-    uint32_t s0lo, s0hi, s1lo, s1hi;
-};
-
-template <int FMT>
-__device__ __forceinline__ void load_chunk(ChunkA& c, const uint8_t* p0, const uint8_t* p1,
-                                           const uint8_t* s0, const uint8_t* s1, int step, int q,
-                                           int mxbias) {
-    c.r0 = ldg_stream128(p0 + step * 64);
-    c.r1 = ldg_stream128(p1 + step * 64);
-    chunk_scales<FMT>(s0, step, q, mxbias, c.s0lo, c.s0hi);
-    chunk_scales<FMT>(s1, step, q, mxbias, c.s1lo, c.s1hi);
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
-
-// A fragment of MMA step i (0..7) from a chunk: rows g / g+8, k-slots (2q,2q+1) = chunk
-// elements 4i, 4i+1 and k-slots (2q+8, 2q+9) = chunk elements 4i+2, 4i+3.
-template <int I>
-__device__ __forceinline__ void frag_a(const ChunkA& c, uint32_t (&a)[4]) {
-    const uint32_t w0 = word_of(c.r0, I >> 1), w1 = word_of(c.r1, I >> 1);
-    const uint32_t sc0 = (I < 4) ? c.s0lo : c.s0hi;
-    const uint32_t sc1 = (I < 4) ? c.s1lo : c.s1hi;
-    constexpr int SEL = (I & 1) * 2;
-    a[0] = hmul2(e2m1x2_to_f16x2<SEL>(w0), sc0);
-    a[1] = hmul2(e2m1x2_to_f16x2<SEL>(w1), sc1);
-    a[2] = hmul2(e2m1x2_to_f16x2<SEL + 1>(w0), sc0);
-    a[3] = hmul2(e2m1x2_to_f16x2<SEL + 1>(w1), sc1);
-}
-
 template <int MODE, int NT, int FMT>
 __device__ __forceinline__ void expert_rows(const FfnLaunch& L, bool shared, int e, int row0,
                                             int cnt, int N, int K, int n0) {
@@ -500,6 +450,12 @@ cudaError_t launch_ffn(const FfnLaunch& L, cudaStream_t st, const PhaseEvents* e
     if (conv_blocks < 1) conv_blocks = 1;
     const int slots_r = L.E < L.T * L.k ? L.E : L.T * L.k;
     const int64_t nthreads = (int64_t)L.T * (L.H / 8);
+    if (L.T <= 8 && L.T * L.k <= 64 && L.act == MOE_ACT_BF16) {
+        // few tokens: dispatch is rebuilt inside both kernels, combine fused into down
+        MOE_PHASE(1, err = launch_decode_phase(L, 1, st); if (err != cudaSuccess) return err)
+        MOE_PHASE(2, err = launch_decode_phase(L, 2, st); if (err != cudaSuccess) return err)
+        return cudaSuccess;
+    }
     MOE_PHASE(0, (prep_kernel<<<1 + conv_blocks, 512, 0, st>>>(L)))
     MOE_PHASE(1, launch_expert_phase<MODE_GATEUP>(L, slots_r, st))
     MOE_PHASE(2, launch_expert_phase<MODE_DOWN>(L, slots_r, st))

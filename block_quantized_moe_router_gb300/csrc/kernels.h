@@ -54,6 +54,9 @@ struct PhaseEvents {
 
 cudaError_t launch_ffn(const FfnLaunch& L, cudaStream_t st, const PhaseEvents* ev = nullptr);
 
+// Few-token path (T <= 8, bf16 activations): phase 1 = gate+up, phase 2 = down + combine.
+cudaError_t launch_decode_phase(const FfnLaunch& L, int phase, cudaStream_t st);
+
 cudaError_t launch_quantize_act(const void* x, int64_t rows, int64_t K, float g, uint8_t* packed,
                                 uint8_t* scales, __half* deq16, cudaStream_t st);
 

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(KSPLIT * 32)
 router_logits_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wr,
                      float* __restrict__ logits, int T, int E, int H) {
     __shared__ float red[KSPLIT][NT * 4][32];
+    pdl_wait();  // x may come from the preceding kernel
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
     const int e0 = blockIdx.x * 16;
@@ -82,78 +84,79 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* _
 }
 
 // ------------------------------------------------------------------------------------------
-// Top-K over fp32 logits: one warp per token.  Lane l holds experts l, l+32, ...  K rounds
-// of a warp arg-max on (score, -index) pick the experts in descending score order with ties
-// to the lower index.  Non-finite logits rank below every finite score and get weight 0.
+// Top-K over fp32 logits: one warp per token; lane l holds experts l, l+32, ... (EPL of them).
+// Each expert gets a 64-bit key (order-preserving bits of its selection score, then the
+// complemented index), so one warp max per round picks the highest score with ties to the
+// lower index.  Non-finite logits get score -inf and weight 0.
 // ------------------------------------------------------------------------------------------
-constexpr int kEPL = kMaxExperts / 32;  // experts per lane (max)
+__device__ __forceinline__ uint32_t orderable(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
-__global__ void __launch_bounds__(128)
-topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
-            int k, int scoring, int renorm, float scaling, int32_t* __restrict__ ids,
+template <int EPL>
+__global__ void __launch_bounds__(256)
+topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+            int scoring, int renorm, float scaling, int32_t* __restrict__ ids,
             float* __restrict__ wout, int32_t* __restrict__ status) {
+    pdl_wait();  // logits come from the router kernel
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 4 + warp;
+    const int t = blockIdx.x * (blockDim.x >> 5) + warp;
     if (t >= T) return;
     const float* row = logits + (size_t)t * E;
-    float lg[kEPL], v[kEPL];
+    unsigned long long key[EPL];
+    float lg[EPL];
     bool nonfinite = false;
     float lmax = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kEPL; ++j) {
+    for (int j = 0; j < EPL; ++j) {
         const int e = lane + 32 * j;
+        key[j] = 0ull;
         lg[j] = -INFINITY;
-        v[j] = -INFINITY;
         if (e < E) {
             const float l = row[e];
+            float v = -INFINITY;
             if (!isfinite(l)) {
                 nonfinite = true;
             } else {
                 lg[j] = l;
                 lmax = fmaxf(lmax, l);
-                v[j] = (scoring == MOE_SCORE_SOFTMAX) ? l
-                                                      : 1.0f / (1.0f + expf(-l)) + (bias ? bias[e] : 0.f);
+                v = (scoring == MOE_SCORE_SOFTMAX) ? l
+                                                   : 1.0f / (1.0f + expf(-l)) + (bias ? bias[e] : 0.f);
             }
+            key[j] = ((unsigned long long)orderable(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
         }
     }
     if (__any_sync(0xffffffffu, nonfinite) && lane == 0) status_or(status, MOE_DEV_NONFINITE);
 #pragma unroll
     for (int o = 16; o; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
 
-    uint32_t taken = 0;  // bit j: expert lane+32j already selected
-    int my_e = -1;       // lane j < k keeps the j-th selection
-    float my_l = -INFINITY;
+    int my_e = 0;
     for (int r = 0; r < k; ++r) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
+        unsigned long long best = key[0];
 #pragma unroll
-        for (int j = 0; j < kEPL; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && !((taken >> j) & 1u)) {
-                if (v[j] > bv || (v[j] == bv && e < be)) { bv = v[j]; be = e; }
-            }
-        }
+        for (int j = 1; j < EPL; ++j) best = key[j] > best ? key[j] : best;
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+            best = other > best ? other : best;
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        // logit of the winner, fetched from its owner lane
-        float wl = -INFINITY;
+        const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+        if ((e & 31) == lane) {
 #pragma unroll
-        for (int j = 0; j < kEPL; ++j)
-            if (lane + 32 * j == be) wl = lg[j];
-        wl = __shfl_sync(0xffffffffu, wl, be & 31);
-        if (lane == r) { my_e = be; my_l = wl; }
+            for (int j = 0; j < EPL; ++j)
+                if (j == (e >> 5)) key[j] = 0ull;
+        }
+        if (lane == r) my_e = e;
     }
-    // weights
     float num = 0.f;
-    if (lane < k && isfinite(my_l)) {
-        num = (scoring == MOE_SCORE_SOFTMAX) ? expf(my_l - lmax) : 1.0f / (1.0f + expf(-my_l));
+    if (lane < k) {
+        const float l = row[my_e];
+        if (isfinite(l))
+            num = (scoring == MOE_SCORE_SOFTMAX) ? expf(l - lmax) : 1.0f / (1.0f + expf(-l));
     }
-    float den = 0.f;
+    float den = 1.f;
     if (renorm) {
         den = num;
 #pragma unroll
@@ -161,13 +164,11 @@ topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, in
     } else if (scoring == MOE_SCORE_SOFTMAX) {
         float z = 0.f;
 #pragma unroll
-        for (int j = 0; j < kEPL; ++j)
+        for (int j = 0; j < EPL; ++j)
             if (isfinite(lg[j])) z += expf(lg[j] - lmax);
 #pragma unroll
         for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         den = z;
-    } else {
-        den = 1.f;
     }
     if (lane < k) {
         ids[(size_t)t * k + lane] = my_e;
@@ -209,21 +210,30 @@ cudaError_t launch_router_logits(const void* x, const void* wr, float* logits, i
     const auto* xb = static_cast<const __nv_bfloat16*>(x);
     const auto* wb = static_cast<const __nv_bfloat16*>(wr);
     if (T <= 8) {
-        dim3 grid((E + 15) / 16, (T + 7) / 8);
-        router_logits_kernel<1, 16><<<grid, 16 * 32, 0, st>>>(xb, wb, logits, T, E, H);
-    } else {
-        dim3 grid((E + 15) / 16, (T + 31) / 32);
-        router_logits_kernel<4, 8><<<grid, 8 * 32, 0, st>>>(xb, wb, logits, T, E, H);
+        return launch_pdl(router_logits_kernel<1, 16>, dim3((E + 15) / 16, (T + 7) / 8),
+                          dim3(16 * 32), st, xb, wb, logits, T, E, H);
     }
-    return cudaGetLastError();
+    return launch_pdl(router_logits_kernel<4, 8>, dim3((E + 15) / 16, (T + 31) / 32),
+                      dim3(8 * 32), st, xb, wb, logits, T, E, H);
+}
+
+template <int EPL>
+static cudaError_t launch_topk_epl(const float* logits, const float* bias, int T, int E, int k,
+                                   int scoring, int renorm, float scaling, int32_t* ids, float* w,
+                                   int32_t* status, cudaStream_t st) {
+    const int warps = T < 8 ? T : 8;
+    return launch_pdl(topk_kernel<EPL>, dim3((T + warps - 1) / warps), dim3(32 * warps), st,
+                      logits, bias, T, E, k, scoring, renorm, scaling, ids, w, status);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int scoring,
                         int renorm, float scaling, int32_t* ids, float* w, int32_t* status,
                         cudaStream_t st) {
-    topk_kernel<<<(T + 3) / 4, 128, 0, st>>>(logits, bias, T, E, k, scoring, renorm, scaling,
-                                             ids, w, status);
-    return cudaGetLastError();
+    if (E <= 32) return launch_topk_epl<1>(logits, bias, T, E, k, scoring, renorm, scaling, ids, w, status, st);
+    if (E <= 64) return launch_topk_epl<2>(logits, bias, T, E, k, scoring, renorm, scaling, ids, w, status, st);
+    if (E <= 128) return launch_topk_epl<4>(logits, bias, T, E, k, scoring, renorm, scaling, ids, w, status, st);
+    if (E <= 256) return launch_topk_epl<8>(logits, bias, T, E, k, scoring, renorm, scaling, ids, w, status, st);
+    return launch_topk_epl<16>(logits, bias, T, E, k, scoring, renorm, scaling, ids, w, status, st);
 }
 
 cudaError_t launch_hash_route(const int64_t* tid2eid, const int32_t* token_ids, int64_t vocab,

@@ -37,6 +37,18 @@ SMALL = {
                                I_shared=128),
     "hash_small": S.MoeConfig("hash_small", T=20, H=256, I=128, E=16, k=3, scoring=S.SCORE_HASH,
                               I_shared=128, fmt=S.FMT_MXFP4, vocab=100),
+    # few-token path (T <= 8, bf16 activations): fused dispatch, split-K gate+up, down+combine
+    "dec_ragged": S.MoeConfig("dec_ragged", T=7, H=384, I=256, E=10, k=3, scoring=S.SCORE_SOFTMAX,
+                              I_shared=384),
+    "dec_mx": S.MoeConfig("dec_mx", T=5, H=2304, I=384, E=12, k=4, scoring=S.SCORE_SIGMOID,
+                          scaling=2.5, I_shared=128, fmt=S.FMT_MXFP4, shared_fmt=S.FMT_NVFP4),
+    "dec_mx_shared": S.MoeConfig("dec_mx_shared", T=8, H=256, I=128, E=40, k=8,
+                                 scoring=S.SCORE_SIGMOID, scaling=1.5, I_shared=256,
+                                 fmt=S.FMT_NVFP4, shared_fmt=S.FMT_MXFP4),
+    "dec_hash": S.MoeConfig("dec_hash", T=6, H=256, I=256, E=16, k=4, scoring=S.SCORE_HASH,
+                            I_shared=128, fmt=S.FMT_MXFP4, vocab=50),
+    "dec_t1": S.MoeConfig("dec_t1", T=1, H=512, I=128, E=16, k=4, scoring=S.SCORE_SOFTMAX,
+                          renorm=False),
 }
 
 
