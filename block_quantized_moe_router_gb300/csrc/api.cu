@@ -39,7 +39,13 @@ struct Handle {
     PreparedProj gate, up, down, sh_gate, sh_up, sh_down;
     uint32_t profile_mask = 0;
     PhaseEvents events{};  // owned; created by moe_profile_enable
+    bool tc_shape = false;
+    TcWeights tc{};        // owned; the tcgen05 path's scale tiles and tensor maps
 };
+
+bool desc_tc_shape(const moe_ffn_desc& d) {
+    return tc_shape_ok(d.H, d.I, d.I_shared, d.gate.fmt, d.I_shared > 0 ? d.sh_gate.fmt : d.gate.fmt);
+}
 
 void destroy_events(Handle* h) {
     for (int i = 0; i < 4; ++i) {
@@ -151,7 +157,8 @@ moe_status_t moe_workspace_size(const moe_ffn_desc* d, int32_t T, int32_t act, s
     moe_status_t v = validate_ffn_desc(d);
     if (v != MOE_OK) return v;
     if (T < 0 || (act != MOE_ACT_BF16 && act != MOE_ACT_NVFP4)) return MOE_ERR_INVALID_ARG;
-    *bytes = Workspace::plan(d->E, d->H, d->I, d->I_shared, d->top_k, T, act).total;
+    const int path = select_path(T, d->top_k, act, desc_tc_shape(*d));
+    *bytes = Workspace::plan(d->E, d->H, d->I, d->I_shared, d->top_k, T, act, path).total;
     return MOE_OK;
 }
 
@@ -174,6 +181,14 @@ moe_status_t moe_prepare_weights(const moe_ffn_desc* d, void** handle_out, void*
         if (s == MOE_OK) s = prepare_proj(d->sh_up, 1, Is, H, h->sh_up, st);
         if (s == MOE_OK) s = prepare_proj(d->sh_down, 1, H, Is, h->sh_down, st);
     }
+    h->tc_shape = desc_tc_shape(*d);
+    if (s == MOE_OK && h->tc_shape) {
+        FfnLaunch L{};
+        L.E = E; L.H = H; L.I = I; L.I_shared = Is;
+        L.gate = h->gate.view; L.up = h->up.view; L.down = h->down.view;
+        L.sh_gate = h->sh_gate.view; L.sh_up = h->sh_up.view; L.sh_down = h->sh_down.view;
+        if (tc_prepare(L, &h->tc, st) != cudaSuccess) s = MOE_ERR_CUDA;
+    }
     if (s == MOE_OK && cudaStreamSynchronize(st) != cudaSuccess) s = MOE_ERR_CUDA;
     if (s != MOE_OK) {
         moe_release_weights(h);
@@ -189,6 +204,7 @@ moe_status_t moe_release_weights(void* handle) {
     free_proj(h->gate); free_proj(h->up); free_proj(h->down);
     free_proj(h->sh_gate); free_proj(h->sh_up); free_proj(h->sh_down);
     destroy_events(h);
+    tc_release(&h->tc);
     h->magic = 0;
     delete h;
     return MOE_OK;
@@ -206,12 +222,14 @@ moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g
     if (T == 0) return MOE_OK;
     if (!x_bf16 || !topk_ids || !topk_w || !out_bf16 || !workspace) return MOE_ERR_INVALID_ARG;
     const moe_ffn_desc& d = h->desc;
-    const Workspace ws = Workspace::plan(d.E, d.H, d.I, d.I_shared, d.top_k, T, act);
+    const int path = select_path(T, d.top_k, act, h->tc_shape);
+    if (path == PATH_TC && !h->tc.ready) return MOE_ERR_UNSUPPORTED;
+    const Workspace ws = Workspace::plan(d.E, d.H, d.I, d.I_shared, d.top_k, T, act, path);
     if (ws_bytes < ws.total) return MOE_ERR_WORKSPACE;
     char* base = static_cast<char*>(workspace);
     FfnLaunch L{};
     L.T = T; L.E = d.E; L.H = d.H; L.I = d.I; L.k = d.top_k; L.I_shared = d.I_shared;
-    L.act = act; L.g1 = g_act1; L.g2 = g_act2;
+    L.act = act; L.path = path; L.g1 = g_act1; L.g2 = g_act2;
     L.x = x_bf16; L.ids = topk_ids; L.w = topk_w; L.out = out_bf16; L.status = dev_status;
     L.gate = h->gate.view; L.up = h->up.view; L.down = h->down.view;
     L.sh_gate = h->sh_gate.view; L.sh_up = h->sh_up.view; L.sh_down = h->sh_down.view;
@@ -228,9 +246,27 @@ moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g
     L.hq = reinterpret_cast<uint8_t*>(base + ws.hq);
     L.hs = reinterpret_cast<uint8_t*>(base + ws.hs);
     L.y = reinterpret_cast<float*>(base + ws.y);
-    return launch_ffn(L, static_cast<cudaStream_t>(stream), h->profile_mask ? &h->events : nullptr) ==
-                   cudaSuccess
-               ? MOE_OK : MOE_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const PhaseEvents* ev = h->profile_mask ? &h->events : nullptr;
+    cudaError_t err;
+    if (path == PATH_TC) {
+        TcBuffers B{};
+        B.meta = L.meta;
+        B.mblock_expert = reinterpret_cast<int32_t*>(base + ws.mblock_expert);
+        B.padrow_pair = reinterpret_cast<int32_t*>(base + ws.padrow_pair);
+        B.tiles1 = reinterpret_cast<int4*>(base + ws.tiles1);
+        B.tiles2 = reinterpret_cast<int4*>(base + ws.tiles2);
+        B.xq = reinterpret_cast<uint8_t*>(base + ws.txq);
+        B.xsf = reinterpret_cast<uint8_t*>(base + ws.txsf);
+        B.hq = reinterpret_cast<uint8_t*>(base + ws.thq);
+        B.hsf = reinterpret_cast<uint8_t*>(base + ws.thsf);
+        B.y = reinterpret_cast<__nv_bfloat16*>(base + ws.ybf);
+        B.max_blocks = ws.max_blocks;
+        err = launch_ffn_tc(L, h->tc, B, st, ev);
+    } else {
+        err = launch_ffn(L, st, ev);
+    }
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status_t moe_profile_enable(void* handle, uint32_t mask) {

@@ -162,11 +162,30 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, c
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Which implementation of the expert FFN a call takes (shared by moe_workspace_size and
+// moe_ffn_forward, so the workspace always matches the path).
+enum FfnPath { PATH_DECODE = 0, PATH_GENERIC = 1, PATH_TC = 2 };
+
+// The tcgen05 path needs NVFP4 weights and K / N extents in whole 256-element tiles.
+inline bool tc_shape_ok(int H, int I, int I_shared, int fmt_routed, int fmt_shared) {
+    return fmt_routed == MOE_FMT_NVFP4 && (I_shared == 0 || fmt_shared == MOE_FMT_NVFP4) &&
+           H % 256 == 0 && I % 256 == 0 && I_shared % 256 == 0;
+}
+
+inline int select_path(int T, int top_k, int act, bool tc_shape) {
+    if (T <= 8 && T * top_k <= 64 && act == MOE_ACT_BF16) return PATH_DECODE;
+    if (act == MOE_ACT_NVFP4 && tc_shape) return PATH_TC;
+    return PATH_GENERIC;
+}
+
 // Workspace carve-up shared by moe_workspace_size and moe_ffn_forward.
 struct Workspace {
-    size_t counts, offsets, active, meta, sorted_pair, pos_of_pair, x16, xq, xs, h16, hq, hs, y,
-        total;
-    static Workspace plan(int E, int H, int I, int I_shared, int top_k, int T, int act) {
+    size_t counts, offsets, active, meta, sorted_pair, pos_of_pair, x16, xq, xs, h16, hq, hs, y;
+    // tcgen05 path
+    size_t mblock_expert, padrow_pair, tiles1, tiles2, txq, txsf, thq, thsf, ybf;
+    int max_blocks;
+    size_t total;
+    static Workspace plan(int E, int H, int I, int I_shared, int top_k, int T, int act, int path) {
         Workspace w{};
         const size_t P = (size_t)T * top_k;
         const size_t R = P + (I_shared > 0 ? (size_t)T : 0);
@@ -181,20 +200,35 @@ struct Workspace {
         w.offsets = take(sizeof(int32_t) * (E + 2));
         w.active = take(sizeof(int32_t) * (E + 1));
         w.meta = take(sizeof(int32_t) * 64);
-        w.sorted_pair = take(sizeof(int32_t) * (P + 1));
-        w.pos_of_pair = take(sizeof(int32_t) * (P + 1));
-        w.x16 = take(sizeof(__half) * (size_t)T * H);
-        w.xq = take(act == MOE_ACT_NVFP4 ? (size_t)T * H / 2 : 0);
-        w.xs = take(act == MOE_ACT_NVFP4 ? (size_t)T * H / 16 : 0);
-        // few-token path: h is token-major per expert slot, [slots][8][Imax]
-        const size_t dec_rows =
-            (T <= 8 && T * top_k <= 64)
-                ? ((size_t)(E < T * top_k ? E : T * top_k) + (I_shared > 0 ? 1 : 0)) * 8
-                : 0;
-        w.h16 = take(sizeof(__half) * (R > dec_rows ? R : dec_rows) * Imax);
-        w.hq = take(act == MOE_ACT_NVFP4 ? R * Imax / 2 : 0);
-        w.hs = take(act == MOE_ACT_NVFP4 ? R * Imax / 16 : 0);
-        w.y = take(sizeof(float) * R * H);
+        if (path == PATH_DECODE) {
+            // h token-major per expert slot: [routed slots + shared][8][Imax]
+            const size_t rows = ((size_t)(E < T * top_k ? E : T * top_k) + (I_shared > 0 ? 1 : 0)) * 8;
+            w.h16 = take(sizeof(__half) * rows * Imax);
+        } else if (path == PATH_GENERIC) {
+            w.sorted_pair = take(sizeof(int32_t) * (P + 1));
+            w.pos_of_pair = take(sizeof(int32_t) * (P + 1));
+            w.x16 = take(sizeof(__half) * (size_t)T * H);
+            w.xq = take(act == MOE_ACT_NVFP4 ? (size_t)T * H / 2 : 0);
+            w.xs = take(act == MOE_ACT_NVFP4 ? (size_t)T * H / 16 : 0);
+            w.h16 = take(sizeof(__half) * R * Imax);
+            w.hq = take(act == MOE_ACT_NVFP4 ? R * Imax / 2 : 0);
+            w.hs = take(act == MOE_ACT_NVFP4 ? R * Imax / 16 : 0);
+            w.y = take(sizeof(float) * R * H);
+        } else {
+            // expert rows padded to 128: at most one partial block per active expert
+            const size_t active = (size_t)E < P ? (size_t)E : P;
+            w.max_blocks = (int)((P + 127) / 128 + active + (I_shared > 0 ? (T + 127) / 128 : 0));
+            const size_t rows = (size_t)w.max_blocks * 128;
+            w.mblock_expert = take(sizeof(int32_t) * w.max_blocks);
+            w.padrow_pair = take(sizeof(int32_t) * rows);
+            w.tiles1 = take(16 * (size_t)w.max_blocks * (Imax / 128));
+            w.tiles2 = take(16 * (size_t)w.max_blocks * (H / 256));
+            w.txq = take(rows * H / 2);
+            w.txsf = take(rows * H / 16);
+            w.thq = take(rows * Imax / 2);
+            w.thsf = take(rows * Imax / 16);
+            w.ybf = take(sizeof(__nv_bfloat16) * R * H);
+        }
         w.total = off;
         return w;
     }

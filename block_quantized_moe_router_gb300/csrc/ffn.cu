@@ -24,59 +24,11 @@
 #include "common.cuh"
 #include "frag.cuh"
 #include "kernels.h"
+#include "quant.cuh"
 
 namespace moe {
 
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
-
-// ------------------------------------------------------------------------------------------
-// The NVFP4 activation quantizer on 16 fp32 values: writes 8 packed bytes, one E4M3 scale
-// byte and (optionally) the 16 exact dequantized values as f16.
-// ------------------------------------------------------------------------------------------
-__device__ __forceinline__ void quant16(const float (&v)[16], float g, uint8_t* packed,
-                                        uint8_t* scale, __half* deq) {
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    float qs = amax / 6.0f;
-    qs = qs / g;
-    const uint32_t s = f32_to_e4m3(qs);
-    const float denom = e4m3_to_f32(s) * g;
-    uint32_t bytes[8];
-    float dq[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t b = 0;
-        if (denom != 0.f) b = f32x2_to_e2m1x2(v[2 * i] / denom, v[2 * i + 1] / denom);
-        bytes[i] = b;
-        dq[2 * i] = e2m1_to_f32(b & 0xF) * denom;
-        dq[2 * i + 1] = e2m1_to_f32(b >> 4) * denom;
-    }
-    uint2 pk;
-    pk.x = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-    pk.y = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
-    *reinterpret_cast<uint2*>(packed) = pk;
-    *scale = (uint8_t)s;
-    if (deq) {
-        uint4 a, b;
-        a.x = pack_half2(dq[0], dq[1]);   a.y = pack_half2(dq[2], dq[3]);
-        a.z = pack_half2(dq[4], dq[5]);   a.w = pack_half2(dq[6], dq[7]);
-        b.x = pack_half2(dq[8], dq[9]);   b.y = pack_half2(dq[10], dq[11]);
-        b.z = pack_half2(dq[12], dq[13]); b.w = pack_half2(dq[14], dq[15]);
-        reinterpret_cast<uint4*>(deq)[0] = a;
-        reinterpret_cast<uint4*>(deq)[1] = b;
-    }
-}
-
-__device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v)[16]) {
-    const uint4 a = ldg_cached128(src), b = ldg_cached128(src + 8);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
 
 // ------------------------------------------------------------------------------------------
 // Dispatch (block 0) + activation conversion/quantization (blocks 1..).
@@ -397,7 +349,7 @@ __global__ void mx_offsets_kernel(const uint8_t* __restrict__ scales, int64_t pe
 
 // ------------------------------------------------------------------------------------------
 // Records a timing event on `st`; inside stream capture it becomes an event-record node.
-static cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
+cudaError_t record_phase_event(cudaEvent_t ev, cudaStream_t st) {
     if (!ev) return cudaSuccess;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     cudaError_t err = cudaStreamIsCapturing(st, &cs);
@@ -440,17 +392,17 @@ static void launch_expert_phase(const FfnLaunch& L, int slots_r, cudaStream_t st
 cudaError_t launch_ffn(const FfnLaunch& L, cudaStream_t st, const PhaseEvents* ev) {
     cudaError_t err = cudaSuccess;
 #define MOE_PHASE(i, body)                                                  \
-    if (ev && (err = record_event(ev->begin[i], st)) != cudaSuccess) return err; \
+    if (ev && (err = record_phase_event(ev->begin[i], st)) != cudaSuccess) return err; \
     body;                                                                  \
     if ((err = cudaGetLastError()) != cudaSuccess) return err;             \
-    if (ev && (err = record_event(ev->end[i], st)) != cudaSuccess) return err;
+    if (ev && (err = record_phase_event(ev->end[i], st)) != cudaSuccess) return err;
     const int64_t n16 = (int64_t)L.T * L.H / 16;
     int conv_blocks = (int)((n16 + 511) / 512);
     if (conv_blocks > 4 * 152) conv_blocks = 4 * 152;
     if (conv_blocks < 1) conv_blocks = 1;
     const int slots_r = L.E < L.T * L.k ? L.E : L.T * L.k;
     const int64_t nthreads = (int64_t)L.T * (L.H / 8);
-    if (L.T <= 8 && L.T * L.k <= 64 && L.act == MOE_ACT_BF16) {
+    if (L.path == PATH_DECODE) {
         // few tokens: dispatch is rebuilt inside both kernels, combine fused into down
         MOE_PHASE(1, err = launch_decode_phase(L, 1, st); if (err != cudaSuccess) return err)
         MOE_PHASE(2, err = launch_decode_phase(L, 2, st); if (err != cudaSuccess) return err)

@@ -1,5 +1,7 @@
 // kernels.h -- host-side launchers of the library's kernels (internal).
 #pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -29,7 +31,7 @@ struct ProjView {
 };
 
 struct FfnLaunch {
-    int T, E, H, I, k, I_shared, act;
+    int T, E, H, I, k, I_shared, act, path;
     float g1, g2;
     const void* x;          // bf16 [T][H]
     const int32_t* ids;     // [T][k]
@@ -53,6 +55,70 @@ struct PhaseEvents {
 };
 
 cudaError_t launch_ffn(const FfnLaunch& L, cudaStream_t st, const PhaseEvents* ev = nullptr);
+cudaError_t record_phase_event(cudaEvent_t ev, cudaStream_t st);
+
+// ---- many-token FFN on the tcgen05 tensor cores (prefill_tc.cu) -----------------------------
+// Weights prepared once: TMA maps over the packed codes and the block scales rearranged into
+// the MMA's 128-row x 4 scale-factor tiles (owned buffers).
+struct TcWeights {
+    bool ready = false;
+    CUtensorMap gate, up, down, sh_gate, sh_up, sh_down;
+    uint8_t *sf_gate = nullptr, *sf_up = nullptr, *sf_down = nullptr;
+    uint8_t *sf_sh_gate = nullptr, *sf_sh_up = nullptr, *sf_sh_down = nullptr;
+};
+struct TcBuffers {  // workspace views
+    int32_t *meta, *mblock_expert, *padrow_pair;
+    int4 *tiles1, *tiles2;
+    uint8_t *xq, *xsf, *hq, *hsf;
+    __nv_bfloat16* y;
+    int max_blocks;
+};
+struct TcPrepArgs {
+    const int32_t* ids;
+    int T, k, E, H, I, I_shared, has_shared;
+    int32_t* status;
+    int32_t *meta, *mblock_expert, *padrow_pair;
+    int4 *tiles1, *tiles2;
+};
+struct TcQuantArgs {
+    const void* x;
+    int H, k, P;
+    float g1;
+    const int32_t *meta, *padrow_pair;
+    uint8_t *xq, *xsf;
+};
+struct TcTensorMaps {
+    CUtensorMap a, b0, b1, sb0, sb1;
+};
+struct TcGemmParams {
+    int mode;  // 0: gate+up -> NVFP4 h; 1: down -> bf16 rows per pair
+    int E, H, I, I_shared, k, T, P;
+    const int4* tiles;
+    const int32_t* num_tiles;
+    const int32_t *mblock_expert, *padrow_pair;
+    const uint8_t* sfa;
+    int sfa_kblocks;
+    const uint8_t *sfb0, *sfb1, *ssfb0, *ssfb1;
+    const float *post0, *post1, *spost0, *spost1;
+    const float* topk_w;
+    uint8_t *hq, *hsf;
+    int hq_row_bytes, hsf_kblocks;
+    float g2;
+    __nv_bfloat16* y;
+    int32_t* status;
+};
+struct TcCombineArgs {
+    const __nv_bfloat16* y;
+    const int32_t* ids;
+    void* out;
+    int T, H, k, E, has_shared;
+};
+
+bool tc_supported(int E, int H, int I, int I_shared, int fmt_routed, int fmt_shared);
+cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, cudaStream_t st);
+void tc_release(TcWeights* tw);
+cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffers& B,
+                          cudaStream_t st, const PhaseEvents* ev);
 
 // Few-token path (T <= 8, bf16 activations): phase 1 = gate+up, phase 2 = down + combine.
 cudaError_t launch_decode_phase(const FfnLaunch& L, int phase, cudaStream_t st);

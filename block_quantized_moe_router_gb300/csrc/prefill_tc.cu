@@ -1,0 +1,616 @@
+// prefill_tc.cu -- the many-token expert FFN with NVFP4 activations on the sm_103a tensor
+// cores (tcgen05, block-scaled E2M1 x E2M1 with UE4M3 scales per 16, accumulators in TMEM).
+//
+// The block-scaled FP4 x FP4 product is the spark_model prefill recipe (moe/mod.rs,
+// `moe_fused_gate_up_t_k64_fp4` field doc: one block-scaled MMA per 64-element K tile, NVFP4
+// activations from the `quantize_bf16_to_nvfp4` step of qwen3_attention/init.rs); the pages
+// run it as warp-level MMAs on GB10, here it is tcgen05 with operands staged by TMA.
+//
+// Data flow (every step on the device, no host synchronisation):
+//   tc_prep_kernel   histogram of the routed pairs, expert rows padded to 128 (one MMA M tile),
+//                    padded-row -> pair map, per-128-row block -> expert map, and the two tile
+//                    lists (expert-major, then N block, then M block, so that concurrently
+//                    running CTAs share one expert's weight tile through L2);
+//   tc_quant_kernel  NVFP4 quantization of each pair's token into its padded row, the scales
+//                    written directly in the 128 x 4 scale-factor tile layout of the MMA;
+//   tc_gemm_kernel   (gate+up) D[128 pairs][128 gate | 128 up] over K = H; the epilogue
+//                    computes h = SiLU(g) * u and requantizes it to NVFP4 (codes + scale tiles)
+//                    as the next GEMM's activation operand;
+//   tc_gemm_kernel   (down) D[128 pairs][256 outputs] over K = I; the epilogue applies the
+//                    per-tensor global and the routing weight and stores bf16 rows per pair;
+//   tc_combine_kernel  out[t] = sum_j y[t, j] + y_shared[t].
+//
+// The GEMM kernel is persistent (one CTA per SM, tiles strided by the grid) and warp
+// specialised: warp 0 issues TMA / bulk copies into a 4-stage shared-memory ring, warp 1
+// allocates TMEM and one of its lanes issues tcgen05.cp (scale factors) and tcgen05.mma,
+// warps 2-5 drain the accumulator with tcgen05.ld.  Every mbarrier wait is bounded; a wait
+// that gives up sets MOE_DEV_TIMEOUT, the CTA stops issuing work, waits (bounded) for its
+// copies and MMAs in flight, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "quant.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+using namespace tc;
+
+constexpr int kTcStages = 4;
+constexpr int kTcABytes = 128 * 128;          // 128 rows x 128 B (256 E2M1 codes)
+constexpr int kTcBBytes = 256 * 128;          // 256 rows x 128 B
+constexpr int kTcSfaBytes = 4 * 512;          // 4 K blocks of 64 x one 128-row scale tile
+constexpr int kTcSfbBytes = 8 * 512;          // 4 K blocks x two 128-row scale tiles
+constexpr int kTcSfaOff = kTcABytes + kTcBBytes;
+constexpr int kTcSfbOff = kTcSfaOff + kTcSfaBytes;
+constexpr int kTcStageBytes = kTcSfbOff + kTcSfbBytes;  // 55296 (54 KiB, 1 KiB multiple)
+constexpr int kTcSmemBytes = kTcStages * kTcStageBytes + 1024 + 256;
+constexpr uint32_t kTcTmemCols = 512;         // 256 accumulator + 4 stages x 48 scale columns
+constexpr int kTcThreads = 192;
+constexpr uint64_t kTcWaitLimit = 1ull << 26;  // polls before a wait is declared stuck
+
+// Byte offset of the scale of (row r of a 128-row block, 16-element block j of a 64-element
+// K block) inside that K block's 512-byte scale tile: rows r, r+32, r+64, r+96 share one
+// 16-byte line, which the 32x128b tcgen05.cp spreads over TMEM lanes and columns.
+__host__ __device__ __forceinline__ int sf_tile_offset(int r, int j) {
+    return (r & 31) * 16 + (r >> 5) * 4 + j;
+}
+
+// ------------------------------------------------------------------------------------------
+// dispatch + tile lists (one CTA)
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) tc_prep_kernel(TcPrepArgs a) {
+    __shared__ int cnt[kMaxExperts + 1];
+    __shared__ int cursor[kMaxExperts + 1];
+    __shared__ int mbase[kMaxExperts + 2];
+    __shared__ int tb1[kMaxExperts + 2];
+    __shared__ int tb2[kMaxExperts + 2];
+    const int tid = threadIdx.x, E = a.E, P = a.T * a.k;
+    for (int e = tid; e <= E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int p = tid; p < P; p += blockDim.x) {
+        const int e = a.ids[p];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else if (e != -1) bad = 1;
+    }
+    if (bad) status_or(a.status, MOE_DEV_BAD_EXPERT_ID);
+    __syncthreads();
+    if (tid == 0) cnt[E] = a.has_shared ? a.T : 0;  // the shared expert takes every token
+    __syncthreads();
+    if (tid < 32) {  // exclusive scans over E + 1 entries (routed experts, then shared)
+        const int lane = tid, n = E + 1, per = (n + 31) / 32;
+        const int lo = min(n, lane * per), hi = min(n, lo + per);
+        int smb = 0, st1 = 0, st2 = 0;
+        for (int e = lo; e < hi; ++e) {
+            const int nmb = (cnt[e] + 127) / 128;
+            const int nb1 = (e < E ? a.I : a.I_shared) / 128;
+            smb += nmb;
+            st1 += nmb * nb1;
+            st2 += nmb * (a.H / 256);
+        }
+        int i_mb = smb, i_t1 = st1, i_t2 = st2;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, i_mb, o);
+            const int y = __shfl_up_sync(0xffffffffu, i_t1, o);
+            const int z = __shfl_up_sync(0xffffffffu, i_t2, o);
+            if (lane >= o) { i_mb += x; i_t1 += y; i_t2 += z; }
+        }
+        int b = i_mb - smb, t1 = i_t1 - st1, t2 = i_t2 - st2;
+        for (int e = lo; e < hi; ++e) {
+            const int nmb = (cnt[e] + 127) / 128;
+            const int nb1 = (e < E ? a.I : a.I_shared) / 128;
+            mbase[e] = b;
+            tb1[e] = t1;
+            tb2[e] = t2;
+            cursor[e] = b * 128;
+            b += nmb;
+            t1 += nmb * nb1;
+            t2 += nmb * (a.H / 256);
+        }
+        if (lane == 31) {
+            mbase[n] = i_mb;
+            tb1[n] = i_t1;
+            tb2[n] = i_t2;
+            a.meta[0] = i_t1;       // gate+up tiles
+            a.meta[1] = i_t2;       // down tiles
+            a.meta[2] = i_mb * 128; // padded rows in use
+            a.meta[3] = i_mb;       // 128-row blocks in use
+        }
+    }
+    __syncthreads();
+    const int nblocks = mbase[E + 1];
+    for (int r = tid; r < nblocks * 128; r += blockDim.x) a.padrow_pair[r] = -1;
+    for (int b = tid; b < nblocks; b += blockDim.x) {
+        int lo = 0, hi = E + 1;  // largest e with mbase[e] <= b
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (mbase[mid] <= b) lo = mid; else hi = mid;
+        }
+        a.mblock_expert[b] = lo;
+    }
+    __syncthreads();
+    for (int p = tid; p < P; p += blockDim.x) {
+        const int e = a.ids[p];
+        if (e >= 0 && e < E) a.padrow_pair[atomicAdd(&cursor[e], 1)] = p;
+    }
+    if (a.has_shared)
+        for (int t = tid; t < a.T; t += blockDim.x) a.padrow_pair[mbase[E] * 128 + t] = P + t;
+    // tile lists: entry = (128-row block, N block, expert (E = shared), K stages)
+    for (int pass = 0; pass < 2; ++pass) {
+        const int* tb = pass == 0 ? tb1 : tb2;
+        int4* out = pass == 0 ? a.tiles1 : a.tiles2;
+        const int total = tb[E + 1];
+        for (int t = tid; t < total; t += blockDim.x) {
+            int lo = 0, hi = E + 1;  // largest e with tb[e] <= t and a nonzero range
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (tb[mid] <= t) lo = mid; else hi = mid;
+            }
+            while (lo < E && tb[lo + 1] <= t) ++lo;  // skip experts with no tiles
+            const int nmb = mbase[lo + 1] - mbase[lo];
+            const int r = t - tb[lo];
+            const int nb = r / nmb, mb = r - nb * nmb;
+            const int K = pass == 0 ? a.H : (lo < E ? a.I : a.I_shared);
+            out[t] = make_int4(mbase[lo] + mb, nb, lo, K / 256);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// NVFP4 quantization of the tokens into the padded, expert-sorted rows
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tc_quant_kernel(TcQuantArgs a) {
+    const int rows = a.meta[2];
+    const int nb16 = a.H / 16;
+    const int64_t total = (int64_t)rows * nb16;
+    const auto* x = static_cast<const __nv_bfloat16*>(a.x);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int prow = (int)(i / nb16), blk = (int)(i - (int64_t)prow * nb16);
+        const int p = a.padrow_pair[prow];
+        if (p < 0) continue;
+        const int t = p < a.P ? p / a.k : p - a.P;
+        float v[16];
+        load_bf16x16(x + (size_t)t * a.H + blk * 16, v);
+        const int mb = prow >> 7, r = prow & 127;
+        uint8_t* sf = a.xsf + ((size_t)mb * (a.H / 64) + (blk >> 2)) * 512 + sf_tile_offset(r, blk & 3);
+        quant16(v, a.g1, a.xq + (size_t)prow * (a.H / 2) + blk * 8, sf, nullptr);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// the tcgen05 grouped GEMM
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void tc_abort(TcGemmParams const& p, volatile int* flag) {
+    *flag = 1;
+    status_or(p.status, MOE_DEV_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
+    uint64_t* empty = full + kTcStages;
+    uint64_t* acc_full = empty + kTcStages;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* drain = acc_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 128);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&maps.a);
+        prefetch_tmap(&maps.b0);
+        prefetch_tmap(&maps.b1);
+        prefetch_tmap(&maps.sb0);
+        prefetch_tmap(&maps.sb1);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTcTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int ntiles = p.num_tiles[0];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+                const int4 tl = p.tiles[tile];
+                const int b = tl.x, nb = tl.y, e = tl.z, kst = tl.w;
+                const bool sh = e == p.E;
+                const int es = sh ? 0 : e;
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kTcWaitLimit)) {
+                        tc_abort(p, abort_flag);
+                        break;
+                    }
+                    if (*abort_flag) break;
+                    uint8_t* base = smem + stage * kTcStageBytes;
+                    mbar_arrive_expect_tx(&full[stage], kTcStageBytes);
+                    const int xb = ks * 128;
+                    tma_load_2d(base, &maps.a, xb, b * 128, &full[stage]);
+                    bulk_load(base + kTcSfaOff, p.sfa + ((size_t)b * p.sfa_kblocks + 4 * ks) * 512,
+                              kTcSfaBytes, &full[stage]);
+                    if (p.mode == 0) {
+                        const int N = sh ? p.I_shared : p.I;
+                        const int row = es * N + nb * 128;
+                        tma_load_2d(base + kTcABytes, sh ? &maps.sb0 : &maps.b0, xb, row, &full[stage]);
+                        tma_load_2d(base + kTcABytes + 16384, sh ? &maps.sb1 : &maps.b1, xb, row,
+                                    &full[stage]);
+                        const size_t tix = ((size_t)es * (N / 128) + nb) * (p.H / 64) + 4 * ks;
+                        bulk_load(base + kTcSfbOff, (sh ? p.ssfb0 : p.sfb0) + tix * 512, 2048,
+                                  &full[stage]);
+                        bulk_load(base + kTcSfbOff + 2048, (sh ? p.ssfb1 : p.sfb1) + tix * 512,
+                                  2048, &full[stage]);
+                    } else {
+                        const int K = sh ? p.I_shared : p.I;
+                        const int row = es * p.H + nb * 256;
+                        tma_load_2d(base + kTcABytes, sh ? &maps.sb0 : &maps.b0, xb, row, &full[stage]);
+                        const uint8_t* sfb = sh ? p.ssfb0 : p.sfb0;
+                        const size_t t0 = ((size_t)es * (p.H / 128) + 2 * nb) * (K / 64) + 4 * ks;
+                        const size_t t1 = ((size_t)es * (p.H / 128) + 2 * nb + 1) * (K / 64) + 4 * ks;
+                        bulk_load(base + kTcSfbOff, sfb + t0 * 512, 2048, &full[stage]);
+                        bulk_load(base + kTcSfbOff + 2048, sfb + t1 * 512, 2048, &full[stage]);
+                    }
+                    ++issued;
+                    if (++stage == kTcStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (*abort_flag) {
+                // wait (bounded) for the copies this thread may still have in flight
+                int s = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < kTcStages && i < issued; ++i) {
+                    if (--s < 0) { s = kTcStages - 1; ph ^= 1u; }
+                    mbar_wait_bounded(&full[s], ph, kTcWaitLimit);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            const uint32_t idesc = idesc_fp4(128, 256, 0);
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool any = false;
+            for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+                const int kst = p.tiles[tile].w;
+                if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, kTcWaitLimit)) {
+                    tc_abort(p, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                bool ok = true;
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (!mbar_wait_bounded(&full[stage], phase, kTcWaitLimit) || *abort_flag) {
+                        tc_abort(p, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint8_t* base = smem + stage * kTcStageBytes;
+                    const uint32_t sbase = smem_u32(base);
+                    const uint32_t sfcol = 256 + stage * 48;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t c = tmem + sfcol + 12 * j;
+                        tc_cp_32x128b_warpx4(c, smem_desc(sbase + kTcSfaOff + 512 * j, 0, 128, kLayoutNone));
+                        tc_cp_32x128b_warpx4(c + 4, smem_desc(sbase + kTcSfbOff + 512 * j, 0, 128, kLayoutNone));
+                        tc_cp_32x128b_warpx4(c + 8, smem_desc(sbase + kTcSfbOff + 2048 + 512 * j, 0, 128, kLayoutNone));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint64_t ad = smem_desc(sbase + 32 * j, 16, 1024, kLayoutSw128);
+                        const uint64_t bd = smem_desc(sbase + kTcABytes + 32 * j, 16, 1024, kLayoutSw128);
+                        const uint32_t c = tmem + sfcol + 12 * j;
+                        tc_mma_nvf4(tmem, ad, bd, idesc, c, c + 4, (ks | j) != 0 ? 1u : 0u);
+                    }
+                    any = true;
+                    tc_commit(&empty[stage]);
+                    if (++stage == kTcStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(acc_full);
+                acc_phase ^= 1u;
+            }
+            if (any) {  // every MMA this thread issued has completed before TMEM is freed
+                tc_commit(drain);
+                mbar_wait_bounded(drain, 0, kTcWaitLimit);
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            if (!mbar_wait_bounded(acc_full, acc_phase, kTcWaitLimit)) {
+                tc_abort(p, abort_flag);
+                break;
+            }
+            if (*abort_flag) break;
+            tc_fence_after();
+            const int4 tl = p.tiles[tile];
+            const int b = tl.x, nb = tl.y, e = tl.z;
+            const bool sh = e == p.E;
+            const int es = sh ? 0 : e;
+            const int prow = b * 128 + r;
+            const int pair = p.padrow_pair[prow];
+            if (p.mode == 0) {
+                const float pg = (sh ? p.spost0 : p.post0)[es];
+                const float pu = (sh ? p.spost1 : p.post1)[es];
+                const int i0 = nb * 128;
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 16) {
+                    uint32_t G[16], U[16];
+                    tmem_ld_16(trow + c, G);
+                    tmem_ld_16(trow + 128 + c, U);
+                    tmem_ld_wait();
+                    float h[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        h[i] = silu_f32(__uint_as_float(G[i]) * pg) * (__uint_as_float(U[i]) * pu);
+                    if (pair >= 0) {
+                        const int i = i0 + c;
+                        uint8_t* sf = p.hsf + ((size_t)b * p.hsf_kblocks + (i >> 6)) * 512 +
+                                      sf_tile_offset(r, (i >> 4) & 3);
+                        quant16(h, p.g2, p.hq + (size_t)prow * p.hq_row_bytes + i / 2, sf, nullptr);
+                    }
+                }
+            } else {
+                const float pd = (sh ? p.spost0 : p.post0)[es];
+                const float wgt = pair < 0 ? 0.f : (pair < p.P ? p.topk_w[pair] : 1.f);
+                const float sc = pd * wgt;
+                const int n0 = nb * 256;
+#pragma unroll 1
+                for (int c = 0; c < 256; c += 16) {
+                    uint32_t Y[16];
+                    tmem_ld_16(trow + c, Y);
+                    tmem_ld_wait();
+                    if (pair >= 0) {
+                        uint4 o0, o1;
+                        uint32_t* w0 = &o0.x;
+                        uint32_t* w1 = &o1.x;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(Y[2 * i]) * sc,
+                                                                      __uint_as_float(Y[2 * i + 1]) * sc);
+                            __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(Y[8 + 2 * i]) * sc,
+                                                                      __uint_as_float(Y[9 + 2 * i]) * sc);
+                            w0[i] = *reinterpret_cast<uint32_t*>(&v0);
+                            w1[i] = *reinterpret_cast<uint32_t*>(&v1);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(p.y + (size_t)pair * p.H + n0 + c);
+                        dst[0] = o0;
+                        dst[1] = o1;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+            acc_phase ^= 1u;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTcTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// combine: out[t] = sum_j y[t*k + j] (valid pairs) + y[P + t]
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tc_combine_kernel(TcCombineArgs a) {
+    const int H8 = a.H / 8;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)a.T * H8) return;
+    const int t = (int)(idx / H8), c = (int)(idx - (int64_t)t * H8);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    auto add = [&](int row) {
+        const uint4 v = *reinterpret_cast<const uint4*>(a.y + (size_t)row * a.H + c * 8);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += __uint_as_float(w[i] << 16);
+            acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    };
+    for (int j = 0; j < a.k; ++j) {
+        const int e = a.ids[t * a.k + j];
+        if (e >= 0 && e < a.E) add(t * a.k + j);
+    }
+    if (a.has_shared) add(a.T * a.k + t);
+    uint4 o;
+    uint32_t* ow = &o.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        ow[i] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + (size_t)t * a.H)[c] = o;
+}
+
+// ------------------------------------------------------------------------------------------
+// weight preparation: scale-factor tiles and tensor maps
+// ------------------------------------------------------------------------------------------
+// out[((e * N/128 + rb) * K/64 + kb) * 512 + sf_tile_offset(r, j)] = in[e][rb*128 + r][kb*4 + j]
+__global__ void sf_tiles_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out,
+                                int E, int N, int K) {
+    const int64_t total = (int64_t)E * N * (K / 16);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int kk = (int)(i % (K / 16));
+        const int64_t row = i / (K / 16);
+        const int e = (int)(row / N), n = (int)(row % N);
+        const int rb = n >> 7, r = n & 127, kb = kk >> 2, j = kk & 3;
+        out[(((size_t)e * (N / 128) + rb) * (K / 64) + kb) * 512 + sf_tile_offset(r, j)] = in[i];
+    }
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2D map over a [rows][row_bytes] uint8 matrix, 128-byte x box_rows boxes, 128B swizzle.
+static bool encode_rows(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
+                        uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn || rows < box_rows || row_bytes % 128) return false;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static cudaError_t make_sf_tiles(const uint8_t* scales, int E, int N, int K, uint8_t** out,
+                                 cudaStream_t st) {
+    const size_t bytes = (size_t)E * N * (K / 16);
+    cudaError_t err = cudaMalloc(out, bytes);
+    if (err != cudaSuccess) return err;
+    sf_tiles_kernel<<<1024, 256, 0, st>>>(scales, *out, E, N, K);
+    return cudaGetLastError();
+}
+
+bool tc_supported(int E, int H, int I, int I_shared, int fmt_routed, int fmt_shared) {
+    (void)E;
+    return fmt_routed == MOE_FMT_NVFP4 && (I_shared == 0 || fmt_shared == MOE_FMT_NVFP4) &&
+           H % 256 == 0 && I % 256 == 0 && I_shared % 256 == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, cudaStream_t st) {
+    *tw = TcWeights{};
+    const int E = L.E, H = L.H, I = L.I, Is = L.I_shared;
+    cudaError_t err;
+    if ((err = make_sf_tiles(L.gate.scales, E, I, H, &tw->sf_gate, st)) != cudaSuccess) return err;
+    if ((err = make_sf_tiles(L.up.scales, E, I, H, &tw->sf_up, st)) != cudaSuccess) return err;
+    if ((err = make_sf_tiles(L.down.scales, E, H, I, &tw->sf_down, st)) != cudaSuccess) return err;
+    bool ok = encode_rows(&tw->gate, L.gate.packed, H / 2, (uint64_t)E * I, 128) &&
+              encode_rows(&tw->up, L.up.packed, H / 2, (uint64_t)E * I, 128) &&
+              encode_rows(&tw->down, L.down.packed, I / 2, (uint64_t)E * H, 256);
+    if (Is > 0) {
+        if ((err = make_sf_tiles(L.sh_gate.scales, 1, Is, H, &tw->sf_sh_gate, st)) != cudaSuccess) return err;
+        if ((err = make_sf_tiles(L.sh_up.scales, 1, Is, H, &tw->sf_sh_up, st)) != cudaSuccess) return err;
+        if ((err = make_sf_tiles(L.sh_down.scales, 1, H, Is, &tw->sf_sh_down, st)) != cudaSuccess) return err;
+        ok = ok && encode_rows(&tw->sh_gate, L.sh_gate.packed, H / 2, Is, 128) &&
+             encode_rows(&tw->sh_up, L.sh_up.packed, H / 2, Is, 128) &&
+             encode_rows(&tw->sh_down, L.sh_down.packed, Is / 2, H, 256);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTcSmemBytes);
+    if (err != cudaSuccess) return err;
+    tw->ready = true;
+    return cudaSuccess;
+}
+
+void tc_release(TcWeights* tw) {
+    uint8_t* bufs[6] = {tw->sf_gate, tw->sf_up, tw->sf_down, tw->sf_sh_gate, tw->sf_sh_up,
+                        tw->sf_sh_down};
+    for (uint8_t* b : bufs)
+        if (b) cudaFree(b);
+    *tw = TcWeights{};
+}
+
+// ------------------------------------------------------------------------------------------
+cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffers& B,
+                          cudaStream_t st, const PhaseEvents* ev) {
+    const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
+    const int P = L.T * L.k;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t err = cudaSuccess;
+#define TC_PHASE(i, body)                                                            \
+    if (ev && (err = record_phase_event(ev->begin[i], st)) != cudaSuccess) return err; \
+    body;                                                                           \
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;                      \
+    if (ev && (err = record_phase_event(ev->end[i], st)) != cudaSuccess) return err;
+
+    TcPrepArgs pa{};
+    pa.ids = L.ids; pa.T = L.T; pa.k = L.k; pa.E = L.E; pa.H = L.H; pa.I = L.I;
+    pa.I_shared = L.I_shared; pa.has_shared = L.I_shared > 0; pa.status = L.status;
+    pa.meta = B.meta; pa.mblock_expert = B.mblock_expert; pa.padrow_pair = B.padrow_pair;
+    pa.tiles1 = B.tiles1; pa.tiles2 = B.tiles2;
+    TcQuantArgs qa{};
+    qa.x = L.x; qa.H = L.H; qa.k = L.k; qa.P = P; qa.g1 = L.g1; qa.meta = B.meta;
+    qa.padrow_pair = B.padrow_pair; qa.xq = B.xq; qa.xsf = B.xsf;
+    TC_PHASE(0, (tc_prep_kernel<<<1, 1024, 0, st>>>(pa), tc_quant_kernel<<<sms * 8, 256, 0, st>>>(qa)))
+
+    TcTensorMaps m1{}, m2{};
+    const uint64_t rows = (uint64_t)B.max_blocks * 128;
+    if (!encode_rows(&m1.a, B.xq, L.H / 2, rows, 128) ||
+        !encode_rows(&m2.a, B.hq, Imax / 2, rows, 128))
+        return cudaErrorInvalidValue;
+    m1.b0 = tw.gate; m1.b1 = tw.up; m1.sb0 = tw.sh_gate; m1.sb1 = tw.sh_up;
+    m2.b0 = tw.down; m2.b1 = tw.down; m2.sb0 = tw.sh_down; m2.sb1 = tw.sh_down;
+    if (L.I_shared == 0) { m1.sb0 = tw.gate; m1.sb1 = tw.up; m2.sb0 = tw.down; m2.sb1 = tw.down; }
+
+    TcGemmParams g{};
+    g.E = L.E; g.H = L.H; g.I = L.I; g.I_shared = L.I_shared; g.k = L.k; g.T = L.T; g.P = P;
+    g.mblock_expert = B.mblock_expert; g.padrow_pair = B.padrow_pair; g.topk_w = L.w;
+    g.status = L.status; g.g2 = L.g2;
+    g.hq = B.hq; g.hsf = B.hsf; g.hq_row_bytes = Imax / 2; g.hsf_kblocks = Imax / 64;
+    g.y = B.y;
+
+    TcGemmParams g1 = g;
+    g1.mode = 0;
+    g1.tiles = B.tiles1; g1.num_tiles = B.meta + 0;
+    g1.sfa = B.xsf; g1.sfa_kblocks = L.H / 64;
+    g1.sfb0 = tw.sf_gate; g1.sfb1 = tw.sf_up; g1.ssfb0 = tw.sf_sh_gate; g1.ssfb1 = tw.sf_sh_up;
+    g1.post0 = L.gate.post; g1.post1 = L.up.post; g1.spost0 = L.sh_gate.post; g1.spost1 = L.sh_up.post;
+    TC_PHASE(1, (tc_gemm_kernel<<<sms, kTcThreads, kTcSmemBytes, st>>>(m1, g1)))
+
+    TcGemmParams g2 = g;
+    g2.mode = 1;
+    g2.tiles = B.tiles2; g2.num_tiles = B.meta + 1;
+    g2.sfa = B.hsf; g2.sfa_kblocks = Imax / 64;
+    g2.sfb0 = tw.sf_down; g2.sfb1 = tw.sf_down; g2.ssfb0 = tw.sf_sh_down; g2.ssfb1 = tw.sf_sh_down;
+    g2.post0 = L.down.post; g2.post1 = L.down.post; g2.spost0 = L.sh_down.post; g2.spost1 = L.sh_down.post;
+    TC_PHASE(2, (tc_gemm_kernel<<<sms, kTcThreads, kTcSmemBytes, st>>>(m2, g2)))
+
+    TcCombineArgs ca{};
+    ca.y = B.y; ca.ids = L.ids; ca.out = L.out; ca.T = L.T; ca.H = L.H; ca.k = L.k; ca.E = L.E;
+    ca.has_shared = L.I_shared > 0;
+    const int64_t n = (int64_t)L.T * (L.H / 8);
+    TC_PHASE(3, (tc_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(ca)))
+#undef TC_PHASE
+    return cudaSuccess;
+}
+
+}  // namespace moe

@@ -49,6 +49,15 @@ SMALL = {
                             I_shared=128, fmt=S.FMT_MXFP4, vocab=50),
     "dec_t1": S.MoeConfig("dec_t1", T=1, H=512, I=128, E=16, k=4, scoring=S.SCORE_SOFTMAX,
                           renorm=False),
+    # NVFP4 activations with 256-multiple shapes: tcgen05 block-scaled path
+    "tc_small": S.MoeConfig("tc_small", T=40, H=512, I=256, E=16, k=4, scoring=S.SCORE_SIGMOID,
+                            scaling=2.5, I_shared=256, act=S.ACT_NVFP4),
+    "tc_multi_block": S.MoeConfig("tc_multi_block", T=300, H=768, I=512, E=4, k=2,
+                                  scoring=S.SCORE_SOFTMAX, act=S.ACT_NVFP4),
+    "tc_shared_wide": S.MoeConfig("tc_shared_wide", T=70, H=256, I=256, E=8, k=2,
+                                  scoring=S.SCORE_SOFTMAX, I_shared=512, act=S.ACT_NVFP4),
+    "tc_t1": S.MoeConfig("tc_t1", T=1, H=256, I=256, E=8, k=2, scoring=S.SCORE_SOFTMAX,
+                         I_shared=256, act=S.ACT_NVFP4),
 }
 
 
@@ -100,8 +109,16 @@ def test_full_size_configs(cuda_lib, name):
     assert (out.float().abs().amax(1) > 0).all()
 
 
-def test_dropped_pairs_and_zero_tokens(cuda_lib):
-    cfg = SMALL["hash_small"]
+DROP = {
+    "generic": SMALL["hash_small"],
+    "tc": S.MoeConfig("hash_tc", T=50, H=512, I=256, E=16, k=3, scoring=S.SCORE_HASH,
+                      I_shared=256, vocab=100, act=S.ACT_NVFP4),
+}
+
+
+@pytest.mark.parametrize("name", list(DROP))
+def test_dropped_pairs_and_zero_tokens(cuda_lib, name):
+    cfg = DROP[name]
     inp, _ = parity.make_case(cfg, seed=2, device="cpu")
     tab = inp["tid2eid"].clone()
     tok = inp["token_ids"]
