@@ -52,17 +52,28 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio (13.5 vs 2.25 PFLOP/s)
+
+
 def measured_peaks():
+    """(HBM GB/s, dense bf16 TFLOP/s burst, source) from MEASURED_PEAKS.json, else fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    hbm, bf16, src = FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
     try:
         with open(path) as fh:
             d = json.load(fh)
         for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
             if key in d:
-                return float(d[key]), "measured"
+                hbm, src = float(d[key]), "measured"
+                break
+        for key in ("bf16_tflops", "bf16_TFLOPs"):
+            if key in d:
+                bf16 = float(d[key])
+                break
     except Exception:
         pass
-    return FALLBACK_HBM_GBS, "fallback"
+    return hbm, bf16, src
 
 
 # ------------------------------------------------------------------------------------------
@@ -131,8 +142,10 @@ def step_bytes(cfg, n_touched):
     sh_down = proj_bytes(H, Is, cfg.shared_fmt) if Is else 0
     router = cfg.E * H * 2 if cfg.scoring != synth.SCORE_HASH else cfg.T * cfg.k * 8
     acts = cfg.T * H * 2 * 2
+    pairs = cfg.T * cfg.k
     return {"gate_up": n_touched * gate_up + sh_gate_up + cfg.T * H * 2,
-            "total": n_touched * (gate_up + down) + sh_gate_up + sh_down + router + acts}
+            "total": n_touched * (gate_up + down) + sh_gate_up + sh_down + router + acts,
+            "gate_up_flops": 2 * 2 * I * H * pairs + (2 * 2 * Is * H * cfg.T if Is else 0)}
 
 
 # ------------------------------------------------------------------------------------------
@@ -355,8 +368,10 @@ def run_ours(args, cfg):
     d2h = T * cfg.H * 2
 
     if rank == 0:
-        peak, peak_kind = measured_peaks()
+        peak, bf16_peak, peak_kind = measured_peaks()
         achieved = nbytes["gate_up"] / (dom_ms * 1e-3) / 1e9
+        fp4_peak = bf16_peak * FP4_OVER_BF16
+        tflops = nbytes["gate_up_flops"] / (dom_ms * 1e-3) / 1e12
         layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
         src = kernel_source_hash()
         tr = TRAFFIC.get(cfg.name)
@@ -376,9 +391,18 @@ def run_ours(args, cfg):
             "gpu_launches": args.steps * launches_per_step(cfg),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "expert_mma_kernel<gate+up>",
+                         "kernel": "gate+up GEMM (" + ("tc_gemm_kernel" if cfg.act == synth.ACT_NVFP4
+                                                       else "dec_gateup_kernel" if cfg.T <= 8
+                                                       else "expert_mma_kernel") + ")",
                          "bytes_per_launch": nbytes["gate_up"], "launch_ms": dom_ms,
                          "peak_source": peak_kind},
+            "tensor_view": {"achieved_tflops": tflops,
+                            "peak_tflops": fp4_peak if cfg.act == synth.ACT_NVFP4 else bf16_peak,
+                            "frac": tflops / (fp4_peak if cfg.act == synth.ACT_NVFP4 else bf16_peak),
+                            "dtype": "nvfp4 x nvfp4" if cfg.act == synth.ACT_NVFP4 else "f16 mma",
+                            "flops_per_launch": nbytes["gate_up_flops"],
+                            "peak_source": peak_kind + " bf16 x nominal fp4/bf16 ratio"
+                            if cfg.act == synth.ACT_NVFP4 else peak_kind},
             "layer_roofline": {"achieved": layer_gbs, "peak": peak, "unit": "GB/s",
                                "frac": layer_gbs / peak, "bytes_per_step": nbytes["total"]},
             "clocks": clk,
