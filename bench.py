@@ -77,6 +77,23 @@ def measured_peaks():
 
 
 # ------------------------------------------------------------------------------------------
+# multi-rank helpers (one process per GPU; each rank runs its own replica on its own tokens)
+# ------------------------------------------------------------------------------------------
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings (the slowest rank sets the job's time)."""
+    if dist is None or not dist.is_initialized():
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(tokens_per_rank, world, seconds):
+    """Whole-job throughput under weak scaling: every rank processed its own batch."""
+    return tokens_per_rank * world / seconds
+
+
+# ------------------------------------------------------------------------------------------
 # clocks
 # ------------------------------------------------------------------------------------------
 class ClockSampler:
@@ -331,10 +348,7 @@ def run_ours(args, cfg):
     # timed region when steps >= replicas
     dom = [capi.moe_profile_read(l.handle)[capi.PHASE_GATE_UP] for l in layers]
     dom_ms = float(np.mean(dom))
-    if dist is not None:
-        t = torch.tensor([ms, dom_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, dom_ms = float(t[0]), float(t[1])
+    ms, dom_ms = max_over_ranks([ms, dom_ms], dist, device="cuda")
     ok = all(torch.equal(bufs[0]["out"], b["out"]) for b in bufs[1:])
 
     # end to end through the public API with host buffers: H2D of x, route + FFN, D2H of out
@@ -360,10 +374,7 @@ def run_ours(args, cfg):
             stream.synchronize()
     if args.e2e:
         e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t[0])
+    e2e_s = max_over_ranks([e2e_s], dist, device="cuda")[0]
     h2d = T * cfg.H * 2 + (T * 4 if tok is not None else 0)
     d2h = T * cfg.H * 2
 
@@ -377,7 +388,7 @@ def run_ours(args, cfg):
         tr = TRAFFIC.get(cfg.name)
         traffic = tr[0] if tr and tr[1] == src else None
         line = {
-            "metric": METRIC, "value": T * world / (ms * 1e-3), "unit": "tokens/s",
+            "metric": METRIC, "value": job_tokens_per_s(T, world, ms * 1e-3), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "nvfp4 weights, f16 mma / f32 accumulate" if cfg.act == synth.ACT_BF16
@@ -406,7 +417,7 @@ def run_ours(args, cfg):
             "layer_roofline": {"achieved": layer_gbs, "peak": peak, "unit": "GB/s",
                                "frac": layer_gbs / peak, "bytes_per_step": nbytes["total"]},
             "clocks": clk,
-            "e2e": {"value": T * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_tokens_per_s(T, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
             "replica_outputs_equal": ok,
             "kernel_source": src,

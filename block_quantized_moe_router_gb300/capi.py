@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = range(5)
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_TOKEN_ID, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT = 1, 2, 4, 8
-MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID, MOE_SCORE_HASH = 0, 1, 2
+MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID, MOE_SCORE_HASH, MOE_SCORE_SQRTSOFTPLUS = 0, 1, 2, 3
 MOE_FMT_NVFP4, MOE_FMT_MXFP4 = 0, 1
 MOE_ACT_BF16, MOE_ACT_NVFP4 = 0, 1
 

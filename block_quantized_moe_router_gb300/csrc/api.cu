@@ -124,7 +124,7 @@ moe_status_t moe_route(const moe_route_desc* d, const void* x_bf16, const float*
     if (d->top_k < 1 || d->top_k > d->E || d->top_k > kMaxTopK) return MOE_ERR_INVALID_ARG;
     if (!std::isfinite(d->routed_scaling)) return MOE_ERR_INVALID_ARG;
     if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID &&
-        d->scoring != MOE_SCORE_HASH)
+        d->scoring != MOE_SCORE_HASH && d->scoring != MOE_SCORE_SQRTSOFTPLUS)
         return MOE_ERR_INVALID_ARG;
     if (d->scoring == MOE_SCORE_HASH && d->vocab < 1) return MOE_ERR_INVALID_ARG;
     if (d->scoring != MOE_SCORE_HASH && !logits_in && (d->H < 32 || d->H % 32))
@@ -146,7 +146,7 @@ moe_status_t moe_route(const moe_route_desc* d, const void* x_bf16, const float*
             return MOE_ERR_CUDA;
         logits = logits_out;
     }
-    const float* bias = d->scoring == MOE_SCORE_SIGMOID ? d->correction_bias : nullptr;
+    const float* bias = d->scoring != MOE_SCORE_SOFTMAX ? d->correction_bias : nullptr;
     return launch_topk(logits, bias, d->T, d->E, d->top_k, d->scoring, d->renormalize ? 1 : 0,
                        d->routed_scaling, topk_ids, topk_w, dev_status, st) == cudaSuccess
                ? MOE_OK : MOE_ERR_CUDA;

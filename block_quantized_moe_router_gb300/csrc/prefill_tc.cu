@@ -48,7 +48,8 @@ constexpr int kTcSfbOff = kTcSfaOff + kTcSfaBytes;
 constexpr int kTcStageBytes = kTcSfbOff + kTcSfbBytes;  // 55296 (54 KiB, 1 KiB multiple)
 constexpr int kTcSmemBytes = kTcStages * kTcStageBytes + 1024 + 256;
 constexpr uint32_t kTcTmemCols = 512;         // 256 accumulator + 4 stages x 48 scale columns
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;    // producer warp, MMA warp, 8 epilogue warps
+constexpr int kTcEpiThreads = 256;
 constexpr uint64_t kTcWaitLimit = 1ull << 26;  // polls before a wait is declared stuck
 
 // Byte offset of the scale of (row r of a 128-row block, 16-element block j of a 64-element
@@ -210,7 +211,7 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 128);
+        mbar_init(acc_empty, kTcEpiThreads);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -340,8 +341,12 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
             }
         }
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
+        // ---------------- epilogue (warps 2..9) ----------------
+        // Two warps per TMEM lane quarter, each owning half of the tile's columns: a warp copies
+        // its whole slice (128 columns) into registers and releases the accumulator at once, so
+        // the next tile's MMAs run while it computes and stores.
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int r = quad * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t acc_phase = 0;
@@ -352,65 +357,64 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
             }
             if (*abort_flag) break;
             tc_fence_after();
+            uint32_t V[128];
+            if (p.mode == 0) {  // gate columns [64 half, +64) and up columns [128 + 64 half, +64)
+#pragma unroll
+                for (int c = 0; c < 64; c += 16) {
+                    tmem_ld_16(trow + 64 * half + c, *reinterpret_cast<uint32_t(*)[16]>(V + c));
+                    tmem_ld_16(trow + 128 + 64 * half + c, *reinterpret_cast<uint32_t(*)[16]>(V + 64 + c));
+                }
+            } else {            // output columns [128 half, +128)
+#pragma unroll
+                for (int c = 0; c < 128; c += 16)
+                    tmem_ld_16(trow + 128 * half + c, *reinterpret_cast<uint32_t(*)[16]>(V + c));
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+            acc_phase ^= 1u;
+
             const int4 tl = p.tiles[tile];
             const int b = tl.x, nb = tl.y, e = tl.z;
             const bool sh = e == p.E;
             const int es = sh ? 0 : e;
             const int prow = b * 128 + r;
             const int pair = p.padrow_pair[prow];
+            if (pair < 0) continue;
             if (p.mode == 0) {
                 const float pg = (sh ? p.spost0 : p.post0)[es];
                 const float pu = (sh ? p.spost1 : p.post1)[es];
-                const int i0 = nb * 128;
-#pragma unroll 1
-                for (int c = 0; c < 128; c += 16) {
-                    uint32_t G[16], U[16];
-                    tmem_ld_16(trow + c, G);
-                    tmem_ld_16(trow + 128 + c, U);
-                    tmem_ld_wait();
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
                     float h[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        h[i] = silu_f32(__uint_as_float(G[i]) * pg) * (__uint_as_float(U[i]) * pu);
-                    if (pair >= 0) {
-                        const int i = i0 + c;
-                        uint8_t* sf = p.hsf + ((size_t)b * p.hsf_kblocks + (i >> 6)) * 512 +
-                                      sf_tile_offset(r, (i >> 4) & 3);
-                        quant16(h, p.g2, p.hq + (size_t)prow * p.hq_row_bytes + i / 2, sf, nullptr);
+                    for (int i = 0; i < 16; ++i) {
+                        const float gv = __uint_as_float(V[16 * blk + i]) * pg;
+                        const float uv = __uint_as_float(V[64 + 16 * blk + i]) * pu;
+                        h[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                     }
+                    const int i = nb * 128 + 64 * half + 16 * blk;
+                    uint8_t* sf = p.hsf + ((size_t)b * p.hsf_kblocks + (i >> 6)) * 512 +
+                                  sf_tile_offset(r, (i >> 4) & 3);
+                    quant16_rcp(h, p.g2, p.hq + (size_t)prow * p.hq_row_bytes + i / 2, sf);
                 }
             } else {
                 const float pd = (sh ? p.spost0 : p.post0)[es];
-                const float wgt = pair < 0 ? 0.f : (pair < p.P ? p.topk_w[pair] : 1.f);
-                const float sc = pd * wgt;
-                const int n0 = nb * 256;
-#pragma unroll 1
-                for (int c = 0; c < 256; c += 16) {
-                    uint32_t Y[16];
-                    tmem_ld_16(trow + c, Y);
-                    tmem_ld_wait();
-                    if (pair >= 0) {
-                        uint4 o0, o1;
-                        uint32_t* w0 = &o0.x;
-                        uint32_t* w1 = &o1.x;
+                const float sc = pd * (pair < p.P ? p.topk_w[pair] : 1.f);
+                uint4* dst = reinterpret_cast<uint4*>(p.y + (size_t)pair * p.H + nb * 256 + 128 * half);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            __nv_bfloat162 v0 = __floats2bfloat162_rn(__uint_as_float(Y[2 * i]) * sc,
-                                                                      __uint_as_float(Y[2 * i + 1]) * sc);
-                            __nv_bfloat162 v1 = __floats2bfloat162_rn(__uint_as_float(Y[8 + 2 * i]) * sc,
-                                                                      __uint_as_float(Y[9 + 2 * i]) * sc);
-                            w0[i] = *reinterpret_cast<uint32_t*>(&v0);
-                            w1[i] = *reinterpret_cast<uint32_t*>(&v1);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(p.y + (size_t)pair * p.H + n0 + c);
-                        dst[0] = o0;
-                        dst[1] = o1;
+                for (int c = 0; c < 128; c += 8) {
+                    uint4 o;
+                    uint32_t* ow = &o.x;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(V[c + 2 * i]) * sc,
+                                                                 __uint_as_float(V[c + 2 * i + 1]) * sc);
+                        ow[i] = *reinterpret_cast<uint32_t*>(&v);
                     }
+                    dst[c / 8] = o;
                 }
             }
-            tc_fence_before();
-            mbar_arrive(acc_empty);
-            acc_phase ^= 1u;
         }
     }
     tc_fence_before();

@@ -56,4 +56,28 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16* src, float (&v
     }
 }
 
+// The same recipe with the 16 per-element divisions replaced by one reciprocal per block
+// (v * (1 / denom)); the scale byte is computed exactly as above.  Used where the input is
+// itself an fp32 intermediate (h inside the tensor-core GEMM epilogue), so a code can differ
+// from the divided form only when v / denom lies within one ulp of an E2M1 midpoint.
+__device__ __forceinline__ void quant16_rcp(const float (&v)[16], float g, uint8_t* packed,
+                                            uint8_t* scale) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    float qs = amax / 6.0f;
+    qs = qs / g;
+    const uint32_t s = f32_to_e4m3(qs);
+    const float denom = e4m3_to_f32(s) * g;
+    const float inv = denom != 0.f ? 1.0f / denom : 0.f;
+    uint2 pk;
+    uint32_t bytes[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bytes[i] = f32x2_to_e2m1x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+    pk.x = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
+    pk.y = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+    *reinterpret_cast<uint2*>(packed) = pk;
+    *scale = (uint8_t)s;
+}
+
 }  // namespace moe

@@ -4,6 +4,7 @@
 //   softmax top-K           -- moe/init.rs, the `moe_topk_softmax` handles;
 //   sigmoid + correction bias (selection on sigmoid+bias, weights from the unbiased sigmoid,
 //     renormalised and scaled) -- moe/mod.rs, `correction_bias_dev` field doc;
+//   sqrt(softplus) scores in the same scheme -- moe/mod.rs, `moe_topk_sqrtsoftplus` handles;
 //   static hash routing through tid2eid [vocab, top_k] -- moe/init.rs, `new_with_hash` doc.
 // The router keeps fp32 logits (moe/mod.rs, `dense_gemm_f32out` field doc: an fp32-output
 // router GEMM feeding an fp32-input top-K).  Ids and weights stay on the device.
@@ -89,6 +90,12 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* _
 // complemented index), so one warp max per round picks the highest score with ties to the
 // lower index.  Non-finite logits get score -inf and weight 0.
 // ------------------------------------------------------------------------------------------
+// score of the sigmoid-style routers
+__device__ __forceinline__ float gate_score(int scoring, float l) {
+    if (scoring == MOE_SCORE_SQRTSOFTPLUS) return sqrtf(l > 30.f ? l : log1pf(expf(l)));
+    return 1.0f / (1.0f + expf(-l));
+}
+
 __device__ __forceinline__ uint32_t orderable(float v) {
     const uint32_t u = __float_as_uint(v);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -122,8 +129,7 @@ topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, in
             } else {
                 lg[j] = l;
                 lmax = fmaxf(lmax, l);
-                v = (scoring == MOE_SCORE_SOFTMAX) ? l
-                                                   : 1.0f / (1.0f + expf(-l)) + (bias ? bias[e] : 0.f);
+                v = (scoring == MOE_SCORE_SOFTMAX) ? l : gate_score(scoring, l) + (bias ? bias[e] : 0.f);
             }
             key[j] = ((unsigned long long)orderable(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
         }
@@ -154,7 +160,7 @@ topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, in
     if (lane < k) {
         const float l = row[my_e];
         if (isfinite(l))
-            num = (scoring == MOE_SCORE_SOFTMAX) ? expf(l - lmax) : 1.0f / (1.0f + expf(-l));
+            num = (scoring == MOE_SCORE_SOFTMAX) ? expf(l - lmax) : gate_score(scoring, l);
     }
     float den = 1.f;
     if (renorm) {

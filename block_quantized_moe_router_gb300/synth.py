@@ -31,7 +31,7 @@ import numpy as np
 import torch
 
 FMT_NVFP4, FMT_MXFP4 = 0, 1
-SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_HASH = 0, 1, 2
+SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_HASH, SCORE_SQRTSOFTPLUS = 0, 1, 2, 3
 ACT_BF16, ACT_NVFP4 = 0, 1
 
 
@@ -185,7 +185,7 @@ def make_inputs(cfg: MoeConfig, seed: int = 0, device="cpu",
             wr[:, H - 1] = zipf_logit_offsets(cfg, seed).float()
         inp["w_router"] = wr.to(torch.bfloat16)
     inp["x"] = x.to(torch.bfloat16)
-    if cfg.scoring == SCORE_SIGMOID:
+    if cfg.scoring in (SCORE_SIGMOID, SCORE_SQRTSOFTPLUS):
         inp["bias"] = (torch.rand((E,), generator=_gen(seed, 4), dtype=torch.float32) * 0.2 - 0.1)
     if cfg.scoring == SCORE_HASH:
         gt = _gen(seed, 5)

@@ -54,7 +54,12 @@ typedef enum {
 #define MOE_DEV_NONFINITE 0x4     /* a NaN/Inf router logit: ranked below every finite one   */
 #define MOE_DEV_TIMEOUT 0x8       /* a bounded device-side wait gave up                      */
 
-typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1, MOE_SCORE_HASH = 2 } moe_scoring_t;
+typedef enum {
+    MOE_SCORE_SOFTMAX = 0,
+    MOE_SCORE_SIGMOID = 1,
+    MOE_SCORE_HASH = 2,
+    MOE_SCORE_SQRTSOFTPLUS = 3
+} moe_scoring_t;
 typedef enum { MOE_FMT_NVFP4 = 0, MOE_FMT_MXFP4 = 1 } moe_fmt_t;
 /* Activation precision of the expert GEMMs.  BF16: W4A16 (bf16 tokens, dequantized
  * weights).  NVFP4: W4A4 -- tokens and the intermediate h are quantized to NVFP4 (per 16
@@ -87,7 +92,7 @@ typedef struct {
     int32_t renormalize;       /* 1: weights renormalised over the selected experts        */
     float routed_scaling;      /* multiplies every routing weight (1.0 for plain top-K)    */
     const void* w_router;      /* [device] bf16 [E][H], or NULL when logits are supplied   */
-    const float* correction_bias; /* [device] float [E] (sigmoid selection only) or NULL  */
+    const float* correction_bias; /* [device] float [E] (sigmoid/sqrt-softplus selection) or NULL */
     const int64_t* tid2eid;    /* [device] int64 [vocab][top_k] (hash only)               */
     int64_t vocab;
     const int32_t* token_ids;  /* [device] int32 [T] (hash only)                          */
@@ -99,6 +104,8 @@ typedef struct {
  *   Sigmoid: s = sigmoid(logits); selection ranks s + correction_bias; weight = s /
  *     sum(selected s) when renormalize, else s; times routed_scaling.  (moe/mod.rs,
  *     `correction_bias_dev` field doc.)
+ *   Sqrt(softplus): the sigmoid scheme with s = sqrt(log(1 + exp(logits))) (moe/mod.rs, the
+ *     `moe_topk_sqrtsoftplus` routing handles).
  *   Hash: ids = tid2eid[token_ids[t]] in table order; weight = routed_scaling / top_k.
  *     (moe/init.rs, `new_with_hash` doc.)
  * Ids are written in descending selection-score order, ties to the lower expert index.

@@ -24,7 +24,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libmoe_oracle.so")
 _lib = None
 
-SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_HASH = 0, 1, 2
+SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_HASH, SCORE_SQRTSOFTPLUS = 0, 1, 2, 3
 FMT_NVFP4, FMT_MXFP4 = 0, 1
 
 

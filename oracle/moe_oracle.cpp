@@ -10,8 +10,9 @@
 //       MXFP4 = packed E2M1 + E8M0 scale per 32 elements, no global.
 //   * routing -- softmax top-K (moe/init.rs, `moe_topk_softmax` handles), sigmoid scoring
 //     with a per-expert correction bias used for selection (moe/mod.rs, `correction_bias_dev`
-//     field doc), static hash routing through a tid2eid [vocab, top_k] i64 table
-//     (moe/init.rs, `new_with_hash` doc; moe/mod.rs, `tid2eid_dev` field doc).
+//     field doc), sqrt(softplus) scoring (moe/mod.rs, the `moe_topk_sqrtsoftplus` handles of
+//     the DeepSeek-V4 routing), static hash routing through a tid2eid [vocab, top_k] i64
+//     table (moe/init.rs, `new_with_hash` doc; moe/mod.rs, `tid2eid_dev` field doc).
 //   * per expert: gate+up projection, SiLU(gate)*up, down projection, then the top-K weighted
 //     sum plus an optional shared expert (moe/mod.rs module doc: "gate+up, silu+down" and
 //     `moe_weighted_sum_blend`).
@@ -30,6 +31,7 @@
 //     selection-score order; hash routing keeps the table's order.
 //   - sigmoid routing selects on sigmoid(logit)+bias, weights with the unbiased sigmoid,
 //     renormalised over the selected set and multiplied by the routed scaling factor.
+//   - sqrt(softplus) routing is the sigmoid scheme with the score sqrt(log(1 + e^logit)).
 //   - hash routing weights are 1/top_k.
 //   - the shared expert is added with weight 1.
 //   - Q: per 16 consecutive elements, s = E4M3_rne_satfinite(amax / 6 / g);
@@ -148,6 +150,12 @@ inline double bf16_to_double(uint16_t b) {
 }
 
 inline double sigmoid(double z) { return 1.0 / (1.0 + std::exp(-z)); }
+inline double sqrt_softplus(double z) {
+    const double sp = z > 30.0 ? z : std::log1p(std::exp(z));
+    return std::sqrt(sp);
+}
+// score of the sigmoid-style routers: 1 = sigmoid, 3 = sqrt(softplus)
+inline double gate_score(int scoring, double z) { return scoring == 3 ? sqrt_softplus(z) : sigmoid(z); }
 inline double silu(double z) { return z * sigmoid(z); }
 
 // One quantized matrix [rows, K] with its format.
@@ -248,7 +256,8 @@ void orc_dequant(const uint8_t* packed, const uint8_t* scales, double global, in
 }
 
 // ----- routing ------------------------------------------------------------------------------
-// scoring: 0 softmax, 1 sigmoid (+ correction bias for selection), 2 hash.
+// scoring: 0 softmax, 1 sigmoid (+ correction bias for selection), 2 hash,
+// 3 sqrt(softplus) (+ correction bias for selection).
 // Inputs: either x_bf16 [T,H] + w_router_bf16 [E,H] (router GEMM) or logits_in f32 [T,E].
 // Outputs: logits_out [T,E] fp64 (may be null), ids [T,k], w [T,k] fp64, score_out [T,E]
 // fp64 selection score (may be null).  Returns 0, or -1 on an invalid argument.
@@ -262,7 +271,7 @@ int orc_route(int T, int E, int H, int k, int scoring, int renorm, double scalin
               double* logits_out, int32_t* ids, double* w, double* score_out, int32_t* status_out,
               int nthreads) {
     build_tables();
-    if (T < 0 || E <= 0 || k <= 0 || k > E) return -1;
+    if (T < 0 || E <= 0 || k <= 0 || k > E || scoring < 0 || scoring > 3) return -1;
     std::vector<int32_t> tok_status(T, 0);
     if (scoring == 2) {
         for (int t = 0; t < T; ++t) {
@@ -306,7 +315,7 @@ int orc_route(int T, int E, int H, int k, int scoring, int renorm, double scalin
                 double l = logit[e];
                 if (!std::isfinite(l)) { nonfinite = true; v[e] = -INFINITY; continue; }
                 if (scoring == 0) v[e] = l;  // softmax is monotone in the logit
-                else v[e] = sigmoid(l) + (bias ? (double)bias[e] : 0.0);
+                else v[e] = gate_score(scoring, l) + (bias ? (double)bias[e] : 0.0);
             }
             if (nonfinite) tok_status[t] |= 4;
             if (score_out)
@@ -341,11 +350,11 @@ int orc_route(int T, int E, int H, int k, int scoring, int renorm, double scalin
                 double ssel = 0.0;
                 for (int j = 0; j < k; ++j) {
                     double l = logit[order[j]];
-                    if (std::isfinite(l)) ssel += sigmoid(l);
+                    if (std::isfinite(l)) ssel += gate_score(scoring, l);
                 }
                 for (int j = 0; j < k; ++j) {
                     int e = order[j];
-                    double s = std::isfinite(logit[e]) ? sigmoid(logit[e]) : 0.0;
+                    double s = std::isfinite(logit[e]) ? gate_score(scoring, logit[e]) : 0.0;
                     ids[t * k + j] = e;
                     w[t * k + j] = (renorm ? s / ssel : s) * scaling;
                 }

@@ -40,6 +40,8 @@ CASES = {
     "soft_norenorm": synth.MoeConfig("nn", T=17, H=512, I=128, E=64, k=6, scoring=synth.SCORE_SOFTMAX,
                                      renorm=False),
     "max_experts": synth.MoeConfig("mx", T=5, H=2048, I=128, E=512, k=8, scoring=synth.SCORE_SOFTMAX),
+    "sqrt_softplus": synth.MoeConfig("sq", T=21, H=1024, I=128, E=96, k=6,
+                                     scoring=synth.SCORE_SQRTSOFTPLUS, scaling=1.5),
     "pre4096": synth.CONFIGS["pre4096"],
 }
 

@@ -32,7 +32,15 @@ def _brute_topk(v, k):
     return best
 
 
-@pytest.mark.parametrize("scoring", [0, 1])
+def _score(scoring, l):
+    if scoring == 0:
+        return l
+    if scoring == 1:
+        return 1 / (1 + np.exp(-l))
+    return np.sqrt(np.log1p(np.exp(l)))   # sqrt(softplus)
+
+
+@pytest.mark.parametrize("scoring", [0, 1, 3])
 @pytest.mark.parametrize("E,k", [(6, 2), (8, 3), (10, 4), (5, 5)])
 def test_topk_matches_brute_force(orc, scoring, E, k):
     rng = np.random.default_rng(E * 10 + k + scoring)
@@ -43,7 +51,7 @@ def test_topk_matches_brute_force(orc, scoring, E, k):
                   logits_in=logits, bias=bias)
     for t in range(T):
         l = logits[t].astype(np.float64)
-        v = l if scoring == 0 else 1 / (1 + np.exp(-l)) + bias
+        v = l if scoring == 0 else _score(scoring, l) + bias
         assert set(r["ids"][t]) == _brute_topk(v, k)
         # descending selection score
         sel = v[r["ids"][t]]
@@ -80,7 +88,37 @@ def test_sigmoid_bias_selects_but_does_not_weight(orc):
     assert np.allclose(r_nr["w"][0], s, atol=1e-15)
 
 
-@pytest.mark.parametrize("scoring,scaling", [(0, 1.0), (1, 2.5)])
+def test_sqrt_softplus_weights_closed_form(orc):
+    rng = np.random.default_rng(21)
+    T, E, k = 6, 24, 5
+    logits = (rng.standard_normal((T, E)) * 3).astype(np.float32)
+    logits[0, 3] = 45.0   # deep in the linear tail of softplus
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    r = orc.route(T=T, E=E, k=k, scoring=3, renorm=True, scaling=1.5, logits_in=logits, bias=bias)
+    for t in range(T):
+        s = np.sqrt(np.log1p(np.exp(logits[t].astype(np.float64))))
+        ids = r["ids"][t]
+        assert np.allclose(r["w"][t], s[ids] / s[ids].sum() * 1.5, rtol=0, atol=1e-14)
+    assert 3 in r["ids"][0] and abs(np.sqrt(45.0) - np.sqrt(np.log1p(np.exp(45.0)))) < 1e-12
+
+
+def test_sqrt_softplus_special_values(orc):
+    # softplus(l) = a when l = ln(e^a - 1): a = 1, 4, 9 give scores 1, 2, 3 -> weights 1:2:3
+    a = np.array([1.0, 4.0, 9.0])
+    l = np.log(np.expm1(a))
+    logits = np.array([[l[0], -5.0, l[2], l[1], -7.0]], np.float32)
+    r = orc.route(T=1, E=5, k=3, scoring=3, renorm=True, scaling=1.0, logits_in=logits)
+    assert list(r["ids"][0]) == [2, 3, 0]
+    assert np.allclose(r["w"][0], [3 / 6, 2 / 6, 1 / 6], rtol=0, atol=1e-6)
+    # without a bias the ranking is the logit ranking, as for softmax (both are monotone)
+    rng = np.random.default_rng(8)
+    lg = (rng.standard_normal((16, 40)) * 4).astype(np.float32)
+    a = orc.route(T=16, E=40, k=7, scoring=3, logits_in=lg)
+    b = orc.route(T=16, E=40, k=7, scoring=0, logits_in=lg)
+    assert np.array_equal(a["ids"], b["ids"])
+
+
+@pytest.mark.parametrize("scoring,scaling", [(0, 1.0), (1, 2.5), (3, 1.0)])
 def test_weight_sum_invariant(orc, scoring, scaling):
     rng = np.random.default_rng(11)
     T, E, k = 64, 256, 8
