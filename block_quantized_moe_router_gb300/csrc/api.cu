@@ -256,6 +256,8 @@ moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g
         B.padrow_pair = reinterpret_cast<int32_t*>(base + ws.padrow_pair);
         B.tiles1 = reinterpret_cast<int4*>(base + ws.tiles1);
         B.tiles2 = reinterpret_cast<int4*>(base + ws.tiles2);
+        B.tokq = reinterpret_cast<uint8_t*>(base + ws.tokq);
+        B.toks = reinterpret_cast<uint8_t*>(base + ws.toks);
         B.xq = reinterpret_cast<uint8_t*>(base + ws.txq);
         B.xsf = reinterpret_cast<uint8_t*>(base + ws.txsf);
         B.hq = reinterpret_cast<uint8_t*>(base + ws.thq);

@@ -166,10 +166,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, c
 // moe_ffn_forward, so the workspace always matches the path).
 enum FfnPath { PATH_DECODE = 0, PATH_GENERIC = 1, PATH_TC = 2 };
 
-// The tcgen05 path needs NVFP4 weights and K / N extents in whole 256-element tiles.
+// The tcgen05 path needs K / N extents in whole 256-element tiles (NVFP4 or MXFP4 weights;
+// MXFP4 block scales are re-expressed as E4M3 powers of two at preparation).
 inline bool tc_shape_ok(int H, int I, int I_shared, int fmt_routed, int fmt_shared) {
-    return fmt_routed == MOE_FMT_NVFP4 && (I_shared == 0 || fmt_shared == MOE_FMT_NVFP4) &&
-           H % 256 == 0 && I % 256 == 0 && I_shared % 256 == 0;
+    (void)fmt_routed;
+    (void)fmt_shared;
+    return H % 256 == 0 && I % 256 == 0 && I_shared % 256 == 0;
 }
 
 inline int select_path(int T, int top_k, int act, bool tc_shape) {
@@ -182,7 +184,7 @@ inline int select_path(int T, int top_k, int act, bool tc_shape) {
 struct Workspace {
     size_t counts, offsets, active, meta, sorted_pair, pos_of_pair, x16, xq, xs, h16, hq, hs, y;
     // tcgen05 path
-    size_t mblock_expert, padrow_pair, tiles1, tiles2, txq, txsf, thq, thsf, ybf;
+    size_t mblock_expert, padrow_pair, tiles1, tiles2, tokq, toks, txq, txsf, thq, thsf, ybf;
     int max_blocks;
     size_t total;
     static Workspace plan(int E, int H, int I, int I_shared, int top_k, int T, int act, int path) {
@@ -223,6 +225,8 @@ struct Workspace {
             w.padrow_pair = take(sizeof(int32_t) * rows);
             w.tiles1 = take(16 * (size_t)w.max_blocks * (Imax / 128));
             w.tiles2 = take(16 * (size_t)w.max_blocks * (H / 256));
+            w.tokq = take((size_t)T * H / 2);   // each token quantized once
+            w.toks = take((size_t)T * H / 16);
             w.txq = take(rows * H / 2);
             w.txsf = take(rows * H / 16);
             w.thq = take(rows * Imax / 2);

@@ -62,4 +62,45 @@ __device__ __forceinline__ void frag_a(const ChunkA& c, uint32_t (&a)[4]) {
     a[3] = hmul2(e2m1x2_to_f16x2<SEL + 1>(w1), sc1);
 }
 
+// ---- asynchronous global -> shared copies (per-thread, no register staging) ----------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t saddr, const void* g) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t saddr, const void* g) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Block scales of a lane's 32-element chunk from the raw scale bits of its row and step:
+// NVFP4 -- the 8 bytes of the row's 128-element step, this lane's pair at byte 2q;
+// MXFP4 -- the 4 bytes of the row's step, this lane's byte at q.
+template <int FMT>
+__device__ __forceinline__ void scales_from_raw(uint2 raw, int q, int mxbias, uint32_t& lo,
+                                                uint32_t& hi) {
+    if constexpr (FMT == MOE_FMT_NVFP4) {
+        const uint32_t word = (q < 2) ? raw.x : raw.y;
+        const uint32_t s2 = (q & 1) ? (word >> 16) : (word & 0xFFFFu);
+        const uint32_t h = e4m3x2_to_f16x2(s2);
+        lo = __byte_perm(h, h, 0x1010);
+        hi = __byte_perm(h, h, 0x3232);
+    } else {
+        const int b = (int)((raw.x >> (8 * q)) & 0xFFu);
+        const int field = min(30, max(0, b - mxbias));
+        const uint32_t bits = (uint32_t)field << 10;
+        lo = hi = bits | (bits << 16);
+    }
+}
+
 }  // namespace moe

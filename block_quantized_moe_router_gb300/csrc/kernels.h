@@ -65,10 +65,16 @@ struct TcWeights {
     CUtensorMap gate, up, down, sh_gate, sh_up, sh_down;
     uint8_t *sf_gate = nullptr, *sf_up = nullptr, *sf_down = nullptr;
     uint8_t *sf_sh_gate = nullptr, *sf_sh_up = nullptr, *sf_sh_down = nullptr;
+    // per-expert post-scales seen by the MMA path: the NVFP4 globals, or for MXFP4 the power of
+    // two left over after the E8M0 scales were re-expressed as E4M3 (owned when MXFP4)
+    const float *post_gate = nullptr, *post_up = nullptr, *post_down = nullptr;
+    const float *post_sh_gate = nullptr, *post_sh_up = nullptr, *post_sh_down = nullptr;
+    float* owned_post[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
 };
 struct TcBuffers {  // workspace views
     int32_t *meta, *mblock_expert, *padrow_pair;
     int4 *tiles1, *tiles2;
+    uint8_t *tokq, *toks;  // tokens quantized once: codes [T][H/2], scales [T][H/16]
     uint8_t *xq, *xsf, *hq, *hsf;
     __nv_bfloat16* y;
     int max_blocks;
@@ -82,9 +88,10 @@ struct TcPrepArgs {
 };
 struct TcQuantArgs {
     const void* x;
-    int H, k, P;
+    int T, H, k, P;
     float g1;
     const int32_t *meta, *padrow_pair;
+    uint8_t *tokq, *toks;
     uint8_t *xq, *xsf;
 };
 struct TcTensorMaps {

@@ -11,8 +11,9 @@
 //                    padded-row -> pair map, per-128-row block -> expert map, and the two tile
 //                    lists (expert-major, then N block, then M block, so that concurrently
 //                    running CTAs share one expert's weight tile through L2);
-//   tc_quant_kernel  NVFP4 quantization of each pair's token into its padded row, the scales
-//                    written directly in the 128 x 4 scale-factor tile layout of the MMA;
+//   tc_quant_tokens_kernel / tc_gather_rows_kernel  NVFP4 quantization of every token once,
+//                    then a copy of each pair's token row into its padded row with the scales
+//                    rearranged into the 128 x 4 scale-factor tile layout of the MMA;
 //   tc_gemm_kernel   (gate+up) D[128 pairs][128 gate | 128 up] over K = H; the epilogue
 //                    computes h = SiLU(g) * u and requantizes it to NVFP4 (codes + scale tiles)
 //                    as the next GEMM's activation operand;
@@ -162,24 +163,38 @@ __global__ void __launch_bounds__(1024) tc_prep_kernel(TcPrepArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------
-// NVFP4 quantization of the tokens into the padded, expert-sorted rows
+// NVFP4 quantization of the tokens (once per token), then a copy into the padded,
+// expert-sorted rows with the scales rearranged into the MMA's scale tiles
 // ------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) tc_quant_kernel(TcQuantArgs a) {
-    const int rows = a.meta[2];
+__global__ void __launch_bounds__(256) tc_quant_tokens_kernel(TcQuantArgs a) {
     const int nb16 = a.H / 16;
-    const int64_t total = (int64_t)rows * nb16;
+    const int64_t total = (int64_t)a.T * nb16;
     const auto* x = static_cast<const __nv_bfloat16*>(a.x);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int prow = (int)(i / nb16), blk = (int)(i - (int64_t)prow * nb16);
+        float v[16];
+        load_bf16x16(x + i * 16, v);
+        quant16(v, a.g1, a.tokq + i * 8, a.toks + i, nullptr);
+    }
+}
+
+// one warp per padded row: 16-byte copies of the codes, 4-byte scale groups into the tiles
+__global__ void __launch_bounds__(256) tc_gather_rows_kernel(TcQuantArgs a) {
+    const int rows = a.meta[2];
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (int prow = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); prow < rows; prow += warps) {
         const int p = a.padrow_pair[prow];
         if (p < 0) continue;
         const int t = p < a.P ? p / a.k : p - a.P;
-        float v[16];
-        load_bf16x16(x + (size_t)t * a.H + blk * 16, v);
+        const uint4* src = reinterpret_cast<const uint4*>(a.tokq + (size_t)t * (a.H / 2));
+        uint4* dst = reinterpret_cast<uint4*>(a.xq + (size_t)prow * (a.H / 2));
+        for (int c = lane; c < a.H / 32; c += 32) dst[c] = src[c];
+        const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(a.toks + (size_t)t * (a.H / 16));
         const int mb = prow >> 7, r = prow & 127;
-        uint8_t* sf = a.xsf + ((size_t)mb * (a.H / 64) + (blk >> 2)) * 512 + sf_tile_offset(r, blk & 3);
-        quant16(v, a.g1, a.xq + (size_t)prow * (a.H / 2) + blk * 8, sf, nullptr);
+        for (int kb = lane; kb < a.H / 64; kb += 32)  // 4 scales (one 64-element K block)
+            *reinterpret_cast<uint32_t*>(a.xsf + ((size_t)mb * (a.H / 64) + kb) * 512 +
+                                         sf_tile_offset(r, 0)) = ssrc[kb];
     }
 }
 
@@ -475,6 +490,34 @@ __global__ void sf_tiles_kernel(const uint8_t* __restrict__ in, uint8_t* __restr
     }
 }
 
+// MXFP4: block scale 2^(b - 127) = 2^d * 2^(bmax - 135) with d = b - bmax + 8 <= 8, written as
+// the E4M3 byte of 2^d (exact for d >= -9; smaller blocks flush to zero); 32-element blocks
+// become two 16-element ones.  post[e] = 2^(bmax - 135), bmax = off[e] + 139.
+__device__ __forceinline__ uint8_t e8m0_as_e4m3(int b, int bmax) {
+    const int d = b - bmax + 8;
+    if (d >= -6) return (uint8_t)((d + 7) << 3);
+    if (d >= -9) return (uint8_t)(1 << (d + 9));
+    return 0;
+}
+
+__global__ void sf_tiles_mx_kernel(const uint8_t* __restrict__ in, const int32_t* __restrict__ off,
+                                   uint8_t* __restrict__ out, float* __restrict__ post, int E,
+                                   int N, int K) {
+    const int64_t total = (int64_t)E * N * (K / 16);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int kk = (int)(i % (K / 16));
+        const int64_t row = i / (K / 16);
+        const int e = (int)(row / N), n = (int)(row % N);
+        const int bmax = off[e] + 139;
+        const int b = in[row * (K / 32) + kk / 2];
+        const int rb = n >> 7, r = n & 127, kb = kk >> 2, j = kk & 3;
+        out[(((size_t)e * (N / 128) + rb) * (K / 64) + kb) * 512 + sf_tile_offset(r, j)] =
+            e8m0_as_e4m3(b, bmax);
+        if (i < E) post[i] = ldexpf(1.0f, off[i] + 4);  // 2^(bmax - 135)
+    }
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -502,35 +545,42 @@ static bool encode_rows(CUtensorMap* m, const void* base, uint64_t row_bytes, ui
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static cudaError_t make_sf_tiles(const uint8_t* scales, int E, int N, int K, uint8_t** out,
-                                 cudaStream_t st) {
+// Scale tiles of one projection; for MXFP4 also its MMA-path post-scales (owned).
+static cudaError_t make_sf_tiles(const ProjView& pv, int E, int N, int K, uint8_t** out,
+                                 const float** post, float** owned, cudaStream_t st) {
     const size_t bytes = (size_t)E * N * (K / 16);
     cudaError_t err = cudaMalloc(out, bytes);
     if (err != cudaSuccess) return err;
-    sf_tiles_kernel<<<1024, 256, 0, st>>>(scales, *out, E, N, K);
+    if (pv.fmt == MOE_FMT_NVFP4) {
+        sf_tiles_kernel<<<1024, 256, 0, st>>>(pv.scales, *out, E, N, K);
+        *post = pv.post;
+    } else {
+        if ((err = cudaMalloc(owned, sizeof(float) * E)) != cudaSuccess) return err;
+        sf_tiles_mx_kernel<<<1024, 256, 0, st>>>(pv.scales, pv.mx_off, *out, *owned, E, N, K);
+        *post = *owned;
+    }
     return cudaGetLastError();
 }
 
 bool tc_supported(int E, int H, int I, int I_shared, int fmt_routed, int fmt_shared) {
     (void)E;
-    return fmt_routed == MOE_FMT_NVFP4 && (I_shared == 0 || fmt_shared == MOE_FMT_NVFP4) &&
-           H % 256 == 0 && I % 256 == 0 && I_shared % 256 == 0 && encode_fn() != nullptr;
+    return tc_shape_ok(H, I, I_shared, fmt_routed, fmt_shared) && encode_fn() != nullptr;
 }
 
 cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, cudaStream_t st) {
     *tw = TcWeights{};
     const int E = L.E, H = L.H, I = L.I, Is = L.I_shared;
     cudaError_t err;
-    if ((err = make_sf_tiles(L.gate.scales, E, I, H, &tw->sf_gate, st)) != cudaSuccess) return err;
-    if ((err = make_sf_tiles(L.up.scales, E, I, H, &tw->sf_up, st)) != cudaSuccess) return err;
-    if ((err = make_sf_tiles(L.down.scales, E, H, I, &tw->sf_down, st)) != cudaSuccess) return err;
+    if ((err = make_sf_tiles(L.gate, E, I, H, &tw->sf_gate, &tw->post_gate, &tw->owned_post[0], st)) != cudaSuccess) return err;
+    if ((err = make_sf_tiles(L.up, E, I, H, &tw->sf_up, &tw->post_up, &tw->owned_post[1], st)) != cudaSuccess) return err;
+    if ((err = make_sf_tiles(L.down, E, H, I, &tw->sf_down, &tw->post_down, &tw->owned_post[2], st)) != cudaSuccess) return err;
     bool ok = encode_rows(&tw->gate, L.gate.packed, H / 2, (uint64_t)E * I, 128) &&
               encode_rows(&tw->up, L.up.packed, H / 2, (uint64_t)E * I, 128) &&
               encode_rows(&tw->down, L.down.packed, I / 2, (uint64_t)E * H, 256);
     if (Is > 0) {
-        if ((err = make_sf_tiles(L.sh_gate.scales, 1, Is, H, &tw->sf_sh_gate, st)) != cudaSuccess) return err;
-        if ((err = make_sf_tiles(L.sh_up.scales, 1, Is, H, &tw->sf_sh_up, st)) != cudaSuccess) return err;
-        if ((err = make_sf_tiles(L.sh_down.scales, 1, H, Is, &tw->sf_sh_down, st)) != cudaSuccess) return err;
+        if ((err = make_sf_tiles(L.sh_gate, 1, Is, H, &tw->sf_sh_gate, &tw->post_sh_gate, &tw->owned_post[3], st)) != cudaSuccess) return err;
+        if ((err = make_sf_tiles(L.sh_up, 1, Is, H, &tw->sf_sh_up, &tw->post_sh_up, &tw->owned_post[4], st)) != cudaSuccess) return err;
+        if ((err = make_sf_tiles(L.sh_down, 1, H, Is, &tw->sf_sh_down, &tw->post_sh_down, &tw->owned_post[5], st)) != cudaSuccess) return err;
         ok = ok && encode_rows(&tw->sh_gate, L.sh_gate.packed, H / 2, Is, 128) &&
              encode_rows(&tw->sh_up, L.sh_up.packed, H / 2, Is, 128) &&
              encode_rows(&tw->sh_down, L.sh_down.packed, Is / 2, H, 256);
@@ -548,6 +598,8 @@ void tc_release(TcWeights* tw) {
                         tw->sf_sh_down};
     for (uint8_t* b : bufs)
         if (b) cudaFree(b);
+    for (float* f : tw->owned_post)
+        if (f) cudaFree(f);
     *tw = TcWeights{};
 }
 
@@ -572,9 +624,11 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
     pa.meta = B.meta; pa.mblock_expert = B.mblock_expert; pa.padrow_pair = B.padrow_pair;
     pa.tiles1 = B.tiles1; pa.tiles2 = B.tiles2;
     TcQuantArgs qa{};
-    qa.x = L.x; qa.H = L.H; qa.k = L.k; qa.P = P; qa.g1 = L.g1; qa.meta = B.meta;
-    qa.padrow_pair = B.padrow_pair; qa.xq = B.xq; qa.xsf = B.xsf;
-    TC_PHASE(0, (tc_prep_kernel<<<1, 1024, 0, st>>>(pa), tc_quant_kernel<<<sms * 8, 256, 0, st>>>(qa)))
+    qa.x = L.x; qa.T = L.T; qa.H = L.H; qa.k = L.k; qa.P = P; qa.g1 = L.g1; qa.meta = B.meta;
+    qa.padrow_pair = B.padrow_pair; qa.tokq = B.tokq; qa.toks = B.toks; qa.xq = B.xq; qa.xsf = B.xsf;
+    TC_PHASE(0, (tc_prep_kernel<<<1, 1024, 0, st>>>(pa),
+                 tc_quant_tokens_kernel<<<sms * 8, 256, 0, st>>>(qa),
+                 tc_gather_rows_kernel<<<sms * 8, 256, 0, st>>>(qa)))
 
     TcTensorMaps m1{}, m2{};
     const uint64_t rows = (uint64_t)B.max_blocks * 128;
@@ -597,7 +651,7 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
     g1.tiles = B.tiles1; g1.num_tiles = B.meta + 0;
     g1.sfa = B.xsf; g1.sfa_kblocks = L.H / 64;
     g1.sfb0 = tw.sf_gate; g1.sfb1 = tw.sf_up; g1.ssfb0 = tw.sf_sh_gate; g1.ssfb1 = tw.sf_sh_up;
-    g1.post0 = L.gate.post; g1.post1 = L.up.post; g1.spost0 = L.sh_gate.post; g1.spost1 = L.sh_up.post;
+    g1.post0 = tw.post_gate; g1.post1 = tw.post_up; g1.spost0 = tw.post_sh_gate; g1.spost1 = tw.post_sh_up;
     TC_PHASE(1, (tc_gemm_kernel<<<sms, kTcThreads, kTcSmemBytes, st>>>(m1, g1)))
 
     TcGemmParams g2 = g;
@@ -605,7 +659,7 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
     g2.tiles = B.tiles2; g2.num_tiles = B.meta + 1;
     g2.sfa = B.hsf; g2.sfa_kblocks = Imax / 64;
     g2.sfb0 = tw.sf_down; g2.sfb1 = tw.sf_down; g2.ssfb0 = tw.sf_sh_down; g2.ssfb1 = tw.sf_sh_down;
-    g2.post0 = L.down.post; g2.post1 = L.down.post; g2.spost0 = L.sh_down.post; g2.spost1 = L.sh_down.post;
+    g2.post0 = tw.post_down; g2.post1 = tw.post_down; g2.spost0 = tw.post_sh_down; g2.spost1 = tw.post_sh_down;
     TC_PHASE(2, (tc_gemm_kernel<<<sms, kTcThreads, kTcSmemBytes, st>>>(m2, g2)))
 
     TcCombineArgs ca{};

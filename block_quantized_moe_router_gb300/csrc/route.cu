@@ -85,6 +85,112 @@ router_logits_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* _
 }
 
 // ------------------------------------------------------------------------------------------
+// Router logits for many tokens: CTA tile 128 tokens x 64 experts, K staged 64 at a time
+// through a 3-stage cp.async ring in shared memory (rows padded to 144 bytes so ldmatrix is
+// conflict-free), 8 warps of 32 tokens x 32 experts on bf16 m16n8k16 MMAs, fp32 accumulation.
+// Rows beyond T or E are zero-filled by the copies and never stored.
+// ------------------------------------------------------------------------------------------
+constexpr int kRgBM = 128, kRgBN = 64, kRgBK = 64, kRgStages = 3;
+constexpr int kRgRow = kRgBK * 2 + 16;  // bytes per staged row (64 bf16 + 16 bytes of padding)
+constexpr int kRgSmem = kRgStages * (kRgBM + kRgBN) * kRgRow;
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t saddr, const void* g, bool valid) {
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t saddr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(saddr));
+}
+
+__global__ void __launch_bounds__(256)
+router_gemm_tiled_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wr,
+                         float* __restrict__ logits, int T, int E, int H) {
+    extern __shared__ __align__(16) uint8_t rsm[];
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * kRgBM, e0 = blockIdx.y * kRgBN;
+    const int wm = warp & 3, wn = warp >> 2;  // warp tile: tokens 32 wm.., experts 32 wn..
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(rsm));
+    auto a_row = [&](int st, int r) { return sbase + (st * (kRgBM + kRgBN) + r) * kRgRow; };
+    auto b_row = [&](int st, int r) { return sbase + (st * (kRgBM + kRgBN) + kRgBM + r) * kRgRow; };
+    const int nk = H / kRgBK;
+
+    auto issue = [&](int kt) {
+        if (kt < nk) {
+            const int st = kt % kRgStages;
+            // 128 token rows + 64 expert rows, 8 x 16 bytes each: 1536 chunks over 256 threads
+            for (int c = tid; c < (kRgBM + kRgBN) * 8; c += 256) {
+                const int r = c >> 3, j = c & 7;
+                if (r < kRgBM) {
+                    const int t = t0 + r;
+                    cp_async16_zfill(a_row(st, r) + j * 16,
+                                     x + (size_t)(t < T ? t : 0) * H + kt * kRgBK + j * 8, t < T);
+                } else {
+                    const int e = e0 + r - kRgBM;
+                    cp_async16_zfill(b_row(st, r - kRgBM) + j * 16,
+                                     wr + (size_t)(e < E ? e : 0) * H + kt * kRgBK + j * 8, e < E);
+                }
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    float acc[2][4][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[i][j][c] = 0.f;
+
+#pragma unroll
+    for (int kt = 0; kt < kRgStages - 1; ++kt) issue(kt);
+    for (int kt = 0; kt < nk; ++kt) {
+        issue(kt + kRgStages - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRgStages - 1) : "memory");
+        __syncthreads();
+        const int st = kt % kRgStages;
+#pragma unroll
+        for (int kk = 0; kk < kRgBK; kk += 16) {
+            uint32_t a[2][4], b[4][2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)  // 16 tokens x 16 k per fragment
+                ldmatrix_x4(a_row(st, wm * 32 + i * 16 + (lane & 15)) + (kk + (lane >> 4) * 8) * 2,
+                            a[i][0], a[i][1], a[i][2], a[i][3]);
+#pragma unroll
+            for (int j = 0; j < 4; j += 2) {  // two 8-expert tiles per ldmatrix.x4
+                const int r = wn * 32 + j * 8 + (lane & 7) + ((lane >> 4) << 3);
+                ldmatrix_x4(b_row(st, r) + (kk + ((lane >> 3) & 1) * 8) * 2, b[j][0], b[j][1],
+                            b[j + 1][0], b[j + 1][1]);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma_bf16_16816(acc[i][j], a[i][0], a[i][1], a[i][2], a[i][3], b[j][0], b[j][1]);
+        }
+        __syncthreads();  // the stage is refilled by the next iteration's copies
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int t = t0 + wm * 32 + i * 16 + g + ((c & 2) ? 8 : 0);
+                const int e = e0 + wn * 32 + j * 8 + 2 * q + (c & 1);
+                if (t < T && e < E) logits[(size_t)t * E + e] = acc[i][j][c];
+            }
+}
+
+// ------------------------------------------------------------------------------------------
 // Top-K over fp32 logits: one warp per token; lane l holds experts l, l+32, ... (EPL of them).
 // Each expert gets a 64-bit key (order-preserving bits of its selection score, then the
 // complemented index), so one warp max per round picks the highest score with ties to the
@@ -218,6 +324,22 @@ cudaError_t launch_router_logits(const void* x, const void* wr, float* logits, i
     if (T <= 8) {
         return launch_pdl(router_logits_kernel<1, 16>, dim3((E + 15) / 16, (T + 7) / 8),
                           dim3(16 * 32), st, xb, wb, logits, T, E, H);
+    }
+    if (H % kRgBK == 0) {
+        cudaError_t err = cudaFuncSetAttribute(router_gemm_tiled_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kRgSmem);
+        if (err != cudaSuccess) return err;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((T + kRgBM - 1) / kRgBM, (E + kRgBN - 1) / kRgBN);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = kRgSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, router_gemm_tiled_kernel, xb, wb, logits, T, E, H);
     }
     return launch_pdl(router_logits_kernel<4, 8>, dim3((E + 15) / 16, (T + 31) / 32),
                       dim3(8 * 32), st, xb, wb, logits, T, E, H);

@@ -58,18 +58,27 @@ SMALL = {
                                   scoring=S.SCORE_SOFTMAX, I_shared=512, act=S.ACT_NVFP4),
     "tc_t1": S.MoeConfig("tc_t1", T=1, H=256, I=256, E=8, k=2, scoring=S.SCORE_SOFTMAX,
                          I_shared=256, act=S.ACT_NVFP4),
+    # MXFP4 weights on the tensor-core path (E8M0 scales re-expressed as E4M3 powers of two)
+    "tc_mx_routed": S.MoeConfig("tc_mx_routed", T=150, H=768, I=512, E=8, k=3,
+                                scoring=S.SCORE_SQRTSOFTPLUS, I_shared=256, fmt=S.FMT_MXFP4,
+                                shared_fmt=S.FMT_NVFP4, act=S.ACT_NVFP4),
+    "tc_mx_hash": S.MoeConfig("tc_mx_hash", T=64, H=512, I=512, E=16, k=6, scoring=S.SCORE_HASH,
+                              I_shared=512, fmt=S.FMT_MXFP4, shared_fmt=S.FMT_NVFP4, vocab=500,
+                              act=S.ACT_NVFP4),
 }
 
 
-def _run(cfg, inp):
+def _run(cfg, inp, with_logits=False):
     layer = MoeLayer.from_inputs(inp)
     x = inp["x"].cuda()
     tok = inp["token_ids"].cuda() if "token_ids" in inp else None
-    ids, w, _ = layer.route(x, token_ids=tok)
+    ids, w, logits = layer.route(x, token_ids=tok)
     out = layer.ffn(x, ids, w)
     torch.cuda.synchronize()
     status = int(layer.status.item())
     layer.close()
+    if with_logits:
+        return ids, w, out, status, logits
     return ids, w, out, status
 
 
@@ -78,9 +87,9 @@ def test_small_configs(cuda_lib, name):
     cfg = SMALL[name]
     inp, _ = parity.make_case(cfg, seed=1, device="cpu")
     ref_r = parity.oracle_route(cfg, inp)
-    ids, w, out, status = _run(cfg, inp)
+    ids, w, out, status, logits = _run(cfg, inp, with_logits=True)
     assert status == 0
-    parity.assert_routing(cfg, ref_r, ids, w)
+    parity.assert_routing(cfg, ref_r, ids, w, gpu_logits=logits, inp=inp)
     ref = parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"])
     parity.assert_close(out, ref, name)
 
@@ -98,9 +107,9 @@ def test_full_size_configs(cuda_lib, name):
     cfg, sample = FULL[name]
     inp, _ = parity.make_case(cfg, seed=0, device="cuda")
     ref_r = parity.oracle_route(cfg, inp)
-    ids, w, out, status = _run(cfg, inp)
+    ids, w, out, status, logits = _run(cfg, inp, with_logits=True)
     assert status == 0
-    parity.assert_routing(cfg, ref_r, ids, w)
+    parity.assert_routing(cfg, ref_r, ids, w, gpu_logits=logits, inp=inp)
     ref = parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"], tokens=sample)
     got = out if sample is None else out[sample]
     parity.assert_close(got, ref, name)

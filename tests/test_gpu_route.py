@@ -56,7 +56,7 @@ def test_router_and_topk(cuda_lib, name):
     assert status == 0
     lg = logits.double().cpu().numpy()
     assert np.max(np.abs(lg - ref["logits"])) <= 1e-4 * max(1.0, np.max(np.abs(ref["logits"])))
-    parity.assert_routing(cfg, ref, ids, w)
+    parity.assert_routing(cfg, ref, ids, w, gpu_logits=logits, inp=inp)
 
 
 def test_logits_in_and_nonfinite(cuda_lib):
