@@ -55,8 +55,9 @@ __device__ __forceinline__ void dec_dispatch(const FfnLaunch& L, DecDispatch& D)
     if (tid < 32) {  // one warp: at most 64 ids, two per lane
         const int lane = tid, P = L.T * L.k;
         int e0 = -1, e1 = -1;
-        if (lane < P) e0 = L.ids[lane];
-        if (lane + 32 < P) e1 = L.ids[lane + 32];
+        float w0 = 0.f, w1 = 0.f;  // loaded with the ids: one global round trip
+        if (lane < P) { e0 = L.ids[lane]; w0 = L.w[lane]; }
+        if (lane + 32 < P) { e1 = L.ids[lane + 32]; w1 = L.w[lane + 32]; }
         if (e0 >= 0 && e0 < L.E) atomicOr(&D.bitmap[e0 >> 5], 1u << (e0 & 31));
         if (e1 >= 0 && e1 < L.E) atomicOr(&D.bitmap[e1 >> 5], 1u << (e1 & 31));
         __syncwarp();
@@ -79,7 +80,7 @@ __device__ __forceinline__ void dec_dispatch(const FfnLaunch& L, DecDispatch& D)
                 const int t = p / L.k;
                 D.expert[slot] = e;
                 atomicOr(&D.tokmask[slot], 1u << t);
-                atomicAdd(&D.w[slot][t], L.w[p]);  // a table may route a token to an expert twice
+                atomicAdd(&D.w[slot][t], h ? w1 : w0);  // a table may route a token to an expert twice
             }
         }
         if (lane == 0) {
@@ -243,6 +244,8 @@ __global__ void __launch_bounds__(kGuWarps * 32, 3) dec_gateup_kernel(FfnLaunch 
     __shared__ DecDispatch D;
     pdl_wait();  // ids / w come from the routing kernels
     dec_dispatch(L, D);
+    // let the down kernel's CTAs start now: they stream their weights while this grid runs
+    pdl_trigger();
     const int nslots = D.n_active + (L.I_shared > 0 ? 1 : 0);
     const int warp = threadIdx.x >> 5;
     uint8_t* ring = dsm + warp * kGuStages * kGuStageBytes;
@@ -256,15 +259,18 @@ __global__ void __launch_bounds__(kGuWarps * 32, 3) dec_gateup_kernel(FfnLaunch 
         if (shared) dec_gateup_task<FMT_S>(L, D, slot, n0, ring, red);
         else dec_gateup_task<FMT_R>(L, D, slot, n0, ring, red);
     }
-    pdl_trigger();
 }
 
 // ------------------------------------------------------------------------------------------
 // down + weighted sum + shared expert
+//
+// The down weights depend only on the routing, not on h, so the CTAs (launched while the
+// gate+up grid still runs) issue their first kDnStages - 1 weight steps before waiting for h.
+// h itself is read from L2 one step ahead in registers.
 // ------------------------------------------------------------------------------------------
 constexpr int kDnWarps = 8;
-constexpr int kDnStages = 3;
-constexpr int kDnStageBytes = 2 * 512 + 4 * 512 + 32 * 8;  // codes, h, scales
+constexpr int kDnStages = 6;
+constexpr int kDnStageBytes = 2 * 512 + 32 * 8;  // codes of rows g and g+8, scales
 constexpr int kDnSmem = kDnWarps * kDnStages * kDnStageBytes + kDnWarps * 4 * 32 * 4;
 
 template <int FMT_R, int FMT_S>
@@ -272,7 +278,7 @@ __global__ void __launch_bounds__(kDnWarps * 32) dec_down_kernel(FfnLaunch L) {
     extern __shared__ __align__(16) uint8_t dsm[];
     __shared__ DecDispatch D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    pdl_wait();  // h comes from the gate+up kernel
+    // the routing ids were complete before the gate+up grid let this grid start
     dec_dispatch(L, D);
     const int n0 = blockIdx.x * 16;
     const int nslots = D.n_active + (L.I_shared > 0 ? 1 : 0);
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(kDnWarps * 32) dec_down_kernel(FfnLaunch L) {
     for (int slot = warp; slot < nslots; slot += kDnWarps)
         total += (slot == D.n_active ? L.I_shared : L.I) / 128;
 
-    int is_slot = warp, is_s = 0;  // issue cursor
+    int is_slot = warp, is_s = 0;  // weight issue cursor
     auto issue = [&](int i) {
         if (i < total) {
             const bool sh = is_slot == D.n_active;
@@ -298,16 +304,10 @@ __global__ void __launch_bounds__(kDnWarps * 32) dec_down_kernel(FfnLaunch L) {
             const uint32_t st = rbase + (i % kDnStages) * kDnStageBytes;
             cp_async16(st + lane * 16, PD.packed + rowA * (K / 2) + 16 * q + is_s * 64);
             cp_async16(st + 512 + lane * 16, PD.packed + (rowA + 8) * (K / 2) + 16 * q + is_s * 64);
-            if ((D.tokmask[is_slot] >> g) & 1u) {  // column g = token g
-                const __half* hrow =
-                    L.h16 + ((size_t)is_slot * kDecMaxT + g) * Imax + 32 * q + is_s * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) cp_async16(st + 1024 + c * 512 + lane * 16, hrow + 8 * c);
-            }
             if (q < 2) {  // scales of row g + 8q
                 const uint8_t* sp = PD.scales + (rowA + 8 * q) * (K / svb);
-                if (svb == 16) cp_async8(st + 3072 + lane * 8, sp + is_s * 8);
-                else cp_async4(st + 3072 + lane * 8, sp + is_s * 4);
+                if (svb == 16) cp_async8(st + 1024 + lane * 8, sp + is_s * 8);
+                else cp_async4(st + 1024 + lane * 8, sp + is_s * 4);
             }
             if (++is_s == K / 128) {
                 is_s = 0;
@@ -316,28 +316,39 @@ __global__ void __launch_bounds__(kDnWarps * 32) dec_down_kernel(FfnLaunch L) {
         }
         cp_async_commit();
     };
+#pragma unroll 1
+    for (int i = 0; i < kDnStages - 1; ++i) issue(i);
+
+    pdl_wait();  // h comes from the gate+up kernel
+
+    int hs_slot = warp, hs_s = 0;  // h cursor (one step ahead of the compute)
+    auto load_h = [&](uint4 (&b)[4]) {
+        const bool ok = hs_slot < nslots && ((D.tokmask[hs_slot] >> g) & 1u);  // column g = token g
+        const __half* hrow = L.h16 + ((size_t)hs_slot * kDecMaxT + g) * Imax + 32 * q + hs_s * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) b[j] = ok ? ldg_cached128(hrow + 8 * j) : make_uint4(0, 0, 0, 0);
+        if (hs_slot < nslots && ++hs_s == (hs_slot == D.n_active ? L.I_shared : L.I) / 128) {
+            hs_s = 0;
+            hs_slot += kDnWarps;
+        }
+    };
+    uint4 hb[4], hn[4];
+    if (total > 0) load_h(hb);
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, part[4] = {0.f, 0.f, 0.f, 0.f};
     int cs_slot = warp, cs_s = 0;  // consume cursor
-#pragma unroll
-    for (int i = 0; i < kDnStages - 1; ++i) issue(i);
     for (int i = 0; i < total; ++i) {
         issue(i + kDnStages - 1);
+        if (i + 1 < total) load_h(hn);
         cp_async_wait<kDnStages - 1>();
         __syncwarp();
         const bool sh = cs_slot == D.n_active;
         const int e = D.expert[cs_slot];
         const uint8_t* st = ring + (i % kDnStages) * kDnStageBytes;
-        const bool tok_ok = (D.tokmask[cs_slot] >> g) & 1u;
         ChunkA c;
         c.r0 = *reinterpret_cast<const uint4*>(st + lane * 16);
         c.r1 = *reinterpret_cast<const uint4*>(st + 512 + lane * 16);
-        const uint2* sc = reinterpret_cast<const uint2*>(st + 3072);
-        uint4 b[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            b[j] = tok_ok ? *reinterpret_cast<const uint4*>(st + 1024 + j * 512 + lane * 16)
-                          : make_uint4(0, 0, 0, 0);
+        const uint2* sc = reinterpret_cast<const uint2*>(st + 1024);
         if ((sh ? FMT_S : FMT_R) == MOE_FMT_NVFP4) {
             scales_from_raw<MOE_FMT_NVFP4>(sc[g * 4 + 0], q, 0, c.s0lo, c.s0hi);
             scales_from_raw<MOE_FMT_NVFP4>(sc[g * 4 + 1], q, 0, c.s1lo, c.s1hi);
@@ -347,16 +358,18 @@ __global__ void __launch_bounds__(kDnWarps * 32) dec_down_kernel(FfnLaunch L) {
             scales_from_raw<MOE_FMT_MXFP4>(sc[g * 4 + 1], q, mx, c.s1lo, c.s1hi);
         }
         __syncwarp();  // every lane has read this stage before it is refilled
-#define DOWN_STEP(I)                                                                     \
-    {                                                                                    \
-        uint32_t fa[4];                                                                  \
-        frag_a<I>(c, fa);                                                                \
-        mma_f16_16816(part, fa[0], fa[1], fa[2], fa[3], word_of(b[I >> 1], (I & 1) * 2), \
-                      word_of(b[I >> 1], (I & 1) * 2 + 1));                              \
+#define DOWN_STEP(I)                                                                       \
+    {                                                                                      \
+        uint32_t fa[4];                                                                    \
+        frag_a<I>(c, fa);                                                                  \
+        mma_f16_16816(part, fa[0], fa[1], fa[2], fa[3], word_of(hb[I >> 1], (I & 1) * 2),  \
+                      word_of(hb[I >> 1], (I & 1) * 2 + 1));                               \
     }
         DOWN_STEP(0) DOWN_STEP(1) DOWN_STEP(2) DOWN_STEP(3)
         DOWN_STEP(4) DOWN_STEP(5) DOWN_STEP(6) DOWN_STEP(7)
 #undef DOWN_STEP
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hb[j] = hn[j];
         const int K = sh ? L.I_shared : L.I;
         if (++cs_s == K / 128) {  // expert done: fold in with its post-scale and token weights
             const float post = (sh ? L.sh_down : L.down).post[e];
@@ -425,7 +438,7 @@ static cudaError_t launch_decode_fmt(const FfnLaunch& L, int phase, cudaStream_t
         const int tiles = Imax / 16;
         const int slots = (L.E < L.T * L.k ? L.E : L.T * L.k) + (L.I_shared > 0 ? 1 : 0);
         int grid = slots * tiles;
-        if (grid > 3 * sms) grid = 3 * sms;  // three resident CTAs per SM; CTAs loop over tasks
+        if (grid > 2 * sms) grid = 2 * sms;  // two per SM, leaving room for the down kernel
         if ((err = set_smem(dec_gateup_kernel<FR, FS>, kGuSmem)) != cudaSuccess) return err;
         return launch_pdl_smem(dec_gateup_kernel<FR, FS>, dim3(grid), dim3(kGuWarps * 32), kGuSmem,
                                st, L, tiles);
