@@ -162,7 +162,14 @@ def step_bytes(cfg, n_touched):
     pairs = cfg.T * cfg.k
     return {"gate_up": n_touched * gate_up + sh_gate_up + cfg.T * H * 2,
             "total": n_touched * (gate_up + down) + sh_gate_up + sh_down + router + acts,
-            "gate_up_flops": 2 * 2 * I * H * pairs + (2 * 2 * Is * H * cfg.T if Is else 0)}
+            "gate_up_flops": 2 * 2 * I * H * pairs + (2 * 2 * Is * H * cfg.T if Is else 0),
+            "flops": 2 * 3 * I * H * pairs + (2 * 3 * Is * H * cfg.T if Is else 0)
+            + (2 * cfg.T * H * cfg.E if cfg.scoring != synth.SCORE_HASH else 0)}
+
+
+def is_decode(cfg):
+    """The few-token case that runs as one persistent launch (route + FFN)."""
+    return cfg.T <= 8 and cfg.T * cfg.k <= 64 and cfg.act == synth.ACT_BF16
 
 
 # ------------------------------------------------------------------------------------------
@@ -308,18 +315,18 @@ def run_ours(args, cfg):
 
     stream = torch.cuda.Stream()
     graphs = []
+    def step(layer, b):  # one layer step through the public API: route + FFN in one call
+        layer.forward(x, token_ids=tok, out=b["out"], topk_ids=b["ids"], topk_w=b["w"],
+                      logits_out=None if tok is not None else b["logits"])
+
     with torch.cuda.stream(stream):
         for layer, b in zip(layers, bufs):   # one eager pass per replica before capture
-            layer.route(x, token_ids=tok, topk_ids=b["ids"], topk_w=b["w"],
-                        logits_out=None if tok is not None else b["logits"])
-            layer.ffn(x, b["ids"], b["w"], out=b["out"])
+            step(layer, b)
         stream.synchronize()
         for layer, b in zip(layers, bufs):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                layer.route(x, token_ids=tok, topk_ids=b["ids"], topk_w=b["w"],
-                            logits_out=None if tok is not None else b["logits"])
-                layer.ffn(x, b["ids"], b["w"], out=b["out"])
+                step(layer, b)
             graphs.append(g)
     torch.cuda.synchronize()
 
@@ -370,7 +377,7 @@ def run_ours(args, cfg):
             x_dev.copy_(x_host, non_blocking=True)
             if tok_dev is not None:
                 tok_dev.copy_(tok_host, non_blocking=True)
-            o = layer.forward(x_dev, token_ids=tok_dev)
+            o = layer.forward(x_dev, token_ids=tok_dev)[0]
             out_host.copy_(o, non_blocking=True)
             stream.synchronize()
     if args.e2e:
@@ -381,9 +388,15 @@ def run_ours(args, cfg):
 
     if rank == 0:
         peak, bf16_peak, peak_kind = measured_peaks()
-        achieved = nbytes["gate_up"] / (dom_ms * 1e-3) / 1e9
+        dec = is_decode(cfg)
+        # dominant kernel: the whole-layer persistent kernel for a few tokens, else gate+up
+        dom_bytes = nbytes["total"] if dec else nbytes["gate_up"]
+        dom_flops = nbytes["flops"] if dec else nbytes["gate_up_flops"]
+        dom_name = ("dec_fused_kernel (route + FFN)" if dec else "gate+up GEMM (" +
+                    ("tc_gemm_kernel" if cfg.act == synth.ACT_NVFP4 else "expert_mma_kernel") + ")")
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
         fp4_peak = bf16_peak * FP4_OVER_BF16
-        tflops = nbytes["gate_up_flops"] / (dom_ms * 1e-3) / 1e12
+        tflops = dom_flops / (dom_ms * 1e-3) / 1e12
         layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
         src = kernel_source_hash()
         tr = TRAFFIC.get(cfg.name)
@@ -402,17 +415,14 @@ def run_ours(args, cfg):
                        "touched_experts": touched},
             "gpu_launches": args.steps * launches_per_step(cfg),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "gate+up GEMM (" + ("tc_gemm_kernel" if cfg.act == synth.ACT_NVFP4
-                                                       else "dec_gateup_kernel" if cfg.T <= 8
-                                                       else "expert_mma_kernel") + ")",
-                         "bytes_per_launch": nbytes["gate_up"], "launch_ms": dom_ms,
+                         "frac": achieved / peak, "traffic": traffic, "kernel": dom_name,
+                         "bytes_per_launch": dom_bytes, "launch_ms": dom_ms,
                          "peak_source": peak_kind},
             "tensor_view": {"achieved_tflops": tflops,
                             "peak_tflops": fp4_peak if cfg.act == synth.ACT_NVFP4 else bf16_peak,
                             "frac": tflops / (fp4_peak if cfg.act == synth.ACT_NVFP4 else bf16_peak),
                             "dtype": "nvfp4 x nvfp4" if cfg.act == synth.ACT_NVFP4 else "f16 mma",
-                            "flops_per_launch": nbytes["gate_up_flops"],
+                            "flops_per_launch": dom_flops,
                             "peak_source": peak_kind + " bf16 x nominal fp4/bf16 ratio"
                             if cfg.act == synth.ACT_NVFP4 else peak_kind},
             "layer_roofline": {"achieved": layer_gbs, "peak": peak, "unit": "GB/s",
@@ -447,10 +457,13 @@ def host_inputs_from(inp):
 
 
 def launches_per_step(cfg):
-    """Kernels one step launches: router GEMM + top-K (or the hash lookup), then dispatch,
-    gate+up GEMM, down GEMM and combine."""
+    """Kernels one step launches.  A few tokens: one persistent kernel.  Otherwise router
+    GEMM + top-K (or the hash lookup), then the FFN: tcgen05 path -- prep, token quantizer,
+    row gather, gate+up GEMM, down GEMM, combine; mma path -- prep, gate+up, down, combine."""
+    if is_decode(cfg):
+        return 1
     route = 1 if cfg.scoring == synth.SCORE_HASH else 2
-    return route + 4
+    return route + (6 if cfg.act == synth.ACT_NVFP4 else 4)
 
 
 def main():

@@ -24,7 +24,7 @@ MOE_ACT_BF16, MOE_ACT_NVFP4 = 0, 1
 
 # Every symbol include/moe.h declares.
 EXPORTED = ["moe_route", "moe_workspace_size", "moe_prepare_weights", "moe_release_weights",
-            "moe_ffn_forward", "moe_ffn_forward_noalloc", "moe_quantize_act_nvfp4",
+            "moe_ffn_forward", "moe_forward", "moe_ffn_forward_noalloc", "moe_quantize_act_nvfp4",
             "moe_profile_enable", "moe_profile_read", "moe_status_string"]
 
 
@@ -79,6 +79,9 @@ def load_library(path: str = LIB_PATH):
     lib.moe_release_weights.restype = ctypes.c_int
     lib.moe_ffn_forward.argtypes = [vp, i32, i32, f32, f32, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.moe_ffn_forward.restype = ctypes.c_int
+    lib.moe_forward.argtypes = [vp, ctypes.POINTER(moe_route_desc), i32, f32, f32, vp, vp, vp, vp,
+                                vp, vp, vp, sz, vp, vp]
+    lib.moe_forward.restype = ctypes.c_int
     lib.moe_ffn_forward_noalloc.argtypes = [vp, i32, i32, f32, f32, vp, vp, vp, vp, vp, vp]
     lib.moe_ffn_forward_noalloc.restype = ctypes.c_int
     lib.moe_quantize_act_nvfp4.argtypes = [vp, i64, i64, f32, vp, vp, vp]
@@ -131,15 +134,23 @@ def ffn_desc(E, H, I, top_k, I_shared, gate, up, down, sh_gate=None, sh_up=None,
                         qtensor(sh_gate), qtensor(sh_up), qtensor(sh_down))
 
 
+def route_desc(*, T, E, H, top_k, scoring, renormalize, routed_scaling, w_router=None,
+               correction_bias=None, tid2eid=None, vocab=0, token_ids=None) -> moe_route_desc:
+    return moe_route_desc(int(T), int(E), int(H), int(top_k), int(scoring), int(bool(renormalize)),
+                          float(routed_scaling), _dptr(w_router, torch.bfloat16, "w_router"),
+                          _dptr(correction_bias, torch.float32, "correction_bias"),
+                          _dptr(tid2eid, torch.int64, "tid2eid"), int(vocab),
+                          _dptr(token_ids, torch.int32, "token_ids"))
+
+
 def moe_route(*, T, E, H, top_k, scoring, renormalize, routed_scaling, x=None, w_router=None,
               logits_in=None, logits_out=None, correction_bias=None, tid2eid=None, vocab=0,
               token_ids=None, topk_ids, topk_w, dev_status=None, stream=None):
     lib = load_library()
-    d = moe_route_desc(int(T), int(E), int(H), int(top_k), int(scoring), int(bool(renormalize)),
-                       float(routed_scaling), _dptr(w_router, torch.bfloat16, "w_router"),
-                       _dptr(correction_bias, torch.float32, "correction_bias"),
-                       _dptr(tid2eid, torch.int64, "tid2eid"), int(vocab),
-                       _dptr(token_ids, torch.int32, "token_ids"))
+    d = route_desc(T=T, E=E, H=H, top_k=top_k, scoring=scoring, renormalize=renormalize,
+                   routed_scaling=routed_scaling, w_router=w_router,
+                   correction_bias=correction_bias, tid2eid=tid2eid, vocab=vocab,
+                   token_ids=token_ids)
     st = lib.moe_route(ctypes.byref(d), _dptr(x, torch.bfloat16, "x"),
                        _dptr(logits_in, torch.float32, "logits_in"),
                        _dptr(logits_out, torch.float32, "logits_out"),
@@ -175,6 +186,20 @@ def moe_ffn_forward(handle: int, T: int, act: int, g_act1: float, g_act2: float,
         _dptr(workspace, torch.uint8, "workspace"), workspace.numel(),
         _dptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check(st, "moe_ffn_forward")
+
+
+def moe_forward(handle: int, route: moe_route_desc, act: int, g_act1: float, g_act2: float, x,
+                topk_ids, topk_w, out, workspace, logits_in=None, logits_out=None,
+                dev_status=None, stream=None):
+    """Route + expert FFN in one call (one persistent launch for a few tokens)."""
+    st = load_library().moe_forward(
+        ctypes.c_void_p(handle), ctypes.byref(route), int(act), float(g_act1), float(g_act2),
+        _dptr(x, torch.bfloat16, "x"), _dptr(logits_in, torch.float32, "logits_in"),
+        _dptr(logits_out, torch.float32, "logits_out"), _dptr(topk_ids, torch.int32, "topk_ids"),
+        _dptr(topk_w, torch.float32, "topk_w"), _dptr(out, torch.bfloat16, "out"),
+        _dptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(st, "moe_forward")
 
 
 def moe_ffn_forward_noalloc(handle: int, T: int, act: int, g_act1: float, g_act2: float, x,

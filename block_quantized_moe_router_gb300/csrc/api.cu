@@ -41,6 +41,8 @@ struct Handle {
     PhaseEvents events{};  // owned; created by moe_profile_enable
     bool tc_shape = false;
     TcWeights tc{};        // owned; the tcgen05 path's scale tiles and tensor maps
+    int sms = 0;           // SM count of the device the weights live on
+    unsigned long long* bar = nullptr;  // owned; grid-barrier tickets of the few-token kernel
 };
 
 bool desc_tc_shape(const moe_ffn_desc& d) {
@@ -101,6 +103,56 @@ moe_status_t validate_ffn_desc(const moe_ffn_desc* d) {
     return MOE_OK;
 }
 
+moe_status_t validate_route(const moe_route_desc* d, const float* logits_in) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->E < 1 || d->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (d->top_k < 1 || d->top_k > d->E || d->top_k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+    if (!std::isfinite(d->routed_scaling)) return MOE_ERR_INVALID_ARG;
+    if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID &&
+        d->scoring != MOE_SCORE_HASH && d->scoring != MOE_SCORE_SQRTSOFTPLUS)
+        return MOE_ERR_INVALID_ARG;
+    if (d->scoring == MOE_SCORE_HASH && d->vocab < 1) return MOE_ERR_INVALID_ARG;
+    if (d->scoring != MOE_SCORE_HASH && !logits_in && (d->H < 32 || d->H % 32))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+// The FFN launch description of one call; the workspace carve-up follows the path's plan.
+FfnLaunch make_launch(const Handle* h, int T, int act, float g1, float g2, int path,
+                      const Workspace& ws, char* base, const void* x, const int32_t* ids,
+                      const float* w, void* out, int32_t* status) {
+    const moe_ffn_desc& d = h->desc;
+    FfnLaunch L{};
+    L.T = T; L.E = d.E; L.H = d.H; L.I = d.I; L.k = d.top_k; L.I_shared = d.I_shared;
+    L.act = act; L.path = path; L.g1 = g1; L.g2 = g2;
+    L.x = x; L.ids = ids; L.w = w; L.out = out; L.status = status;
+    L.gate = h->gate.view; L.up = h->up.view; L.down = h->down.view;
+    L.sh_gate = h->sh_gate.view; L.sh_up = h->sh_up.view; L.sh_down = h->sh_down.view;
+    L.counts = reinterpret_cast<int32_t*>(base + ws.counts);
+    L.offsets = reinterpret_cast<int32_t*>(base + ws.offsets);
+    L.active = reinterpret_cast<int32_t*>(base + ws.active);
+    L.meta = reinterpret_cast<int32_t*>(base + ws.meta);
+    L.sorted_pair = reinterpret_cast<int32_t*>(base + ws.sorted_pair);
+    L.pos_of_pair = reinterpret_cast<int32_t*>(base + ws.pos_of_pair);
+    L.x16 = reinterpret_cast<__half*>(base + ws.x16);
+    L.xq = reinterpret_cast<uint8_t*>(base + ws.xq);
+    L.xs = reinterpret_cast<uint8_t*>(base + ws.xs);
+    L.h16 = reinterpret_cast<__half*>(base + ws.h16);
+    L.hq = reinterpret_cast<uint8_t*>(base + ws.hq);
+    L.hs = reinterpret_cast<uint8_t*>(base + ws.hs);
+    L.y = reinterpret_cast<float*>(base + ws.y);
+    return L;
+}
+
+// The few-token path: one persistent launch (phase 1 timing events around it when profiled).
+moe_status_t run_decode(const Handle* h, const FfnLaunch& L, const DecRoute& R, cudaStream_t st) {
+    const PhaseEvents* ev = h->profile_mask ? &h->events : nullptr;
+    if (ev && record_phase_event(ev->begin[1], st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_decode_fused(L, R, h->bar, h->sms, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (ev && record_phase_event(ev->end[1], st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -119,16 +171,8 @@ const char* moe_status_string(moe_status_t s) {
 moe_status_t moe_route(const moe_route_desc* d, const void* x_bf16, const float* logits_in,
                        float* logits_out, int32_t* topk_ids, float* topk_w, int32_t* dev_status,
                        void* stream) {
-    if (!d) return MOE_ERR_INVALID_ARG;
-    if (d->T < 0 || d->E < 1 || d->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
-    if (d->top_k < 1 || d->top_k > d->E || d->top_k > kMaxTopK) return MOE_ERR_INVALID_ARG;
-    if (!std::isfinite(d->routed_scaling)) return MOE_ERR_INVALID_ARG;
-    if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID &&
-        d->scoring != MOE_SCORE_HASH && d->scoring != MOE_SCORE_SQRTSOFTPLUS)
-        return MOE_ERR_INVALID_ARG;
-    if (d->scoring == MOE_SCORE_HASH && d->vocab < 1) return MOE_ERR_INVALID_ARG;
-    if (d->scoring != MOE_SCORE_HASH && !logits_in && (d->H < 32 || d->H % 32))
-        return MOE_ERR_INVALID_ARG;
+    const moe_status_t v = validate_route(d, logits_in);
+    if (v != MOE_OK) return v;
     if (d->T == 0) return MOE_OK;
     if (!topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -157,7 +201,7 @@ moe_status_t moe_workspace_size(const moe_ffn_desc* d, int32_t T, int32_t act, s
     moe_status_t v = validate_ffn_desc(d);
     if (v != MOE_OK) return v;
     if (T < 0 || (act != MOE_ACT_BF16 && act != MOE_ACT_NVFP4)) return MOE_ERR_INVALID_ARG;
-    const int path = select_path(T, d->top_k, act, desc_tc_shape(*d));
+    const int path = select_path(T, d->H, d->top_k, act, desc_tc_shape(*d));
     *bytes = Workspace::plan(d->E, d->H, d->I, d->I_shared, d->top_k, T, act, path).total;
     return MOE_OK;
 }
@@ -181,6 +225,13 @@ moe_status_t moe_prepare_weights(const moe_ffn_desc* d, void** handle_out, void*
         if (s == MOE_OK) s = prepare_proj(d->sh_up, 1, Is, H, h->sh_up, st);
         if (s == MOE_OK) s = prepare_proj(d->sh_down, 1, H, Is, h->sh_down, st);
     }
+    int dev = 0;
+    if (s == MOE_OK && (cudaGetDevice(&dev) != cudaSuccess ||
+                        cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess))
+        s = MOE_ERR_CUDA;
+    if (s == MOE_OK && (cudaMalloc(&h->bar, 256) != cudaSuccess ||
+                        cudaMemsetAsync(h->bar, 0, 256, st) != cudaSuccess))
+        s = MOE_ERR_CUDA;
     h->tc_shape = desc_tc_shape(*d);
     if (s == MOE_OK && h->tc_shape) {
         FfnLaunch L{};
@@ -205,6 +256,7 @@ moe_status_t moe_release_weights(void* handle) {
     free_proj(h->sh_gate); free_proj(h->sh_up); free_proj(h->sh_down);
     destroy_events(h);
     tc_release(&h->tc);
+    if (h->bar) cudaFree(h->bar);
     h->magic = 0;
     delete h;
     return MOE_OK;
@@ -222,31 +274,19 @@ moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g
     if (T == 0) return MOE_OK;
     if (!x_bf16 || !topk_ids || !topk_w || !out_bf16 || !workspace) return MOE_ERR_INVALID_ARG;
     const moe_ffn_desc& d = h->desc;
-    const int path = select_path(T, d.top_k, act, h->tc_shape);
+    const int path = select_path(T, d.H, d.top_k, act, h->tc_shape);
     if (path == PATH_TC && !h->tc.ready) return MOE_ERR_UNSUPPORTED;
     const Workspace ws = Workspace::plan(d.E, d.H, d.I, d.I_shared, d.top_k, T, act, path);
     if (ws_bytes < ws.total) return MOE_ERR_WORKSPACE;
     char* base = static_cast<char*>(workspace);
-    FfnLaunch L{};
-    L.T = T; L.E = d.E; L.H = d.H; L.I = d.I; L.k = d.top_k; L.I_shared = d.I_shared;
-    L.act = act; L.path = path; L.g1 = g_act1; L.g2 = g_act2;
-    L.x = x_bf16; L.ids = topk_ids; L.w = topk_w; L.out = out_bf16; L.status = dev_status;
-    L.gate = h->gate.view; L.up = h->up.view; L.down = h->down.view;
-    L.sh_gate = h->sh_gate.view; L.sh_up = h->sh_up.view; L.sh_down = h->sh_down.view;
-    L.counts = reinterpret_cast<int32_t*>(base + ws.counts);
-    L.offsets = reinterpret_cast<int32_t*>(base + ws.offsets);
-    L.active = reinterpret_cast<int32_t*>(base + ws.active);
-    L.meta = reinterpret_cast<int32_t*>(base + ws.meta);
-    L.sorted_pair = reinterpret_cast<int32_t*>(base + ws.sorted_pair);
-    L.pos_of_pair = reinterpret_cast<int32_t*>(base + ws.pos_of_pair);
-    L.x16 = reinterpret_cast<__half*>(base + ws.x16);
-    L.xq = reinterpret_cast<uint8_t*>(base + ws.xq);
-    L.xs = reinterpret_cast<uint8_t*>(base + ws.xs);
-    L.h16 = reinterpret_cast<__half*>(base + ws.h16);
-    L.hq = reinterpret_cast<uint8_t*>(base + ws.hq);
-    L.hs = reinterpret_cast<uint8_t*>(base + ws.hs);
-    L.y = reinterpret_cast<float*>(base + ws.y);
+    const FfnLaunch L = make_launch(h, T, act, g_act1, g_act2, path, ws, base, x_bf16, topk_ids,
+                                    topk_w, out_bf16, dev_status);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (path == PATH_DECODE) {
+        DecRoute R{};
+        R.mode = DEC_ROUTE_GIVEN;
+        return run_decode(h, L, R, st);
+    }
     const PhaseEvents* ev = h->profile_mask ? &h->events : nullptr;
     cudaError_t err;
     if (path == PATH_TC) {
@@ -269,6 +309,55 @@ moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g
         err = launch_ffn(L, st, ev);
     }
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_forward(const void* handle, const moe_route_desc* rd, int32_t act, float g_act1,
+                         float g_act2, const void* x_bf16, const float* logits_in,
+                         float* logits_out, int32_t* topk_ids, float* topk_w, void* out_bf16,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream) {
+    const Handle* h = static_cast<const Handle*>(handle);
+    if (!h || h->magic != 0x4D4F4531u) return MOE_ERR_INVALID_ARG;
+    const moe_status_t v = validate_route(rd, logits_in);
+    if (v != MOE_OK) return v;
+    const moe_ffn_desc& d = h->desc;
+    if (rd->E != d.E || rd->top_k != d.top_k || rd->H != d.H) return MOE_ERR_INVALID_ARG;
+    if (act != MOE_ACT_BF16 && act != MOE_ACT_NVFP4) return MOE_ERR_INVALID_ARG;
+    if (act == MOE_ACT_NVFP4 && (!pow2_positive(g_act1) || !pow2_positive(g_act2)))
+        return MOE_ERR_INVALID_ARG;
+    const int T = rd->T;
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !topk_ids || !topk_w || !out_bf16 || !workspace) return MOE_ERR_INVALID_ARG;
+    const bool hash = rd->scoring == MOE_SCORE_HASH;
+    if (hash && (!rd->tid2eid || !rd->token_ids)) return MOE_ERR_INVALID_ARG;
+    if (!hash && !logits_in && (!rd->w_router || !logits_out)) return MOE_ERR_INVALID_ARG;
+    const int path = select_path(T, d.H, d.top_k, act, h->tc_shape);
+    if (path != PATH_DECODE) {
+        moe_status_t s = moe_route(rd, x_bf16, logits_in, logits_out, topk_ids, topk_w, dev_status,
+                                   stream);
+        if (s != MOE_OK) return s;
+        return moe_ffn_forward(handle, T, act, g_act1, g_act2, x_bf16, topk_ids, topk_w, out_bf16,
+                               workspace, ws_bytes, dev_status, stream);
+    }
+    const Workspace ws = Workspace::plan(d.E, d.H, d.I, d.I_shared, d.top_k, T, act, path);
+    if (ws_bytes < ws.total) return MOE_ERR_WORKSPACE;
+    const FfnLaunch L = make_launch(h, T, act, g_act1, g_act2, path, ws,
+                                    static_cast<char*>(workspace), x_bf16, topk_ids, topk_w,
+                                    out_bf16, dev_status);
+    DecRoute R{};
+    R.mode = hash ? DEC_ROUTE_HASH : (logits_in ? DEC_ROUTE_LOGITS : DEC_ROUTE_ROUTER);
+    R.w_router = rd->w_router;
+    R.logits_in = logits_in;
+    R.logits_out = logits_out;
+    R.bias = rd->scoring != MOE_SCORE_SOFTMAX ? rd->correction_bias : nullptr;
+    R.scoring = rd->scoring;
+    R.renorm = rd->renormalize ? 1 : 0;
+    R.scaling = rd->routed_scaling;
+    R.tid2eid = rd->tid2eid;
+    R.token_ids = rd->token_ids;
+    R.vocab = rd->vocab;
+    R.ids_out = topk_ids;
+    R.w_out = topk_w;
+    return run_decode(h, L, R, static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_profile_enable(void* handle, uint32_t mask) {

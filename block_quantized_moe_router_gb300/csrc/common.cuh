@@ -174,8 +174,8 @@ inline bool tc_shape_ok(int H, int I, int I_shared, int fmt_routed, int fmt_shar
     return H % 256 == 0 && I % 256 == 0 && I_shared % 256 == 0;
 }
 
-inline int select_path(int T, int top_k, int act, bool tc_shape) {
-    if (T <= 8 && T * top_k <= 64 && act == MOE_ACT_BF16) return PATH_DECODE;
+inline int select_path(int T, int H, int top_k, int act, bool tc_shape) {
+    if (T <= 8 && T * top_k <= 64 && act == MOE_ACT_BF16 && H <= 8192) return PATH_DECODE;
     if (act == MOE_ACT_NVFP4 && tc_shape) return PATH_TC;
     return PATH_GENERIC;
 }
@@ -206,6 +206,7 @@ struct Workspace {
             // h token-major per expert slot: [routed slots + shared][8][Imax]
             const size_t rows = ((size_t)(E < T * top_k ? E : T * top_k) + (I_shared > 0 ? 1 : 0)) * 8;
             w.h16 = take(sizeof(__half) * rows * Imax);
+            w.x16 = take(sizeof(__half) * (size_t)T * H);
         } else if (path == PATH_GENERIC) {
             w.sorted_pair = take(sizeof(int32_t) * (P + 1));
             w.pos_of_pair = take(sizeof(int32_t) * (P + 1));

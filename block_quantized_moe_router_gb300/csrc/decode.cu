@@ -1,40 +1,60 @@
-// decode.cu -- the expert FFN for a few tokens (T <= 8 and T * top_k <= 64, bf16
-// activations): two launches.
+// decode.cu -- the whole MoE block for a few tokens (T <= 8, T * top_k <= 64, bf16
+// activations) in ONE persistent cooperative launch, one CTA per SM.
 //
-//   dec_gateup_kernel   every CTA rebuilds the dispatch (which experts received tokens, in
-//                       ascending id order, and which tokens each one received) from the
-//                       routing ids -- no separate sort launch -- and then works through
-//                       (expert, 16-row tile) tasks: 8 warps split K, each streams its gate and
-//                       up rows, their block scales and the tokens through a per-warp ring of
-//                       asynchronous copies; the partial sums meet in shared memory and
-//                       h = SiLU(gate) * up is written token-major, hT[slot][token][I] (f16).
-//   dec_down_kernel     the down projection fused with the top-K weighted sum and the shared
-//                       expert: the MMA columns are the T tokens and the sum runs over
-//                       (expert, I).  Each of the 8 warps walks a subset of the active experts
-//                       through its copy ring; per expert it accumulates W_down . h in fp32 and
-//                       adds it scaled by that expert's per-tensor post-scale and each token's
-//                       routing weight, so no per-pair outputs reach memory.  Warps are
-//                       reduced through shared memory in a fixed order and bf16 rows are
-//                       written directly.
+//   phase 0  every CTA converts a slice of x to f16 and, when the router runs here, computes
+//            the router logits of the experts e = cta, cta + G, ... (fp32 dot products on
+//            the CUDA cores, the 8 warps splitting H).                 -> grid barrier 1
+//   phase 1  every CTA selects the top-K of all T tokens itself (one warp per token), or
+//            looks the experts up in the hash table, or reads the given ids; CTA 0 writes
+//            the routing outputs.  Each CTA then derives the dispatch: the active experts in
+//            ascending id order, each with its tokens and routing weights.
+//   phase 2  gate+up: tasks (expert slot, 16 rows of I) dealt round-robin to the CTAs; the 8
+//            warps split K = H, partial sums meet in shared memory and h = SiLU(g) * u is
+//            written token-major to hT[slot][token][I] (f16).          -> grid barrier 2
+//   phase 3  down fused with the top-K weighted sum and the shared expert: each CTA owns
+//            16-row tiles of the output; its (tile, slot) pairs are dealt to its warps, each
+//            folds W_down . h of a slot into its tile with the expert's post-scale and each
+//            token's weight; warps are reduced in a fixed order and bf16 rows are written.
 //
-// This is the "gate+up, silu+down in two fused launches" structure of the spark_model MoE
-// module doc (moe/mod.rs), with the weighted sum (init.rs `moe_weighted_sum_blend`) folded
-// into the second launch.  Both kernels are launched with programmatic dependent launch.
+// Every warp streams its operands through its own ring of asynchronous copies, S - 2 steps
+// ahead of the MMAs (which take one or two steps at a time), in ONE sequence that runs from its first gate+up step to its last down
+// step.  A stage holds the codes of rows g and g+8, their block scales and the activation
+// chunk of the step (x in f16 for gate+up, h for down).  The down weights depend only on
+// the routing, so they are already in flight while the CTA waits at barrier 2; the h
+// chunks of the down steps issued before that barrier are copied right after it.
 //
-// Copy ring: a warp's stage holds, per lane, its 16-byte code chunks (rows g and g+8 of each
-// matrix), its 64 bytes of activations and one 8-byte word of block scales; the stage for step
-// i + S - 1 is issued before step i is consumed, so S - 1 steps of every warp are in flight
-// without holding registers.
+// This is the "gate + top-K fused, expert FFN in two fused stages" structure of the
+// spark_model MoE module doc (moe/mod.rs) taken to a single launch, with the weighted sum
+// (init.rs `moe_weighted_sum_blend`) folded into the down stage.  Grid barriers are bounded
+// spins on a 64-bit ticket counter owned by the weights handle; a wait that runs out sets
+// MOE_DEV_TIMEOUT and the kernel carries on (its results are then invalid) instead of hanging.
 #include "common.cuh"
 #include "frag.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace moe {
 
 constexpr int kDecMaxT = 8;
-constexpr int kDecMaxSlots = 65;  // at most 64 routed pairs (T * top_k <= 64) + the shared expert
+constexpr int kDecMaxSlots = 65;   // at most 64 routed pairs (T * top_k <= 64) + the shared expert
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kDecStages = 6;
+// one ring stage: codes (gate+up: 4 x 512 B; down: 2 x 512 B), the activation chunk
+// (32 lanes x 64 B, MMA column = lane / 4), then 32 lanes x 8 B of block scales
+constexpr int kDecStageAct = 2048, kDecStageScales = 4096;
+constexpr int kDecStageBytes = 4096 + 256;
+constexpr int kDecRingBytes = kDecWarps * kDecStages * kDecStageBytes;
+// the gate+up partial sums (double-buffered) and, after barrier 2, the down partial sums
+// (one 16-row output tile per 4 KB) share one region
+constexpr int kDecRedG = 2 * kDecWarps * 256 * 4;
+constexpr int kDecRedDTile = kDecWarps * 128 * 4;
+constexpr int kDecMaxTilesPerCta = 4;
+// router phase: experts handled together per CTA, 8-element chunks per thread and expert
+constexpr int kDecRouterBatch = 4, kDecRouterChunks = 4;  // H <= 8 * 256 * 4 = 8192
+constexpr long long kBarrierCycles = 4000000000ll;  // ~2 s at 2 GHz
 
-// Dispatch of T <= 8 tokens, rebuilt by every CTA from ids/w.
+// Dispatch of T <= 8 tokens, derived by every CTA from the routing ids / weights.
 struct DecDispatch {
     uint32_t bitmap[kMaxExperts / 32];
     int base[kMaxExperts / 32];
@@ -44,7 +64,72 @@ struct DecDispatch {
     float w[kDecMaxSlots][kDecMaxT];
 };
 
-__device__ __forceinline__ void dec_dispatch(const FfnLaunch& L, DecDispatch& D) {
+struct DecShared {
+    DecDispatch D;
+    int32_t ids[64];
+    float w[64];
+    float red_router[4][kDecWarps][kDecMaxT];
+};
+
+// ---- small helpers ---------------------------------------------------------------------------
+// L2-only load: for data written earlier in this launch by other CTAs.
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// bf16x2 -> f16x2 (via fp32; exact for |x| >= 2^-14)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    return pack_half2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// the g-th set bit of mask (ascending), or -1
+__device__ __forceinline__ int nth_bit(uint32_t mask, int g) {
+    for (int c = 0; c < g && mask; ++c) mask &= mask - 1;
+    return mask ? __ffs(mask) - 1 : -1;
+}
+
+// Grid-wide barrier of a cooperative launch: 64-bit arrival tickets, never reset; barrier
+// instance n completes when the counter reaches (n + 1) * G.  The wait is bounded.
+__device__ __forceinline__ void grid_barrier(unsigned long long* bar, int32_t* status) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned long long G = gridDim.x;
+        const unsigned long long ticket = atomicAdd(bar, 1ull);
+        const unsigned long long target = (ticket / G + 1ull) * G;
+        const long long t0 = clock64();
+        bool done = ld_acquire_u64(bar) >= target;
+        int spins = 0;
+        while (!done) {
+            if (++spins > 64) __nanosleep(64);
+            done = ld_acquire_u64(bar) >= target;
+            if (!done && clock64() - t0 > kBarrierCycles) break;
+        }
+        if (!done) status_or(status, MOE_DEV_TIMEOUT);
+        __threadfence();
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// ---- phase 1: dispatch from the routing ids / weights in shared memory --------------------------
+__device__ __forceinline__ void dec_dispatch(int T, int k, int E, int I_shared, const int32_t* ids,
+                                             const float* wts, DecDispatch& D) {
     const int tid = threadIdx.x;
     for (int i = tid; i < kMaxExperts / 32; i += blockDim.x) D.bitmap[i] = 0;
     for (int i = tid; i < kDecMaxSlots * (kDecMaxT + 1); i += blockDim.x) {
@@ -52,14 +137,12 @@ __device__ __forceinline__ void dec_dispatch(const FfnLaunch& L, DecDispatch& D)
         else (&D.w[0][0])[i - kDecMaxSlots] = 0.f;
     }
     __syncthreads();
-    if (tid < 32) {  // one warp: at most 64 ids, two per lane
-        const int lane = tid, P = L.T * L.k;
-        int e0 = -1, e1 = -1;
-        float w0 = 0.f, w1 = 0.f;  // loaded with the ids: one global round trip
-        if (lane < P) { e0 = L.ids[lane]; w0 = L.w[lane]; }
-        if (lane + 32 < P) { e1 = L.ids[lane + 32]; w1 = L.w[lane + 32]; }
-        if (e0 >= 0 && e0 < L.E) atomicOr(&D.bitmap[e0 >> 5], 1u << (e0 & 31));
-        if (e1 >= 0 && e1 < L.E) atomicOr(&D.bitmap[e1 >> 5], 1u << (e1 & 31));
+    if (tid < 32) {  // one warp: at most 64 pairs, two per lane
+        const int lane = tid, P = T * k;
+        const int e0 = lane < P ? ids[lane] : -1, e1 = lane + 32 < P ? ids[lane + 32] : -1;
+        const float w0 = lane < P ? wts[lane] : 0.f, w1 = lane + 32 < P ? wts[lane + 32] : 0.f;
+        if (e0 >= 0 && e0 < E) atomicOr(&D.bitmap[e0 >> 5], 1u << (e0 & 31));
+        if (e1 >= 0 && e1 < E) atomicOr(&D.bitmap[e1 >> 5], 1u << (e1 & 31));
         __syncwarp();
         const int cnt = lane < kMaxExperts / 32 ? __popc(D.bitmap[lane]) : 0;
         int inc = cnt;
@@ -75,9 +158,9 @@ __device__ __forceinline__ void dec_dispatch(const FfnLaunch& L, DecDispatch& D)
         for (int h = 0; h < 2; ++h) {
             const int e = h ? e1 : e0;
             const int p = lane + 32 * h;
-            if (e >= 0 && e < L.E) {
+            if (e >= 0 && e < E) {
                 const int slot = D.base[e >> 5] + __popc(D.bitmap[e >> 5] & ((1u << (e & 31)) - 1u));
-                const int t = p / L.k;
+                const int t = p / k;
                 D.expert[slot] = e;
                 atomicOr(&D.tokmask[slot], 1u << t);
                 atomicAdd(&D.w[slot][t], h ? w1 : w0);  // a table may route a token to an expert twice
@@ -85,376 +168,554 @@ __device__ __forceinline__ void dec_dispatch(const FfnLaunch& L, DecDispatch& D)
         }
         if (lane == 0) {
             D.n_active = n_active;
-            if (L.I_shared > 0) {
+            if (I_shared > 0) {
                 D.expert[n_active] = 0;
-                D.tokmask[n_active] = (1u << L.T) - 1u;
-                for (int t = 0; t < L.T; ++t) D.w[n_active][t] = 1.f;
+                D.tokmask[n_active] = (1u << T) - 1u;
+                for (int t = 0; t < T; ++t) D.w[n_active][t] = 1.f;
             }
         }
     }
     __syncthreads();
 }
 
-// bf16x2 -> f16x2 (via fp32; exact for |x| >= 2^-14)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-    return pack_half2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+// ---- U (1 or 2) MMA steps of 128 K elements, their instruction streams interleaved ----------
+// gate+up: rows g / g+8 of gate (stage codes 0, 1) and up (2, 3); B = x in f16.
+template <int FMT, int U>
+__device__ __forceinline__ void gu_steps(const uint8_t* st0, const uint8_t* st1, bool has_tok,
+                                         int lane, int g, int q, int mxg, int mxu,
+                                         float (&accG)[4][4], float (&accU)[4][4]) {
+    uint4 bx[U][4];
+    ChunkA cg[U], cu[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint8_t* st = u ? st1 : st0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            bx[u][c] = has_tok ? *reinterpret_cast<const uint4*>(st + kDecStageAct + c * 512 + lane * 16)
+                               : make_uint4(0, 0, 0, 0);
+        cg[u].r0 = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
+        cg[u].r1 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
+        cu[u].r0 = *reinterpret_cast<const uint4*>(st + 2 * 512 + lane * 16);
+        cu[u].r1 = *reinterpret_cast<const uint4*>(st + 3 * 512 + lane * 16);
+        const uint2* sc = reinterpret_cast<const uint2*>(st + kDecStageScales);
+        scales_from_raw<FMT>(sc[g * 4 + 0], q, mxg, cg[u].s0lo, cg[u].s0hi);
+        scales_from_raw<FMT>(sc[g * 4 + 1], q, mxg, cg[u].s1lo, cg[u].s1hi);
+        scales_from_raw<FMT>(sc[g * 4 + 2], q, mxu, cu[u].s0lo, cu[u].s0hi);
+        scales_from_raw<FMT>(sc[g * 4 + 3], q, mxu, cu[u].s1lo, cu[u].s1hi);
+    }
+    __syncwarp();  // every lane has read the stages before they are refilled
+#define DEC_GU(I)                                                                 \
+    _Pragma("unroll") for (int u = 0; u < U; ++u) {                               \
+        uint32_t fa[4], fb[4];                                                    \
+        frag_a<I>(cg[u], fa);                                                     \
+        frag_a<I>(cu[u], fb);                                                     \
+        const uint32_t b0 = word_of(bx[u][I >> 1], (I & 1) * 2);                  \
+        const uint32_t b1 = word_of(bx[u][I >> 1], (I & 1) * 2 + 1);              \
+        mma_f16_16816(accG[u * 2 + (I & 1)], fa[0], fa[1], fa[2], fa[3], b0, b1); \
+        mma_f16_16816(accU[u * 2 + (I & 1)], fb[0], fb[1], fb[2], fb[3], b0, b1); \
+    }
+    DEC_GU(0) DEC_GU(1) DEC_GU(2) DEC_GU(3) DEC_GU(4) DEC_GU(5) DEC_GU(6) DEC_GU(7)
+#undef DEC_GU
 }
 
-// the g-th set bit of mask (ascending), or -1
-__device__ __forceinline__ int nth_bit(uint32_t mask, int g) {
-    for (int c = 0; c < g && mask; ++c) mask &= mask - 1;
-    return mask ? __ffs(mask) - 1 : -1;
+// down: rows g / g+8 of W_down (stage codes 0, 1); B = h in f16.
+template <int FMT, int U>
+__device__ __forceinline__ void dn_steps(const uint8_t* st0, const uint8_t* st1, bool has_tok,
+                                         int lane, int g, int q, int mx, float (&part)[4][4]) {
+    uint4 hb[U][4];
+    ChunkA c[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint8_t* st = u ? st1 : st0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            hb[u][j] = has_tok ? *reinterpret_cast<const uint4*>(st + kDecStageAct + j * 512 + lane * 16)
+                               : make_uint4(0, 0, 0, 0);
+        c[u].r0 = *reinterpret_cast<const uint4*>(st + lane * 16);
+        c[u].r1 = *reinterpret_cast<const uint4*>(st + 512 + lane * 16);
+        const uint2* sc = reinterpret_cast<const uint2*>(st + kDecStageScales);
+        scales_from_raw<FMT>(sc[g * 4 + 0], q, mx, c[u].s0lo, c[u].s0hi);
+        scales_from_raw<FMT>(sc[g * 4 + 1], q, mx, c[u].s1lo, c[u].s1hi);
+    }
+    __syncwarp();
+#define DEC_DN(I)                                                                          \
+    _Pragma("unroll") for (int u = 0; u < U; ++u) {                                        \
+        uint32_t fa[4];                                                                    \
+        frag_a<I>(c[u], fa);                                                               \
+        mma_f16_16816(part[u * 2 + (I & 1)], fa[0], fa[1], fa[2], fa[3],                   \
+                      word_of(hb[u][I >> 1], (I & 1) * 2), word_of(hb[u][I >> 1], (I & 1) * 2 + 1)); \
+    }
+    DEC_DN(0) DEC_DN(1) DEC_DN(2) DEC_DN(3) DEC_DN(4) DEC_DN(5) DEC_DN(6) DEC_DN(7)
+#undef DEC_DN
+}
+
+__device__ __forceinline__ float sum4(const float (&a)[4][4], int i) {
+    return (a[0][i] + a[1][i]) + (a[2][i] + a[3][i]);
 }
 
 // ------------------------------------------------------------------------------------------
-// gate+up
-// ------------------------------------------------------------------------------------------
-constexpr int kGuWarps = 8;  // K split over 8 warps
-constexpr int kGuStages = 2;
-constexpr int kGuStageBytes = 4 * 512 + 4 * 512 + 32 * 8;  // codes, tokens, scales
-// the K-split reduction (8 warps x 8 x 32 floats) reuses the rings once they are drained
-constexpr int kGuSmem = kGuWarps * kGuStages * kGuStageBytes;
-static_assert(kGuWarps * 8 * 32 * 4 <= kGuSmem, "reduction buffer must fit in the rings");
+template <int FR, int FS>
+__global__ void __launch_bounds__(kDecThreads, 1)
+dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __shared__ DecShared S;
+    DecDispatch& D = S.D;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+    const int G = gridDim.x, cta = blockIdx.x;
+    const int T = L.T, H = L.H, E = L.E, k = L.k;
+    const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
+    const int tiles_out = H / 16;
+    const int cnt_d = cta < tiles_out ? (tiles_out - cta + G - 1) / G : 0;
+    float* red_g = reinterpret_cast<float*>(dsm + kDecRingBytes);
+    float* red_d = red_g;  // reused for the down partial sums after barrier 2
 
-template <int FMT>
-__device__ __forceinline__ void dec_gateup_task(const FfnLaunch& L, const DecDispatch& D, int slot,
-                                                int n0, uint8_t* ring, float* red) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    const bool shared = slot == D.n_active;
-    const int e = D.expert[slot];
-    const uint32_t mask = D.tokmask[slot];
-    const ProjView& PG = shared ? L.sh_gate : L.gate;
-    const ProjView& PU = shared ? L.sh_up : L.up;
-    const int N = shared ? L.I_shared : L.I;
-    const int K = L.H;
-    const int sv = FMT == MOE_FMT_NVFP4 ? 16 : 32;
-    const int steps = K / 128;
-    const int per = (steps + kGuWarps - 1) / kGuWarps;
-    const int s0 = warp * per, s1 = min(steps, s0 + per);
-    const int n = max(0, s1 - s0);
-
-    const size_t rowA = (size_t)e * N + n0 + g;
-    const uint8_t* pa[4] = {PG.packed + rowA * (K / 2) + 16 * q,
-                            PG.packed + (rowA + 8) * (K / 2) + 16 * q,
-                            PU.packed + rowA * (K / 2) + 16 * q,
-                            PU.packed + (rowA + 8) * (K / 2) + 16 * q};
-    // this lane stages the scales of (row g + 8 * (q & 1), matrix q >> 1)
-    const ProjView& PS = (q >> 1) ? PU : PG;
-    const uint8_t* sp = PS.scales + (rowA + 8 * (q & 1)) * (K / sv);
-    const int mxg = FMT == MOE_FMT_MXFP4 ? 112 + PG.mx_off[e] : 0;
-    const int mxu = FMT == MOE_FMT_MXFP4 ? 112 + PU.mx_off[e] : 0;
-    const int tok = nth_bit(mask, g);  // column g <-> the g-th token of this expert
-    const __nv_bfloat16* xrow =
-        static_cast<const __nv_bfloat16*>(L.x) + (size_t)(tok >= 0 ? tok : 0) * K + 32 * q;
-    const uint32_t rbase = smem_addr(ring);
-
-    auto issue = [&](int i) {
-        if (i < n) {
-            const int s = s0 + i;
-            const uint32_t st = rbase + (i % kGuStages) * kGuStageBytes;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) cp_async16(st + c * 512 + lane * 16, pa[c] + s * 64);
-            if (tok >= 0) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    cp_async16(st + 2048 + c * 512 + lane * 16, xrow + s * 128 + 8 * c);
-            }
-            if constexpr (FMT == MOE_FMT_NVFP4) cp_async8(st + 4096 + lane * 8, sp + s * 8);
-            else cp_async4(st + 4096 + lane * 8, sp + s * 4);
+    // ---- phase 0 ----------------------------------------------------------------------------
+    {   // x -> f16 (this CTA's slice of the flat array)
+        const int n8 = T * H / 8;
+        const uint4* xs = static_cast<const uint4*>(L.x);
+        uint4* xd = reinterpret_cast<uint4*>(L.x16);
+        for (int c = cta * kDecThreads + tid; c < n8; c += G * kDecThreads) {
+            const uint4 v = ldg_cached128(xs + c);
+            xd[c] = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                               bf16x2_to_f16x2(v.w));
         }
-        cp_async_commit();
+    }
+    if (R.mode == DEC_ROUTE_ROUTER && cta < E) {
+        // router logits of experts e = cta, cta + G, ...: x (bf16) is staged in the idle ring,
+        // each thread loads its router chunks of all these experts before any arithmetic
+        const int chunks = H / 8;
+        uint4* xs_smem = reinterpret_cast<uint4*>(dsm);
+        const uint4* xg = static_cast<const uint4*>(L.x);
+        for (int c = tid; c < T * chunks; c += kDecThreads) xs_smem[c] = ldg_cached128(xg + c);
+        const uint4* wr = static_cast<const uint4*>(R.w_router);
+        for (int e0 = cta; e0 < E; e0 += kDecRouterBatch * G) {
+            uint4 wv[kDecRouterBatch][kDecRouterChunks];
+#pragma unroll
+            for (int b = 0; b < kDecRouterBatch; ++b)
+#pragma unroll
+                for (int m = 0; m < kDecRouterChunks; ++m) {
+                    const int e = e0 + b * G, c = tid + m * kDecThreads;
+                    wv[b][m] = (e < E && c < chunks) ? ldg_stream128(wr + (size_t)e * chunks + c)
+                                                     : make_uint4(0, 0, 0, 0);
+                }
+            __syncthreads();  // x is staged
+#pragma unroll
+            for (int b = 0; b < kDecRouterBatch; ++b) {
+                float acc[kDecMaxT];
+#pragma unroll
+                for (int t = 0; t < kDecMaxT; ++t) acc[t] = 0.f;
+#pragma unroll
+                for (int m = 0; m < kDecRouterChunks; ++m) {
+                    const int c = tid + m * kDecThreads;
+                    if (c < chunks) {
+                        float wf[8];
+                        unpack_bf16x8(wv[b][m], wf);
+#pragma unroll
+                        for (int t = 0; t < kDecMaxT; ++t) {
+                            if (t < T) {
+                                float xf[8];
+                                unpack_bf16x8(xs_smem[t * chunks + c], xf);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kDecMaxT; ++t)
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+                if (lane == 0)
+#pragma unroll
+                    for (int t = 0; t < kDecMaxT; ++t) S.red_router[b][warp][t] = acc[t];
+            }
+            __syncthreads();
+            if (tid < kDecRouterBatch * kDecMaxT) {
+                const int b = tid / kDecMaxT, t = tid - b * kDecMaxT, e = e0 + b * G;
+                if (t < T && e < E) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kDecWarps; ++w) s += S.red_router[b][w][t];
+                    R.logits_out[(size_t)t * E + e] = s;
+                }
+            }
+        }
+    }
+    grid_barrier(bar, L.status);  // x16 and the logits are written
+
+    // ---- phase 1: routing and dispatch ---------------------------------------------------------
+    const int P = T * k;
+    if (R.mode == DEC_ROUTE_ROUTER || R.mode == DEC_ROUTE_LOGITS) {
+        if (warp < T) {
+            const bool in_launch = R.mode == DEC_ROUTE_ROUTER;
+            const float* row = (in_launch ? R.logits_out : R.logits_in) + (size_t)warp * E;
+            int my_e;
+            float my_w;
+            auto load = [&](int e) { return in_launch ? ld_cg_f32(row + e) : row[e]; };
+            bool nonfinite;
+            if (E <= 64)
+                nonfinite = warp_topk<2>(load, R.bias, E, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
+            else if (E <= 128)
+                nonfinite = warp_topk<4>(load, R.bias, E, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
+            else if (E <= 256)
+                nonfinite = warp_topk<8>(load, R.bias, E, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
+            else
+                nonfinite = warp_topk<16>(load, R.bias, E, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
+            if (nonfinite && lane == 0 && cta == 0) status_or(L.status, MOE_DEV_NONFINITE);
+            if (lane < k) {
+                S.ids[warp * k + lane] = my_e;
+                S.w[warp * k + lane] = my_w;
+            }
+        }
+    } else if (R.mode == DEC_ROUTE_HASH) {
+        if (tid < P) {
+            const int t = tid / k, j = tid - t * k;
+            const int64_t tok = R.token_ids[t];
+            int32_t e = -1;
+            float w = 0.f;
+            if (tok < 0 || tok >= R.vocab) {
+                if (cta == 0) status_or(L.status, MOE_DEV_BAD_TOKEN_ID);
+            } else {
+                const int64_t te = R.tid2eid[tok * k + j];
+                if (te < 0 || te >= E) {
+                    if (cta == 0) status_or(L.status, MOE_DEV_BAD_EXPERT_ID);
+                } else {
+                    e = (int32_t)te;
+                    w = R.scaling / (float)k;
+                }
+            }
+            S.ids[tid] = e;
+            S.w[tid] = w;
+        }
+    } else if (tid < P) {
+        S.ids[tid] = L.ids[tid];
+        S.w[tid] = L.w[tid];
+    }
+    __syncthreads();
+    if (R.mode != DEC_ROUTE_GIVEN && cta == 0 && tid < P) {
+        R.ids_out[tid] = S.ids[tid];
+        R.w_out[tid] = S.w[tid];
+    }
+    dec_dispatch(T, k, E, L.I_shared, S.ids, S.w, D);
+
+    // ---- the work of this CTA and of this warp ----------------------------------------------------
+    // gate+up: tasks (slot, 16 rows) dealt round-robin to the CTAs; in each task warp w takes the
+    // K-steps w, w + 8, ..., so at any time the 8 warps read 512 contiguous bytes of every row.
+    const int n_active = D.n_active;
+    const bool has_shared = L.I_shared > 0;
+    const int tilesR = L.I / 16;
+    const int ntasks = n_active * tilesR + (has_shared ? L.I_shared / 16 : 0);
+    const int cnt_g = cta < ntasks ? (ntasks - cta + G - 1) / G : 0;
+    const int ksteps_g = H / 128;
+    const int n_g = ksteps_g > warp ? (ksteps_g - warp + kDecWarps - 1) / kDecWarps : 0;
+    const int done_g = n_g > 0 ? cnt_g * n_g : 0;  // gate+up steps of this warp
+    // down: 16-row output tiles dealt round-robin to the CTAs; the CTA's (tile, slot) pairs are
+    // dealt to its warps (warp w takes pairs w, w + 8, ...), each streams the whole K of a pair.
+    // Slots are visited in an order rotated by the CTA index so that the CTAs read different
+    // experts at any one time.
+    const int nslots = n_active + (has_shared ? 1 : 0);
+    const int npairs = cnt_d * nslots;
+
+    auto task_of = [&](int j, int& slot, int& n0) {  // task j of this CTA -> (slot, first row)
+        const int tau = cta + j * G;
+        if (tau < n_active * tilesR) {
+            slot = tau / tilesR;
+            n0 = (tau - slot * tilesR) * 16;
+        } else {
+            slot = n_active;
+            n0 = (tau - n_active * tilesR) * 16;
+        }
+    };
+    auto pair_of = [&](int p, int& tl, int& slot) {  // pair p of this CTA -> (tile, slot)
+        tl = p / nslots;
+        slot = (p - tl * nslots + cta) % nslots;
+    };
+    // activation chunk of a lane at K-step ks: x (task j) / h (slot)
+    auto x_src = [&](int j) -> const __half* {
+        int slot, n0;
+        task_of(j, slot, n0);
+        const int tok = nth_bit(D.tokmask[slot], g);  // MMA column g <-> the g-th token of the slot
+        return tok < 0 ? nullptr : L.x16 + (size_t)tok * H + 32 * q;
+    };
+    auto h_src = [&](int slot) -> const __half* {
+        const bool ok = (D.tokmask[slot] >> g) & 1u;  // MMA column g = token g
+        return ok ? L.h16 + ((size_t)slot * kDecMaxT + g) * Imax + 32 * q : nullptr;
+    };
+    auto copy_act = [&](uint32_t st, const __half* a) {  // 64 B of activations of this lane
+        if (a) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) cp_async16(st + kDecStageAct + c * 512 + lane * 16, a + 8 * c);
+        }
     };
 
-    float accG[4] = {0.f, 0.f, 0.f, 0.f}, accU[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < kGuStages - 1; ++i) issue(i);
-    for (int i = 0; i < n; ++i) {
-        issue(i + kGuStages - 1);
-        cp_async_wait<kGuStages - 1>();
-        __syncwarp();
-        const uint8_t* st = ring + (i % kGuStages) * kGuStageBytes;
-        ChunkA cg, cu;
-        cg.r0 = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
-        cg.r1 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
-        cu.r0 = *reinterpret_cast<const uint4*>(st + 2 * 512 + lane * 16);
-        cu.r1 = *reinterpret_cast<const uint4*>(st + 3 * 512 + lane * 16);
-        const uint2* sc = reinterpret_cast<const uint2*>(st + 4096);
-        scales_from_raw<FMT>(sc[g * 4 + 0], q, mxg, cg.s0lo, cg.s0hi);
-        scales_from_raw<FMT>(sc[g * 4 + 1], q, mxg, cg.s1lo, cg.s1hi);
-        scales_from_raw<FMT>(sc[g * 4 + 2], q, mxu, cu.s0lo, cu.s0hi);
-        scales_from_raw<FMT>(sc[g * 4 + 3], q, mxu, cu.s1lo, cu.s1hi);
-        uint32_t bx[16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint4 r = tok >= 0 ? *reinterpret_cast<const uint4*>(st + 2048 + c * 512 + lane * 16)
-                                     : make_uint4(0, 0, 0, 0);
-            bx[4 * c + 0] = bf16x2_to_f16x2(r.x);
-            bx[4 * c + 1] = bf16x2_to_f16x2(r.y);
-            bx[4 * c + 2] = bf16x2_to_f16x2(r.z);
-            bx[4 * c + 3] = bf16x2_to_f16x2(r.w);
-        }
-        __syncwarp();  // every lane has read this stage before it is refilled
-#define DEC_STEP(I)                                                                \
-    {                                                                              \
-        uint32_t fa[4], fb[4];                                                     \
-        frag_a<I>(cg, fa);                                                         \
-        frag_a<I>(cu, fb);                                                         \
-        mma_f16_16816(accG, fa[0], fa[1], fa[2], fa[3], bx[2 * I], bx[2 * I + 1]); \
-        mma_f16_16816(accU, fb[0], fb[1], fb[2], fb[3], bx[2 * I], bx[2 * I + 1]); \
-    }
-        DEC_STEP(0) DEC_STEP(1) DEC_STEP(2) DEC_STEP(3)
-        DEC_STEP(4) DEC_STEP(5) DEC_STEP(6) DEC_STEP(7)
-#undef DEC_STEP
-    }
-    cp_async_wait<0>();
-    __syncthreads();  // every warp's ring is drained: its space now holds the reduction
-    // reduce the K-split partial sums through shared memory
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        red[(warp * 8 + i) * 32 + lane] = accG[i];
-        red[(warp * 8 + 4 + i) * 32 + lane] = accU[i];
-    }
-    __syncthreads();
-    if (warp == 0) {
-        float G[4] = {0.f, 0.f, 0.f, 0.f}, U[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int w = 0; w < kGuWarps; ++w) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                G[i] += red[(w * 8 + i) * 32 + lane];
-                U[i] += red[(w * 8 + 4 + i) * 32 + lane];
-            }
-        }
-        const float pg = PG.post[e], pu = PU.post[e];
-        const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int t = nth_bit(mask, 2 * q + j);  // column -> token
-            if (t < 0) continue;
-            __half* hrow = L.h16 + ((size_t)slot * kDecMaxT + t) * Imax + n0;
-            hrow[g] = __float2half_rn(silu_f32(G[j] * pg) * (U[j] * pu));
-            hrow[g + 8] = __float2half_rn(silu_f32(G[2 + j] * pg) * (U[2 + j] * pu));
-        }
-    }
-    __syncthreads();  // the rings are refilled by the next task
-}
-
-template <int FMT_R, int FMT_S>
-__global__ void __launch_bounds__(kGuWarps * 32, 3) dec_gateup_kernel(FfnLaunch L, int tiles_per_slot) {
-    extern __shared__ __align__(16) uint8_t dsm[];
-    __shared__ DecDispatch D;
-    pdl_wait();  // ids / w come from the routing kernels
-    dec_dispatch(L, D);
-    // let the down kernel's CTAs start now: they stream their weights while this grid runs
-    pdl_trigger();
-    const int nslots = D.n_active + (L.I_shared > 0 ? 1 : 0);
-    const int warp = threadIdx.x >> 5;
-    uint8_t* ring = dsm + warp * kGuStages * kGuStageBytes;
-    float* red = reinterpret_cast<float*>(dsm);
-    const int ntasks = nslots * tiles_per_slot;
-    for (int task = blockIdx.x; task < ntasks; task += gridDim.x) {
-        const int slot = task / tiles_per_slot;
-        const int n0 = (task - slot * tiles_per_slot) * 16;
-        const bool shared = slot == D.n_active;
-        if (n0 >= (shared ? L.I_shared : L.I)) continue;  // uniform over the CTA
-        if (shared) dec_gateup_task<FMT_S>(L, D, slot, n0, ring, red);
-        else dec_gateup_task<FMT_R>(L, D, slot, n0, ring, red);
-    }
-}
-
-// ------------------------------------------------------------------------------------------
-// down + weighted sum + shared expert
-//
-// The down weights depend only on the routing, not on h, so the CTAs (launched while the
-// gate+up grid still runs) issue their first kDnStages - 1 weight steps before waiting for h.
-// h itself is read from L2 one step ahead in registers.
-// ------------------------------------------------------------------------------------------
-constexpr int kDnWarps = 8;
-constexpr int kDnStages = 6;
-constexpr int kDnStageBytes = 2 * 512 + 32 * 8;  // codes of rows g and g+8, scales
-constexpr int kDnSmem = kDnWarps * kDnStages * kDnStageBytes + kDnWarps * 4 * 32 * 4;
-
-template <int FMT_R, int FMT_S>
-__global__ void __launch_bounds__(kDnWarps * 32) dec_down_kernel(FfnLaunch L) {
-    extern __shared__ __align__(16) uint8_t dsm[];
-    __shared__ DecDispatch D;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-    // the routing ids were complete before the gate+up grid let this grid start
-    dec_dispatch(L, D);
-    const int n0 = blockIdx.x * 16;
-    const int nslots = D.n_active + (L.I_shared > 0 ? 1 : 0);
-    const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
-    uint8_t* ring = dsm + warp * kDnStages * kDnStageBytes;
-    float* red = reinterpret_cast<float*>(dsm + kDnWarps * kDnStages * kDnStageBytes);
+    // ---- the ring: one flat issue sequence per warp ------------------------------------------------
+    uint8_t* ring = dsm + warp * kDecStages * kDecStageBytes;
     const uint32_t rbase = smem_addr(ring);
-
-    // this warp's work: slots warp, warp + 8, ...; their K steps in one flat sequence
-    int total = 0;
-    for (int slot = warp; slot < nslots; slot += kDnWarps)
-        total += (slot == D.n_active ? L.I_shared : L.I) / 128;
-
-    int is_slot = warp, is_s = 0;  // weight issue cursor
-    auto issue = [&](int i) {
-        if (i < total) {
-            const bool sh = is_slot == D.n_active;
-            const int e = D.expert[is_slot];
+    int ic_phase = done_g > 0 ? 0 : 1;
+    // gate+up: task, K-step; down: pair, K-step within the pair
+    int ic_j = ic_phase == 0 ? 0 : warp, ic_s = ic_phase == 0 ? warp : 0, ic_ns = 0;
+    int ic_sfb = 8;
+    bool h_ready = false;  // h may be copied only after barrier 2
+    const uint8_t *ic_c0 = nullptr, *ic_c1 = nullptr, *ic_c2 = nullptr, *ic_c3 = nullptr;
+    const uint8_t* ic_sp = nullptr;
+    const __half* ic_ap = nullptr;
+    auto ic_enter = [&]() {  // base pointers of the issue cursor's task / (slot, tile)
+        if (ic_phase == 0) {
+            int slot, n0;
+            task_of(ic_j, slot, n0);
+            const bool sh = slot == n_active;
+            const ProjView& PG = sh ? L.sh_gate : L.gate;
+            const ProjView& PU = sh ? L.sh_up : L.up;
+            const int N = sh ? L.I_shared : L.I;
+            const int fmt = sh ? FS : FR;
+            const size_t rowA = (size_t)D.expert[slot] * N + n0 + g;
+            const size_t rb = (size_t)(H / 2);
+            ic_c0 = PG.packed + rowA * rb + 16 * q;
+            ic_c1 = ic_c0 + 8 * rb;
+            ic_c2 = PU.packed + rowA * rb + 16 * q;
+            ic_c3 = ic_c2 + 8 * rb;
+            ic_sfb = fmt == MOE_FMT_NVFP4 ? 8 : 4;
+            const ProjView& PS = (q >> 1) ? PU : PG;  // this lane stages (row g + 8 (q & 1), matrix q >> 1)
+            ic_sp = PS.scales + (rowA + 8 * (q & 1)) * (size_t)(H / (fmt == MOE_FMT_NVFP4 ? 16 : 32));
+            ic_ap = x_src(ic_j);
+        } else if (ic_phase == 1) {
+            if (ic_j >= npairs) {
+                ic_phase = 2;
+                return;
+            }
+            int tl, slot;
+            pair_of(ic_j, tl, slot);
+            const bool sh = slot == n_active;
             const ProjView& PD = sh ? L.sh_down : L.down;
             const int K = sh ? L.I_shared : L.I;
-            const int svb = (sh ? FMT_S : FMT_R) == MOE_FMT_NVFP4 ? 16 : 32;
-            const size_t rowA = (size_t)e * L.H + n0 + g;
-            const uint32_t st = rbase + (i % kDnStages) * kDnStageBytes;
-            cp_async16(st + lane * 16, PD.packed + rowA * (K / 2) + 16 * q + is_s * 64);
-            cp_async16(st + 512 + lane * 16, PD.packed + (rowA + 8) * (K / 2) + 16 * q + is_s * 64);
-            if (q < 2) {  // scales of row g + 8q
-                const uint8_t* sp = PD.scales + (rowA + 8 * q) * (K / svb);
-                if (svb == 16) cp_async8(st + 1024 + lane * 8, sp + is_s * 8);
-                else cp_async4(st + 1024 + lane * 8, sp + is_s * 4);
+            const int fmt = sh ? FS : FR;
+            const size_t rowA = (size_t)D.expert[slot] * H + (size_t)(cta + tl * G) * 16 + g;
+            ic_c0 = PD.packed + rowA * (size_t)(K / 2) + 16 * q;
+            ic_c1 = ic_c0 + 8 * (size_t)(K / 2);
+            ic_sfb = fmt == MOE_FMT_NVFP4 ? 8 : 4;
+            ic_sp = PD.scales + (rowA + 8 * (q & 1)) * (size_t)(K / (fmt == MOE_FMT_NVFP4 ? 16 : 32));
+            ic_ap = h_src(slot);
+            ic_ns = K / 128;
+        }
+    };
+    ic_enter();
+    int issued = 0;
+    auto issue_next = [&]() {
+        const uint32_t st = rbase + (issued % kDecStages) * kDecStageBytes;
+        if (ic_phase == 0) {
+            const int o = ic_s * 64;
+            cp_async16(st + 0 * 512 + lane * 16, ic_c0 + o);
+            cp_async16(st + 1 * 512 + lane * 16, ic_c1 + o);
+            cp_async16(st + 2 * 512 + lane * 16, ic_c2 + o);
+            cp_async16(st + 3 * 512 + lane * 16, ic_c3 + o);
+            if (ic_sfb == 8) cp_async8(st + kDecStageScales + lane * 8, ic_sp + ic_s * 8);
+            else cp_async4(st + kDecStageScales + lane * 8, ic_sp + ic_s * 4);
+            copy_act(st, ic_ap ? ic_ap + ic_s * 128 : nullptr);
+            ic_s += kDecWarps;
+            if (ic_s >= ksteps_g) {
+                ic_s = warp;
+                if (++ic_j == cnt_g) {
+                    ic_phase = 1;
+                    ic_j = warp;
+                    ic_s = 0;
+                }
+                ic_enter();
             }
-            if (++is_s == K / 128) {
-                is_s = 0;
-                is_slot += kDnWarps;
+        } else if (ic_phase == 1) {
+            const int o = ic_s * 64;
+            cp_async16(st + lane * 16, ic_c0 + o);
+            cp_async16(st + 512 + lane * 16, ic_c1 + o);
+            if (q < 2) {  // scales of row g + 8 q
+                if (ic_sfb == 8) cp_async8(st + kDecStageScales + lane * 8, ic_sp + ic_s * 8);
+                else cp_async4(st + kDecStageScales + lane * 8, ic_sp + ic_s * 4);
+            }
+            if (h_ready) copy_act(st, ic_ap ? ic_ap + ic_s * 128 : nullptr);
+            if (++ic_s == ic_ns) {
+                ic_s = 0;
+                ic_j += kDecWarps;
+                ic_enter();
             }
         }
         cp_async_commit();
+        ++issued;
     };
+    // ring invariant: before a warp consumes n (1 or 2) stages from position c, stages
+    // c .. c + S - 3 are issued; it issues n more (into the stages freed by c - 2 and c - 1)
+    // and waits until at most S - 2 groups are pending, so c .. c + n - 1 have landed.
 #pragma unroll 1
-    for (int i = 0; i < kDnStages - 1; ++i) issue(i);
+    for (int i = 0; i < kDecStages - 2; ++i) issue_next();
+    int consumed = 0;
+    auto stage_ptr = [&](int c) { return ring + (c % kDecStages) * kDecStageBytes; };
 
-    pdl_wait();  // h comes from the gate+up kernel
-
-    int hs_slot = warp, hs_s = 0;  // h cursor (one step ahead of the compute)
-    auto load_h = [&](uint4 (&b)[4]) {
-        const bool ok = hs_slot < nslots && ((D.tokmask[hs_slot] >> g) & 1u);  // column g = token g
-        const __half* hrow = L.h16 + ((size_t)hs_slot * kDecMaxT + g) * Imax + 32 * q + hs_s * 128;
+    // ---- phase 2: gate+up ------------------------------------------------------------------------
+    for (int j = 0; j < cnt_g; ++j) {
+        int slot, n0;
+        task_of(j, slot, n0);
+        const bool sh = slot == n_active;
+        const int e = D.expert[slot];
+        const ProjView& PG = sh ? L.sh_gate : L.gate;
+        const ProjView& PU = sh ? L.sh_up : L.up;
+        const int fmt = sh ? FS : FR;
+        const int mxg = fmt == MOE_FMT_MXFP4 ? 112 + PG.mx_off[e] : 0;
+        const int mxu = fmt == MOE_FMT_MXFP4 ? 112 + PU.mx_off[e] : 0;
+        const bool has_tok = nth_bit(D.tokmask[slot], g) >= 0;
+        float accG[4][4] = {}, accU[4][4] = {};
+        for (int s = 0; s < n_g; s += 2) {
+            const bool two = s + 1 < n_g;
+            issue_next();
+            if (two) issue_next();
+            cp_async_wait<kDecStages - 2>();
+            __syncwarp();
+            const uint8_t *st0 = stage_ptr(consumed), *st1 = stage_ptr(consumed + 1);
+            if (fmt == MOE_FMT_NVFP4) {
+                if (two) gu_steps<MOE_FMT_NVFP4, 2>(st0, st1, has_tok, lane, g, q, mxg, mxu, accG, accU);
+                else gu_steps<MOE_FMT_NVFP4, 1>(st0, st1, has_tok, lane, g, q, mxg, mxu, accG, accU);
+            } else {
+                if (two) gu_steps<MOE_FMT_MXFP4, 2>(st0, st1, has_tok, lane, g, q, mxg, mxu, accG, accU);
+                else gu_steps<MOE_FMT_MXFP4, 1>(st0, st1, has_tok, lane, g, q, mxg, mxu, accG, accU);
+            }
+            consumed += two ? 2 : 1;
+        }
+        // K-split reduction, double-buffered: one CTA barrier per task
+        float* rg = red_g + (j & 1) * kDecWarps * 256;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) b[j] = ok ? ldg_cached128(hrow + 8 * j) : make_uint4(0, 0, 0, 0);
-        if (hs_slot < nslots && ++hs_s == (hs_slot == D.n_active ? L.I_shared : L.I) / 128) {
-            hs_s = 0;
-            hs_slot += kDnWarps;
+        for (int i = 0; i < 4; ++i) {
+            rg[(warp * 8 + i) * 32 + lane] = sum4(accG, i);
+            rg[(warp * 8 + 4 + i) * 32 + lane] = sum4(accU, i);
         }
-    };
-    uint4 hb[4], hn[4];
-    if (total > 0) load_h(hb);
-
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, part[4] = {0.f, 0.f, 0.f, 0.f};
-    int cs_slot = warp, cs_s = 0;  // consume cursor
-    for (int i = 0; i < total; ++i) {
-        issue(i + kDnStages - 1);
-        if (i + 1 < total) load_h(hn);
-        cp_async_wait<kDnStages - 1>();
-        __syncwarp();
-        const bool sh = cs_slot == D.n_active;
-        const int e = D.expert[cs_slot];
-        const uint8_t* st = ring + (i % kDnStages) * kDnStageBytes;
-        ChunkA c;
-        c.r0 = *reinterpret_cast<const uint4*>(st + lane * 16);
-        c.r1 = *reinterpret_cast<const uint4*>(st + 512 + lane * 16);
-        const uint2* sc = reinterpret_cast<const uint2*>(st + 1024);
-        if ((sh ? FMT_S : FMT_R) == MOE_FMT_NVFP4) {
-            scales_from_raw<MOE_FMT_NVFP4>(sc[g * 4 + 0], q, 0, c.s0lo, c.s0hi);
-            scales_from_raw<MOE_FMT_NVFP4>(sc[g * 4 + 1], q, 0, c.s1lo, c.s1hi);
-        } else {
-            const int mx = 112 + (sh ? L.sh_down : L.down).mx_off[e];
-            scales_from_raw<MOE_FMT_MXFP4>(sc[g * 4 + 0], q, mx, c.s0lo, c.s0hi);
-            scales_from_raw<MOE_FMT_MXFP4>(sc[g * 4 + 1], q, mx, c.s1lo, c.s1hi);
+        __syncthreads();
+        if (tid < 128) {
+            const int i = tid >> 5, ln = tid & 31;
+            float Gs = 0.f, Us = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) {
+                Gs += rg[(w * 8 + i) * 32 + ln];
+                Us += rg[(w * 8 + 4 + i) * 32 + ln];
+            }
+            const int row = (ln >> 2) + 8 * (i >> 1), col = 2 * (ln & 3) + (i & 1);
+            const int t = nth_bit(D.tokmask[slot], col);  // column -> token
+            if (t >= 0) {
+                const float hv = silu_f32(Gs * PG.post[e]) * (Us * PU.post[e]);
+                L.h16[((size_t)slot * kDecMaxT + t) * Imax + n0 + row] = __float2half_rn(hv);
+            }
         }
-        __syncwarp();  // every lane has read this stage before it is refilled
-#define DOWN_STEP(I)                                                                       \
-    {                                                                                      \
-        uint32_t fa[4];                                                                    \
-        frag_a<I>(c, fa);                                                                  \
-        mma_f16_16816(part, fa[0], fa[1], fa[2], fa[3], word_of(hb[I >> 1], (I & 1) * 2),  \
-                      word_of(hb[I >> 1], (I & 1) * 2 + 1));                               \
     }
-        DOWN_STEP(0) DOWN_STEP(1) DOWN_STEP(2) DOWN_STEP(3)
-        DOWN_STEP(4) DOWN_STEP(5) DOWN_STEP(6) DOWN_STEP(7)
-#undef DOWN_STEP
+    grid_barrier(bar, L.status);  // every h is written (and red_g is no longer read)
+
+    // ---- phase 3: down + weighted sum + shared expert ----------------------------------------------
+    // the h chunks of the down steps already in the ring, then every later stage copies its own
+    h_ready = true;
+    for (int p = warp, idx = 0; p < npairs && done_g + idx < issued; p += kDecWarps) {
+        int tl, slot;
+        pair_of(p, tl, slot);
+        const __half* a = h_src(slot);
+        const int ns = (slot == n_active ? L.I_shared : L.I) / 128;
+        for (int s = 0; s < ns && done_g + idx < issued; ++s, ++idx)
+            copy_act(rbase + ((done_g + idx) % kDecStages) * kDecStageBytes, a ? a + s * 128 : nullptr);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    float acc[kDecMaxTilesPerCta][4] = {};
+    for (int p = warp; p < npairs; p += kDecWarps) {
+        int tl, slot;
+        pair_of(p, tl, slot);
+        const bool sh = slot == n_active;
+        const int e = D.expert[slot];
+        const ProjView& PD = sh ? L.sh_down : L.down;
+        const int fmt = sh ? FS : FR;
+        const int mx = fmt == MOE_FMT_MXFP4 ? 112 + PD.mx_off[e] : 0;
+        const int ns = (sh ? L.I_shared : L.I) / 128;
+        const bool has_tok = (D.tokmask[slot] >> g) & 1u;
+        float part[4][4] = {};
+        for (int s = 0; s < ns; s += 2) {
+            const bool two = s + 1 < ns;
+            issue_next();
+            if (two) issue_next();
+            cp_async_wait<kDecStages - 2>();
+            __syncwarp();
+            const uint8_t *st0 = stage_ptr(consumed), *st1 = stage_ptr(consumed + 1);
+            if (fmt == MOE_FMT_NVFP4) {
+                if (two) dn_steps<MOE_FMT_NVFP4, 2>(st0, st1, has_tok, lane, g, q, mx, part);
+                else dn_steps<MOE_FMT_NVFP4, 1>(st0, st1, has_tok, lane, g, q, mx, part);
+            } else {
+                if (two) dn_steps<MOE_FMT_MXFP4, 2>(st0, st1, has_tok, lane, g, q, mx, part);
+                else dn_steps<MOE_FMT_MXFP4, 1>(st0, st1, has_tok, lane, g, q, mx, part);
+            }
+            consumed += two ? 2 : 1;
+        }
+        // expert done: fold in its post-scale and the token weights (MMA column = token)
+        const float post = PD.post[e];
+        const float w0 = D.w[slot][2 * q] * post, w1 = D.w[slot][2 * q + 1] * post;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) hb[j] = hn[j];
-        const int K = sh ? L.I_shared : L.I;
-        if (++cs_s == K / 128) {  // expert done: fold in with its post-scale and token weights
-            const float post = (sh ? L.sh_down : L.down).post[e];
-            const float w0 = D.w[cs_slot][2 * q] * post, w1 = D.w[cs_slot][2 * q + 1] * post;
-            acc[0] += part[0] * w0;
-            acc[1] += part[1] * w1;
-            acc[2] += part[2] * w0;
-            acc[3] += part[3] * w1;
-            part[0] = part[1] = part[2] = part[3] = 0.f;
-            cs_s = 0;
-            cs_slot += kDnWarps;
+        for (int t = 0; t < kDecMaxTilesPerCta; ++t) {
+            if (t == tl) {
+                acc[t][0] += sum4(part, 0) * w0;
+                acc[t][1] += sum4(part, 1) * w1;
+                acc[t][2] += sum4(part, 2) * w0;
+                acc[t][3] += sum4(part, 3) * w1;
+            }
         }
     }
     cp_async_wait<0>();
+    __syncthreads();  // every warp is done with the ring and red_g
 #pragma unroll
-    for (int i = 0; i < 4; ++i) red[(warp * 4 + i) * 32 + lane] = acc[i];
+    for (int t = 0; t < kDecMaxTilesPerCta; ++t)
+        if (t < cnt_d)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red_d[(t * kDecWarps + warp) * 128 + i * 32 + lane] = acc[t][i];
     __syncthreads();
-    pdl_trigger();
-    if (warp == 0) {
-        float o[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int w = 0; w < kDnWarps; ++w)
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(L.out);
+    for (int o = tid; o < cnt_d * 128; o += kDecThreads) {
+        const int tl = o >> 7, r = o & 127, i = r >> 5, ln = r & 31;
+        float sum = 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] += red[(w * 4 + i) * 32 + lane];
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(L.out);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int t = 2 * q + j;
-            if (t < L.T) {
-                out[(size_t)t * L.H + n0 + g] = __float2bfloat16_rn(o[j]);
-                out[(size_t)t * L.H + n0 + g + 8] = __float2bfloat16_rn(o[2 + j]);
-            }
-        }
+        for (int w = 0; w < kDecWarps; ++w) sum += red_d[(tl * kDecWarps + w) * 128 + r];
+        const int row = (ln >> 2) + 8 * (i >> 1), col = 2 * (ln & 3) + (i & 1);
+        if (col < T) out[(size_t)col * H + (size_t)(cta + tl * G) * 16 + row] = __float2bfloat16_rn(sum);
     }
 }
 
 // ------------------------------------------------------------------------------------------
-template <typename Kern>
-static cudaError_t set_smem(Kern kernel, int bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
-
-template <typename... KArgs, typename... Args>
-static cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem,
-                                   cudaStream_t st, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
+int decode_smem_bytes(int H, int sms) {
+    const int tpc = (H / 16 + sms - 1) / sms;
+    if (tpc > kDecMaxTilesPerCta) return -1;
+    return kDecRingBytes + (kDecRedG > tpc * kDecRedDTile ? kDecRedG : tpc * kDecRedDTile);
 }
 
 template <int FR, int FS>
-static cudaError_t launch_decode_fmt(const FfnLaunch& L, int phase, cudaStream_t st) {
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+static cudaError_t launch_fused_fmt(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
+                                    int sms, cudaStream_t st) {
+    const int smem = decode_smem_bytes(L.H, sms);
+    if (smem < 0) return cudaErrorInvalidConfiguration;
+    auto kern = dec_fused_kernel<FR, FS>;
     cudaError_t err;
-    if (phase == 1) {
-        const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
-        const int tiles = Imax / 16;
-        const int slots = (L.E < L.T * L.k ? L.E : L.T * L.k) + (L.I_shared > 0 ? 1 : 0);
-        int grid = slots * tiles;
-        if (grid > 2 * sms) grid = 2 * sms;  // two per SM, leaving room for the down kernel
-        if ((err = set_smem(dec_gateup_kernel<FR, FS>, kGuSmem)) != cudaSuccess) return err;
-        return launch_pdl_smem(dec_gateup_kernel<FR, FS>, dim3(grid), dim3(kGuWarps * 32), kGuSmem,
-                               st, L, tiles);
-    }
-    if ((err = set_smem(dec_down_kernel<FR, FS>, kDnSmem)) != cudaSuccess) return err;
-    return launch_pdl_smem(dec_down_kernel<FR, FS>, dim3(L.H / 16), dim3(kDnWarps * 32), kDnSmem,
-                           st, L);
+    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+        return err;
+    int per_sm = 0;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecThreads, smem)) != cudaSuccess)
+        return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);  // one CTA per SM, all co-resident (cooperative launch)
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, L, R, bar);
 }
 
-cudaError_t launch_decode_phase(const FfnLaunch& L, int phase, cudaStream_t st) {
+cudaError_t launch_decode_fused(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
+                                int sms, cudaStream_t st) {
     const int fr = L.gate.fmt;
     const int fs = L.I_shared > 0 ? L.sh_gate.fmt : fr;
-    if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_NVFP4) return launch_decode_fmt<0, 0>(L, phase, st);
-    if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_MXFP4) return launch_decode_fmt<0, 1>(L, phase, st);
-    if (fr == MOE_FMT_MXFP4 && fs == MOE_FMT_NVFP4) return launch_decode_fmt<1, 0>(L, phase, st);
-    return launch_decode_fmt<1, 1>(L, phase, st);
+    if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_NVFP4) return launch_fused_fmt<0, 0>(L, R, bar, sms, st);
+    if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_MXFP4) return launch_fused_fmt<0, 1>(L, R, bar, sms, st);
+    if (fr == MOE_FMT_MXFP4 && fs == MOE_FMT_NVFP4) return launch_fused_fmt<1, 0>(L, R, bar, sms, st);
+    return launch_fused_fmt<1, 1>(L, R, bar, sms, st);
 }
 
 }  // namespace moe

@@ -402,12 +402,6 @@ cudaError_t launch_ffn(const FfnLaunch& L, cudaStream_t st, const PhaseEvents* e
     if (conv_blocks < 1) conv_blocks = 1;
     const int slots_r = L.E < L.T * L.k ? L.E : L.T * L.k;
     const int64_t nthreads = (int64_t)L.T * (L.H / 8);
-    if (L.path == PATH_DECODE) {
-        // few tokens: dispatch is rebuilt inside both kernels, combine fused into down
-        MOE_PHASE(1, err = launch_decode_phase(L, 1, st); if (err != cudaSuccess) return err)
-        MOE_PHASE(2, err = launch_decode_phase(L, 2, st); if (err != cudaSuccess) return err)
-        return cudaSuccess;
-    }
     MOE_PHASE(0, (prep_kernel<<<1 + conv_blocks, 512, 0, st>>>(L)))
     MOE_PHASE(1, launch_expert_phase<MODE_GATEUP>(L, slots_r, st))
     MOE_PHASE(2, launch_expert_phase<MODE_DOWN>(L, slots_r, st))

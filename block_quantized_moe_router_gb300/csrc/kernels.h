@@ -127,8 +127,33 @@ void tc_release(TcWeights* tw);
 cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffers& B,
                           cudaStream_t st, const PhaseEvents* ev);
 
-// Few-token path (T <= 8, bf16 activations): phase 1 = gate+up, phase 2 = down + combine.
-cudaError_t launch_decode_phase(const FfnLaunch& L, int phase, cudaStream_t st);
+// Few-token path (T <= 8, T * top_k <= 64, bf16 activations): the whole block in one
+// persistent cooperative launch of `sms` CTAs (decode.cu).  Where the routing comes from:
+enum DecRouteMode {
+    DEC_ROUTE_GIVEN = 0,   // ids / weights in L.ids / L.w
+    DEC_ROUTE_ROUTER = 1,  // router GEMM (w_router, x) -> logits_out, then top-K
+    DEC_ROUTE_LOGITS = 2,  // top-K of logits_in
+    DEC_ROUTE_HASH = 3     // tid2eid[token_ids]
+};
+struct DecRoute {
+    int mode;
+    const void* w_router;     // bf16 [E][H]
+    const float* logits_in;   // [T][E]
+    float* logits_out;        // [T][E]
+    const float* bias;        // [E] or null (selection only)
+    int scoring, renorm;
+    float scaling;
+    const int64_t* tid2eid;   // [vocab][k]
+    const int32_t* token_ids; // [T]
+    int64_t vocab;
+    int32_t* ids_out;         // [T][k] (modes 1-3)
+    float* w_out;             // [T][k]
+};
+// `bar`: a device 64-bit counter, zero when first used, owned by the weights handle and used
+// only by launches of `sms` CTAs.
+cudaError_t launch_decode_fused(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
+                                int sms, cudaStream_t st);
+int decode_smem_bytes(int H, int sms);
 
 cudaError_t launch_quantize_act(const void* x, int64_t rows, int64_t K, float g, uint8_t* packed,
                                 uint8_t* scales, __half* deq16, cudaStream_t st);

@@ -10,6 +10,7 @@
 // router GEMM feeding an fp32-input top-K).  Ids and weights stay on the device.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -197,16 +198,6 @@ router_gemm_tiled_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat1
 // lower index.  Non-finite logits get score -inf and weight 0.
 // ------------------------------------------------------------------------------------------
 // score of the sigmoid-style routers
-__device__ __forceinline__ float gate_score(int scoring, float l) {
-    if (scoring == MOE_SCORE_SQRTSOFTPLUS) return sqrtf(l > 30.f ? l : log1pf(expf(l)));
-    return 1.0f / (1.0f + expf(-l));
-}
-
-__device__ __forceinline__ uint32_t orderable(float v) {
-    const uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 template <int EPL>
 __global__ void __launch_bounds__(256)
 topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
@@ -218,73 +209,14 @@ topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, in
     const int t = blockIdx.x * (blockDim.x >> 5) + warp;
     if (t >= T) return;
     const float* row = logits + (size_t)t * E;
-    unsigned long long key[EPL];
-    float lg[EPL];
-    bool nonfinite = false;
-    float lmax = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-        const int e = lane + 32 * j;
-        key[j] = 0ull;
-        lg[j] = -INFINITY;
-        if (e < E) {
-            const float l = row[e];
-            float v = -INFINITY;
-            if (!isfinite(l)) {
-                nonfinite = true;
-            } else {
-                lg[j] = l;
-                lmax = fmaxf(lmax, l);
-                v = (scoring == MOE_SCORE_SOFTMAX) ? l : gate_score(scoring, l) + (bias ? bias[e] : 0.f);
-            }
-            key[j] = ((unsigned long long)orderable(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
-        }
-    }
-    if (__any_sync(0xffffffffu, nonfinite) && lane == 0) status_or(status, MOE_DEV_NONFINITE);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
-
-    int my_e = 0;
-    for (int r = 0; r < k; ++r) {
-        unsigned long long best = key[0];
-#pragma unroll
-        for (int j = 1; j < EPL; ++j) best = key[j] > best ? key[j] : best;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-            best = other > best ? other : best;
-        }
-        const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
-        if ((e & 31) == lane) {
-#pragma unroll
-            for (int j = 0; j < EPL; ++j)
-                if (j == (e >> 5)) key[j] = 0ull;
-        }
-        if (lane == r) my_e = e;
-    }
-    float num = 0.f;
-    if (lane < k) {
-        const float l = row[my_e];
-        if (isfinite(l))
-            num = (scoring == MOE_SCORE_SOFTMAX) ? expf(l - lmax) : gate_score(scoring, l);
-    }
-    float den = 1.f;
-    if (renorm) {
-        den = num;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    } else if (scoring == MOE_SCORE_SOFTMAX) {
-        float z = 0.f;
-#pragma unroll
-        for (int j = 0; j < EPL; ++j)
-            if (isfinite(lg[j])) z += expf(lg[j] - lmax);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        den = z;
-    }
+    int my_e;
+    float my_w;
+    const bool nonfinite = warp_topk<EPL>([&](int e) { return row[e]; }, bias, E, k, scoring,
+                                          renorm, scaling, lane, my_e, my_w);
+    if (nonfinite && lane == 0) status_or(status, MOE_DEV_NONFINITE);
     if (lane < k) {
         ids[(size_t)t * k + lane] = my_e;
-        wout[(size_t)t * k + lane] = (den > 0.f ? num / den : 0.f) * scaling;
+        wout[(size_t)t * k + lane] = my_w;
     }
 }
 

@@ -93,6 +93,26 @@ class MoeLayer:
                              topk_w, out, self.workspace(T), dev_status=self.status, stream=stream)
         return out
 
-    def forward(self, x, token_ids=None, out=None, stream=None):
-        ids, w, _ = self.route(x, token_ids=token_ids, stream=stream)
-        return self.ffn(x, ids, w, out=out, stream=stream)
+    def forward(self, x=None, *, token_ids=None, logits_in=None, out=None, topk_ids=None,
+                topk_w=None, logits_out=None, stream=None):
+        """Route + FFN through moe_forward (one launch for a few tokens).
+        Returns (out, topk_ids, topk_w, logits_out)."""
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.bfloat16, device="cuda")
+        if topk_ids is None:
+            topk_ids = torch.empty((T, self.top_k), dtype=torch.int32, device="cuda")
+        if topk_w is None:
+            topk_w = torch.empty((T, self.top_k), dtype=torch.float32, device="cuda")
+        if (logits_out is None and logits_in is None and self.scoring != capi.MOE_SCORE_HASH):
+            logits_out = torch.empty((T, self.E), dtype=torch.float32, device="cuda")
+        d = capi.route_desc(T=T, E=self.E, H=self.H, top_k=self.top_k, scoring=self.scoring,
+                            renormalize=self.renormalize, routed_scaling=self.routed_scaling,
+                            w_router=None if logits_in is not None else self.w_router,
+                            correction_bias=self.correction_bias, tid2eid=self.tid2eid,
+                            vocab=0 if self.tid2eid is None else self.tid2eid.shape[0],
+                            token_ids=token_ids)
+        capi.moe_forward(self.handle, d, self.act, self.g_act1, self.g_act2, x, topk_ids, topk_w,
+                         out, self.workspace(T), logits_in=logits_in, logits_out=logits_out,
+                         dev_status=self.status, stream=stream)
+        return out, topk_ids, topk_w, logits_out

@@ -138,11 +138,32 @@ moe_status_t moe_release_weights(void* handle);
  * power of two) before the FP4 products; MOE_ACT_BF16 ignores both.
  * x_bf16 [device] bf16 [T][H]; topk_ids/topk_w as written by moe_route;
  * out_bf16 [device] bf16 [T][H]; workspace [device], ws_bytes >= moe_workspace_size.
- * T == 0 is a valid no-op. */
+ * T == 0 is a valid no-op.  Few tokens (T <= 8, T * top_k <= 64, MOE_ACT_BF16) run as one
+ * persistent cooperative launch with the constraints stated at moe_forward. */
 moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g_act1,
                              float g_act2, const void* x_bf16, const int32_t* topk_ids,
                              const float* topk_w, void* out_bf16, void* workspace,
                              size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Route + expert FFN in one call: the result of moe_route(route, x_bf16, logits_in,
+ * logits_out, topk_ids, topk_w, dev_status) followed by moe_ffn_forward(handle, route->T, act,
+ * g_act1, g_act2, x_bf16, topk_ids, topk_w, out_bf16, workspace, ws_bytes, dev_status), with the
+ * same argument rules, outputs and workspace size (moe_workspace_size of the handle's
+ * descriptor).  route->E, route->top_k and route->H must equal the handle's E, top_k and H.
+ * For a few tokens (T <= 8, T * top_k <= 64, act == MOE_ACT_BF16) the router GEMV, the top-K
+ * selection (or the hash lookup), the expert FFN and the weighted sum run in ONE persistent
+ * kernel launch with one thread block per SM and two device-wide barriers -- the single-launch
+ * decode structure that the spark_model MoE module doc (moe/mod.rs) works towards by fusing
+ * the gate with the top-K; there the router logits come from fp32 dot products on the CUDA
+ * cores, so they can differ from moe_route's in the last bits.  That launch is cooperative:
+ * it needs every SM of the device free to co-schedule (MOE_ERR_CUDA if the device cannot run
+ * it), and calls on one handle must not overlap on the GPU (the handle owns the barrier
+ * counter).  If a device-side barrier wait gives up (MOE_DEV_TIMEOUT) the outputs of that
+ * call are invalid and the handle must be released and prepared again. */
+moe_status_t moe_forward(const void* handle, const moe_route_desc* route, int32_t act,
+                         float g_act1, float g_act2, const void* x_bf16, const float* logits_in,
+                         float* logits_out, int32_t* topk_ids, float* topk_w, void* out_bf16,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* The NVFP4 activation quantizer on its own (the `quantize_bf16_to_nvfp4` step of the
  * FP4 x FP4 recipe, qwen3_attention/init.rs handle list): per 16 consecutive elements of

@@ -1,0 +1,183 @@
+"""GPU parity of moe_forward: route + expert FFN in one call through the C ABI.
+
+For a few tokens (T <= 8, T * top_k <= 64, bf16 activations) the whole block -- router GEMV,
+top-K (or the hash lookup), gate+up, SiLU * up, down, top-K weighted sum and shared expert --
+runs as one persistent launch (the single-launch decode structure of the spark_model MoE
+module doc, moe/mod.rs, with the gate fused into the top-K).  Larger batches take moe_route then
+moe_ffn_forward.  Ids are bit-exact against the fp64 oracle on gap-safe inputs; weights are
+checked against the oracle's top-K of the GPU's own fp32 logits; outputs within
+max|gpu - ref| <= 1e-2 * max|ref| + 1e-3.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import parity
+from block_quantized_moe_router_gb300 import capi, synth
+from block_quantized_moe_router_gb300.layer import MoeLayer
+
+pytestmark = pytest.mark.gpu
+
+S = synth
+CASES = {
+    "tiny": S.CONFIGS["tiny"],
+    # H / 128 = 3 K-steps: five of the eight warps have no gate+up work
+    "ragged": S.MoeConfig("fw_ragged", T=7, H=384, I=256, E=10, k=3, scoring=S.SCORE_SOFTMAX,
+                          I_shared=384),
+    "sigmoid_mx": S.MoeConfig("fw_sigmoid_mx", T=5, H=2304, I=384, E=12, k=4,
+                              scoring=S.SCORE_SIGMOID, scaling=2.5, I_shared=128,
+                              fmt=S.FMT_MXFP4, shared_fmt=S.FMT_NVFP4),
+    # 64 routed pairs: the largest dispatch the single launch takes
+    "max_pairs": S.MoeConfig("fw_max_pairs", T=8, H=256, I=128, E=40, k=8,
+                             scoring=S.SCORE_SIGMOID, scaling=1.5, I_shared=256,
+                             fmt=S.FMT_NVFP4, shared_fmt=S.FMT_MXFP4),
+    "sqrtsoftplus": S.MoeConfig("fw_sqrtsoftplus", T=3, H=512, I=256, E=24, k=5,
+                                scoring=S.SCORE_SQRTSOFTPLUS, scaling=1.5, I_shared=256),
+    "hash": S.MoeConfig("fw_hash", T=6, H=256, I=256, E=16, k=4, scoring=S.SCORE_HASH,
+                        I_shared=128, fmt=S.FMT_MXFP4, vocab=50),
+    "t1_no_renorm": S.MoeConfig("fw_t1", T=1, H=512, I=128, E=16, k=4, scoring=S.SCORE_SOFTMAX,
+                                renorm=False),
+    "many_experts": S.MoeConfig("fw_many_e", T=2, H=512, I=256, E=512, k=8,
+                                scoring=S.SCORE_SOFTMAX),
+    # more tokens: moe_route + moe_ffn_forward behind the same call
+    "fallback_generic": S.MoeConfig("fw_generic", T=20, H=256, I=128, E=16, k=3,
+                                    scoring=S.SCORE_SIGMOID, scaling=2.5, I_shared=128),
+    "fallback_tc": S.MoeConfig("fw_tc", T=40, H=512, I=256, E=16, k=4, scoring=S.SCORE_SIGMOID,
+                               scaling=2.5, I_shared=256, act=S.ACT_NVFP4),
+}
+
+
+def _forward(layer, inp, logits_in=None):
+    x = inp["x"].cuda()
+    tok = inp["token_ids"].cuda() if "token_ids" in inp else None
+    out, ids, w, logits = layer.forward(x, token_ids=tok, logits_in=logits_in)
+    torch.cuda.synchronize()
+    return out, ids, w, logits
+
+
+def _check(cfg, inp, ref_r, out, ids, w, logits, status, tokens=None):
+    assert status == 0
+    parity.assert_routing(cfg, ref_r, ids, w, gpu_logits=logits, inp=inp)
+    if logits is not None:
+        ref_l = ref_r["logits"]
+        rel = np.abs(logits.double().cpu().numpy() - ref_l).max() / np.abs(ref_l).max()
+        assert rel < 1e-4, f"router logits off by {rel:.2e} (relative)"
+    ref = parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"], tokens=tokens)
+    parity.assert_close(out if tokens is None else out[tokens], ref, cfg.name)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_forward_small(cuda_lib, name):
+    cfg = CASES[name]
+    inp, _ = parity.make_case(cfg, seed=3, device="cpu")
+    ref_r = parity.oracle_route(cfg, inp)
+    layer = MoeLayer.from_inputs(inp)
+    out, ids, w, logits = _forward(layer, inp)
+    _check(cfg, inp, ref_r, out, ids, w, logits, int(layer.status.item()))
+    layer.close()
+
+
+@pytest.mark.parametrize("name", ["dec1", "dec8"])
+def test_forward_full_size(cuda_lib, name):
+    cfg = S.CONFIGS[name]
+    inp, _ = parity.make_case(cfg, seed=0, device="cuda")
+    ref_r = parity.oracle_route(cfg, inp)
+    layer = MoeLayer.from_inputs(inp)
+    out, ids, w, logits = _forward(layer, inp)
+    _check(cfg, inp, ref_r, out, ids, w, logits, int(layer.status.item()))
+    layer.close()
+
+
+def test_forward_logits_in(cuda_lib):
+    cfg = CASES["sigmoid_mx"]
+    inp, _ = parity.make_case(cfg, seed=4, device="cpu")
+    ref_r = parity.oracle_route(cfg, inp)
+    layer = MoeLayer.from_inputs(inp)
+    lg = torch.from_numpy(ref_r["logits"].astype(np.float32)).cuda()
+    out, ids, w, logits = _forward(layer, inp, logits_in=lg)
+    assert logits is None
+    parity.assert_routing(cfg, ref_r, ids, w, gpu_logits=lg, inp=inp)
+    parity.assert_close(out, parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"]), "logits_in")
+    layer.close()
+
+
+def test_forward_repeat_and_graph_replay(cuda_lib):
+    """Back-to-back launches and CUDA-graph replays on one handle give identical results (the
+    device barrier counter carries over from launch to launch)."""
+    cfg = CASES["ragged"]
+    inp, _ = parity.make_case(cfg, seed=5, device="cpu")
+    layer = MoeLayer.from_inputs(inp)
+    x = inp["x"].cuda()
+    out0, ids0, w0, _ = layer.forward(x)
+    outs = [layer.forward(x)[0] for _ in range(5)]
+    st = torch.cuda.Stream()
+    o = torch.empty_like(out0)
+    ids = torch.empty_like(ids0)
+    w = torch.empty_like(w0)
+    lg = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(st):
+        layer.forward(x, out=o, topk_ids=ids, topk_w=w, logits_out=lg)
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            layer.forward(x, out=o, topk_ids=ids, topk_w=w, logits_out=lg)
+        o.zero_()
+        for _ in range(4):
+            g.replay()
+    torch.cuda.synchronize()
+    for r in outs + [o]:
+        assert torch.equal(r, out0)
+    assert torch.equal(ids, ids0) and torch.equal(w, w0)
+    assert int(layer.status.item()) == 0
+    layer.close()
+
+
+def test_forward_dropped_pairs(cuda_lib):
+    cfg = CASES["hash"]
+    inp, _ = parity.make_case(cfg, seed=2, device="cpu")
+    tab = inp["tid2eid"].clone()
+    tok = inp["token_ids"]
+    tab[int(tok[1]), 2] = 77     # an id outside [0, E): that pair is dropped
+    inp["tid2eid"] = tab
+    bad_tok = inp["token_ids"].clone()
+    ref_r = parity.oracle_route(cfg, inp)
+    layer = MoeLayer.from_inputs(inp)
+    out, ids, w, _ = _forward(layer, inp)
+    assert int(layer.status.item()) == capi.MOE_DEV_BAD_EXPERT_ID
+    parity.assert_routing(cfg, ref_r, ids, w)
+    parity.assert_close(out, parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"]), "dropped")
+    # a token id outside the vocabulary drops all of that token's pairs
+    bad_tok[0] = cfg.vocab + 5
+    inp2 = dict(inp, token_ids=bad_tok)
+    ref2 = parity.oracle_route(cfg, inp2)
+    layer.status.zero_()
+    out2, ids2, w2, _ = _forward(layer, inp2)
+    assert int(layer.status.item()) & capi.MOE_DEV_BAD_TOKEN_ID
+    parity.assert_routing(cfg, ref2, ids2, w2)
+    parity.assert_close(out2, parity.oracle_ffn(cfg, inp2, ref2["ids"], ref2["w"]), "bad token")
+    layer.close()
+
+
+def test_forward_zero_tokens_and_arg_checks(cuda_lib):
+    cfg = CASES["tiny"]
+    inp, _ = parity.make_case(cfg, seed=0, device="cpu")
+    layer = MoeLayer.from_inputs(inp)
+    x0 = torch.zeros((0, cfg.H), dtype=torch.bfloat16, device="cuda")
+    out0, _, _, _ = layer.forward(x0)
+    torch.cuda.synchronize()
+    assert out0.shape == (0, cfg.H)
+    # a routing descriptor that does not match the weights handle is refused before any launch
+    x = inp["x"].cuda()
+    d = capi.route_desc(T=cfg.T, E=cfg.E + 1, H=cfg.H, top_k=cfg.k, scoring=cfg.scoring,
+                        renormalize=True, routed_scaling=1.0, w_router=layer.w_router)
+    with pytest.raises(capi.MoeError) as ei:
+        capi.moe_forward(layer.handle, d, capi.MOE_ACT_BF16, 1.0, 1.0, x,
+                         torch.empty((cfg.T, cfg.k), dtype=torch.int32, device="cuda"),
+                         torch.empty((cfg.T, cfg.k), device="cuda"),
+                         torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda"),
+                         layer.workspace(cfg.T),
+                         logits_out=torch.empty((cfg.T, cfg.E + 1), device="cuda"))
+    assert ei.value.status == capi.MOE_ERR_INVALID_ARG
+    layer.close()
