@@ -8,7 +8,7 @@
 //            looks the experts up in the hash table, or reads the given ids; CTA 0 writes
 //            the routing outputs.  Each CTA then derives the dispatch: the active experts in
 //            ascending id order, each with its tokens and routing weights.
-//   phase 2  gate+up: tasks (expert slot, 16 rows of I) dealt round-robin to the CTAs; the 8
+//   phase 2  gate+up: tasks (expert slot, 32 rows of I) dealt round-robin to the CTAs; the 8
 //            warps split K = H, partial sums meet in shared memory and h = SiLU(g) * u is
 //            written token-major to hT[slot][token][I] (f16).          -> grid barrier 2
 //   phase 3  down fused with the top-K weighted sum and the shared expert: each CTA owns
@@ -16,12 +16,14 @@
 //            folds W_down . h of a slot into its tile with the expert's post-scale and each
 //            token's weight; warps are reduced in a fixed order and bf16 rows are written.
 //
-// Every warp streams its operands through its own ring of asynchronous copies, S - 2 steps
-// ahead of the MMAs (which take one or two steps at a time), in ONE sequence that runs from its first gate+up step to its last down
-// step.  A stage holds the codes of rows g and g+8, their block scales and the activation
-// chunk of the step (x in f16 for gate+up, h for down).  The down weights depend only on
-// the routing, so they are already in flight while the CTA waits at barrier 2; the h
-// chunks of the down steps issued before that barrier are copied right after it.
+// Every warp streams its operands through its own ring of asynchronous copies, S - 1 stages
+// ahead of the MMAs, in ONE sequence that runs from its first gate+up stage to its last down
+// stage.  A gate+up stage is one 128-element K-step of 32 rows of gate and up (two MMA
+// tiles sharing the activation chunk of the step); a down stage is two K-steps of 16 rows.
+// A stage also holds the block scales and the activations (x in f16 for gate+up, h for
+// down).  The down weights depend only on the routing, so they are already in flight while
+// the CTA waits at barrier 2; the h chunks of the down stages issued before that barrier are
+// copied right after it.
 //
 // This is the "gate + top-K fused, expert FFN in two fused stages" structure of the
 // spark_model MoE module doc (moe/mod.rs) taken to a single launch, with the weighted sum
@@ -39,15 +41,19 @@ constexpr int kDecMaxT = 8;
 constexpr int kDecMaxSlots = 65;   // at most 64 routed pairs (T * top_k <= 64) + the shared expert
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kDecStages = 6;
-// one ring stage: codes (gate+up: 4 x 512 B; down: 2 x 512 B), the activation chunk
-// (32 lanes x 64 B, MMA column = lane / 4), then 32 lanes x 8 B of block scales
-constexpr int kDecStageAct = 2048, kDecStageScales = 4096;
-constexpr int kDecStageBytes = 4096 + 256;
+constexpr int kDecStages = 3;
+// one ring stage, three regions (512 B = 32 lanes x 16 B; MMA row g / column g = lane / 4):
+//   gate+up: [0, 4096)  codes, 512 B each of (tile t, matrix m, rows +8 r) at (4t + 2m + r)
+//            [4096, 6144) activation chunk, [6144, 6656) scales, 256 B per tile
+//   down:    [0, 4096)  activation chunks of the two K-steps, 2048 B each
+//            [4096, 6144) codes, 512 B each of (step u, rows +8 r) at (2u + r)
+//            [6144, 6656) scales, 256 B per step
+constexpr int kDecStageB = 4096, kDecStageC = 6144;
+constexpr int kDecStageBytes = 6656;
 constexpr int kDecRingBytes = kDecWarps * kDecStages * kDecStageBytes;
 // the gate+up partial sums (double-buffered) and, after barrier 2, the down partial sums
 // (one 16-row output tile per 4 KB) share one region
-constexpr int kDecRedG = 2 * kDecWarps * 256 * 4;
+constexpr int kDecRedG = 2 * kDecWarps * 512 * 4;
 constexpr int kDecRedDTile = kDecWarps * 128 * 4;
 constexpr int kDecMaxTilesPerCta = 4;
 // router phase: experts handled together per CTA, 8-element chunks per thread and expert
@@ -62,6 +68,10 @@ struct DecDispatch {
     int expert[kDecMaxSlots];     // slot -> expert id (ascending), shared slot -> 0
     uint32_t tokmask[kDecMaxSlots];
     float w[kDecMaxSlots][kDecMaxT];
+    // per slot and projection (gate, up, down): the fp32 post-scale and, for MXFP4, the
+    // exponent bias of the f16 block-scale conversion -- read once here instead of once per task
+    float post[kDecMaxSlots][3];
+    int mxb[kDecMaxSlots][3];
 };
 
 struct DecShared {
@@ -178,62 +188,60 @@ __device__ __forceinline__ void dec_dispatch(int T, int k, int E, int I_shared, 
     __syncthreads();
 }
 
-// ---- U (1 or 2) MMA steps of 128 K elements, their instruction streams interleaved ----------
-// gate+up: rows g / g+8 of gate (stage codes 0, 1) and up (2, 3); B = x in f16.
-template <int FMT, int U>
-__device__ __forceinline__ void gu_steps(const uint8_t* st0, const uint8_t* st1, bool has_tok,
-                                         int lane, int g, int q, int mxg, int mxu,
-                                         float (&accG)[4][4], float (&accU)[4][4]) {
-    uint4 bx[U][4];
-    ChunkA cg[U], cu[U];
+// ---- the MMAs of one ring stage ---------------------------------------------------------------
+// gate+up: one K-step of 32 rows (tiles t = 0, 1) of gate and up; B = x in f16.
+// acc[t][m][p]: tile t, matrix m (gate, up), MMA chain p (even / odd sub-steps).
+template <int FMT>
+__device__ __forceinline__ void gu_stage(const uint8_t* st, bool has_tok, int lane, int g, int q,
+                                         int mxg, int mxu, float (&acc)[2][2][2][4]) {
+    uint4 bx[4];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const uint8_t* st = u ? st1 : st0;
+    for (int c = 0; c < 4; ++c)
+        bx[c] = has_tok ? *reinterpret_cast<const uint4*>(st + kDecStageB + c * 512 + lane * 16)
+                        : make_uint4(0, 0, 0, 0);
+    ChunkA cw[2][2];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            bx[u][c] = has_tok ? *reinterpret_cast<const uint4*>(st + kDecStageAct + c * 512 + lane * 16)
-                               : make_uint4(0, 0, 0, 0);
-        cg[u].r0 = *reinterpret_cast<const uint4*>(st + 0 * 512 + lane * 16);
-        cg[u].r1 = *reinterpret_cast<const uint4*>(st + 1 * 512 + lane * 16);
-        cu[u].r0 = *reinterpret_cast<const uint4*>(st + 2 * 512 + lane * 16);
-        cu[u].r1 = *reinterpret_cast<const uint4*>(st + 3 * 512 + lane * 16);
-        const uint2* sc = reinterpret_cast<const uint2*>(st + kDecStageScales);
-        scales_from_raw<FMT>(sc[g * 4 + 0], q, mxg, cg[u].s0lo, cg[u].s0hi);
-        scales_from_raw<FMT>(sc[g * 4 + 1], q, mxg, cg[u].s1lo, cg[u].s1hi);
-        scales_from_raw<FMT>(sc[g * 4 + 2], q, mxu, cu[u].s0lo, cu[u].s0hi);
-        scales_from_raw<FMT>(sc[g * 4 + 3], q, mxu, cu[u].s1lo, cu[u].s1hi);
+    for (int t = 0; t < 2; ++t) {
+        const uint2* sc = reinterpret_cast<const uint2*>(st + kDecStageC + t * 256);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            cw[t][m].r0 = *reinterpret_cast<const uint4*>(st + (4 * t + 2 * m) * 512 + lane * 16);
+            cw[t][m].r1 = *reinterpret_cast<const uint4*>(st + (4 * t + 2 * m + 1) * 512 + lane * 16);
+            scales_from_raw<FMT>(sc[g * 4 + 2 * m], q, m ? mxu : mxg, cw[t][m].s0lo, cw[t][m].s0hi);
+            scales_from_raw<FMT>(sc[g * 4 + 2 * m + 1], q, m ? mxu : mxg, cw[t][m].s1lo, cw[t][m].s1hi);
+        }
     }
-    __syncwarp();  // every lane has read the stages before they are refilled
-#define DEC_GU(I)                                                                 \
-    _Pragma("unroll") for (int u = 0; u < U; ++u) {                               \
-        uint32_t fa[4], fb[4];                                                    \
-        frag_a<I>(cg[u], fa);                                                     \
-        frag_a<I>(cu[u], fb);                                                     \
-        const uint32_t b0 = word_of(bx[u][I >> 1], (I & 1) * 2);                  \
-        const uint32_t b1 = word_of(bx[u][I >> 1], (I & 1) * 2 + 1);              \
-        mma_f16_16816(accG[u * 2 + (I & 1)], fa[0], fa[1], fa[2], fa[3], b0, b1); \
-        mma_f16_16816(accU[u * 2 + (I & 1)], fb[0], fb[1], fb[2], fb[3], b0, b1); \
+    __syncwarp();  // every lane has read the stage before it is refilled
+#define DEC_GU(I)                                                                        \
+    {                                                                                    \
+        const uint32_t b0 = word_of(bx[I >> 1], (I & 1) * 2);                            \
+        const uint32_t b1 = word_of(bx[I >> 1], (I & 1) * 2 + 1);                        \
+        _Pragma("unroll") for (int t = 0; t < 2; ++t)                                    \
+        _Pragma("unroll") for (int m = 0; m < 2; ++m) {                                  \
+            uint32_t fa[4];                                                              \
+            frag_a<I>(cw[t][m], fa);                                                     \
+            mma_f16_16816(acc[t][m][I & 1], fa[0], fa[1], fa[2], fa[3], b0, b1);         \
+        }                                                                                \
     }
     DEC_GU(0) DEC_GU(1) DEC_GU(2) DEC_GU(3) DEC_GU(4) DEC_GU(5) DEC_GU(6) DEC_GU(7)
 #undef DEC_GU
 }
 
-// down: rows g / g+8 of W_down (stage codes 0, 1); B = h in f16.
+// down: U (1 or 2) K-steps of 16 rows of W_down; B = h in f16.  part[u][p]: step u, chain p.
 template <int FMT, int U>
-__device__ __forceinline__ void dn_steps(const uint8_t* st0, const uint8_t* st1, bool has_tok,
-                                         int lane, int g, int q, int mx, float (&part)[4][4]) {
+__device__ __forceinline__ void dn_stage(const uint8_t* st, bool has_tok, int lane, int g, int q,
+                                         int mx, float (&part)[2][2][4]) {
     uint4 hb[U][4];
     ChunkA c[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const uint8_t* st = u ? st1 : st0;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            hb[u][j] = has_tok ? *reinterpret_cast<const uint4*>(st + kDecStageAct + j * 512 + lane * 16)
+            hb[u][j] = has_tok ? *reinterpret_cast<const uint4*>(st + u * 2048 + j * 512 + lane * 16)
                                : make_uint4(0, 0, 0, 0);
-        c[u].r0 = *reinterpret_cast<const uint4*>(st + lane * 16);
-        c[u].r1 = *reinterpret_cast<const uint4*>(st + 512 + lane * 16);
-        const uint2* sc = reinterpret_cast<const uint2*>(st + kDecStageScales);
+        c[u].r0 = *reinterpret_cast<const uint4*>(st + kDecStageB + (2 * u) * 512 + lane * 16);
+        c[u].r1 = *reinterpret_cast<const uint4*>(st + kDecStageB + (2 * u + 1) * 512 + lane * 16);
+        const uint2* sc = reinterpret_cast<const uint2*>(st + kDecStageC + u * 256);
         scales_from_raw<FMT>(sc[g * 4 + 0], q, mx, c[u].s0lo, c[u].s0hi);
         scales_from_raw<FMT>(sc[g * 4 + 1], q, mx, c[u].s1lo, c[u].s1hi);
     }
@@ -242,15 +250,15 @@ __device__ __forceinline__ void dn_steps(const uint8_t* st0, const uint8_t* st1,
     _Pragma("unroll") for (int u = 0; u < U; ++u) {                                        \
         uint32_t fa[4];                                                                    \
         frag_a<I>(c[u], fa);                                                               \
-        mma_f16_16816(part[u * 2 + (I & 1)], fa[0], fa[1], fa[2], fa[3],                   \
+        mma_f16_16816(part[u][I & 1], fa[0], fa[1], fa[2], fa[3],                          \
                       word_of(hb[u][I >> 1], (I & 1) * 2), word_of(hb[u][I >> 1], (I & 1) * 2 + 1)); \
     }
     DEC_DN(0) DEC_DN(1) DEC_DN(2) DEC_DN(3) DEC_DN(4) DEC_DN(5) DEC_DN(6) DEC_DN(7)
 #undef DEC_DN
 }
 
-__device__ __forceinline__ float sum4(const float (&a)[4][4], int i) {
-    return (a[0][i] + a[1][i]) + (a[2][i] + a[3][i]);
+__device__ __forceinline__ float sum4(const float (&a)[2][2][4], int i) {
+    return (a[0][0][i] + a[0][1][i]) + (a[1][0][i] + a[1][1][i]);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -397,22 +405,35 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         R.w_out[tid] = S.w[tid];
     }
     dec_dispatch(T, k, E, L.I_shared, S.ids, S.w, D);
+    {
+        const int nsl = D.n_active + (L.I_shared > 0 ? 1 : 0);
+        for (int i = tid; i < nsl * 3; i += kDecThreads) {
+            const int slot = i / 3, pj = i - slot * 3;
+            const bool sh = slot == D.n_active;
+            const ProjView& PV = pj == 0 ? (sh ? L.sh_gate : L.gate)
+                                         : pj == 1 ? (sh ? L.sh_up : L.up) : (sh ? L.sh_down : L.down);
+            const int e = D.expert[slot];
+            D.post[slot][pj] = PV.post[e];
+            D.mxb[slot][pj] = PV.fmt == MOE_FMT_MXFP4 ? 112 + PV.mx_off[e] : 0;
+        }
+        __syncthreads();
+    }
 
     // ---- the work of this CTA and of this warp ----------------------------------------------------
-    // gate+up: tasks (slot, 16 rows) dealt round-robin to the CTAs; in each task warp w takes the
+    // gate+up: tasks (slot, 32 rows) dealt round-robin to the CTAs; in each task warp w takes the
     // K-steps w, w + 8, ..., so at any time the 8 warps read 512 contiguous bytes of every row.
     const int n_active = D.n_active;
     const bool has_shared = L.I_shared > 0;
-    const int tilesR = L.I / 16;
-    const int ntasks = n_active * tilesR + (has_shared ? L.I_shared / 16 : 0);
+    const int tilesR = L.I / 32;
+    const int ntasks = n_active * tilesR + (has_shared ? L.I_shared / 32 : 0);
     const int cnt_g = cta < ntasks ? (ntasks - cta + G - 1) / G : 0;
     const int ksteps_g = H / 128;
     const int n_g = ksteps_g > warp ? (ksteps_g - warp + kDecWarps - 1) / kDecWarps : 0;
-    const int done_g = n_g > 0 ? cnt_g * n_g : 0;  // gate+up steps of this warp
+    const int done_g = n_g > 0 ? cnt_g * n_g : 0;  // gate+up stages of this warp
     // down: 16-row output tiles dealt round-robin to the CTAs; the CTA's (tile, slot) pairs are
-    // dealt to its warps (warp w takes pairs w, w + 8, ...), each streams the whole K of a pair.
-    // Slots are visited in an order rotated by the CTA index so that the CTAs read different
-    // experts at any one time.
+    // dealt to its warps (warp w takes pairs w, w + 8, ...), each streams the whole K of a pair,
+    // two K-steps per stage.  Slots are visited in an order rotated by the CTA index so that
+    // the CTAs read different experts at any one time.
     const int nslots = n_active + (has_shared ? 1 : 0);
     const int npairs = cnt_d * nslots;
 
@@ -420,17 +441,17 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         const int tau = cta + j * G;
         if (tau < n_active * tilesR) {
             slot = tau / tilesR;
-            n0 = (tau - slot * tilesR) * 16;
+            n0 = (tau - slot * tilesR) * 32;
         } else {
             slot = n_active;
-            n0 = (tau - n_active * tilesR) * 16;
+            n0 = (tau - n_active * tilesR) * 32;
         }
     };
     auto pair_of = [&](int p, int& tl, int& slot) {  // pair p of this CTA -> (tile, slot)
         tl = p / nslots;
         slot = (p - tl * nslots + cta) % nslots;
     };
-    // activation chunk of a lane at K-step ks: x (task j) / h (slot)
+    // activation chunk of a lane: x (task j) / h (slot), at K-step 0
     auto x_src = [&](int j) -> const __half* {
         int slot, n0;
         task_of(j, slot, n0);
@@ -441,10 +462,10 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         const bool ok = (D.tokmask[slot] >> g) & 1u;  // MMA column g = token g
         return ok ? L.h16 + ((size_t)slot * kDecMaxT + g) * Imax + 32 * q : nullptr;
     };
-    auto copy_act = [&](uint32_t st, const __half* a) {  // 64 B of activations of this lane
+    auto copy_act = [&](uint32_t dst, const __half* a) {  // 64 B of activations of this lane
         if (a) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) cp_async16(st + kDecStageAct + c * 512 + lane * 16, a + 8 * c);
+            for (int c = 0; c < 4; ++c) cp_async16(dst + c * 512 + lane * 16, a + 8 * c);
         }
     };
 
@@ -452,14 +473,15 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
     uint8_t* ring = dsm + warp * kDecStages * kDecStageBytes;
     const uint32_t rbase = smem_addr(ring);
     int ic_phase = done_g > 0 ? 0 : 1;
-    // gate+up: task, K-step; down: pair, K-step within the pair
+    // gate+up: task, K-step; down: pair, first K-step of the stage
     int ic_j = ic_phase == 0 ? 0 : warp, ic_s = ic_phase == 0 ? warp : 0, ic_ns = 0;
     int ic_sfb = 8;
+    size_t ic_rs = 0;      // row stride of the scales (bytes)
     bool h_ready = false;  // h may be copied only after barrier 2
-    const uint8_t *ic_c0 = nullptr, *ic_c1 = nullptr, *ic_c2 = nullptr, *ic_c3 = nullptr;
-    const uint8_t* ic_sp = nullptr;
+    const uint8_t *ic_c0 = nullptr, *ic_c1 = nullptr, *ic_sp = nullptr;
+    size_t ic_rb = 0;      // row stride of the codes (bytes)
     const __half* ic_ap = nullptr;
-    auto ic_enter = [&]() {  // base pointers of the issue cursor's task / (slot, tile)
+    auto ic_enter = [&]() {  // base pointers of the issue cursor's task / pair
         if (ic_phase == 0) {
             int slot, n0;
             task_of(ic_j, slot, n0);
@@ -469,14 +491,13 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             const int N = sh ? L.I_shared : L.I;
             const int fmt = sh ? FS : FR;
             const size_t rowA = (size_t)D.expert[slot] * N + n0 + g;
-            const size_t rb = (size_t)(H / 2);
-            ic_c0 = PG.packed + rowA * rb + 16 * q;
-            ic_c1 = ic_c0 + 8 * rb;
-            ic_c2 = PU.packed + rowA * rb + 16 * q;
-            ic_c3 = ic_c2 + 8 * rb;
+            ic_rb = (size_t)(H / 2);
+            ic_c0 = PG.packed + rowA * ic_rb + 16 * q;
+            ic_c1 = PU.packed + rowA * ic_rb + 16 * q;
             ic_sfb = fmt == MOE_FMT_NVFP4 ? 8 : 4;
+            ic_rs = (size_t)(H / (fmt == MOE_FMT_NVFP4 ? 16 : 32));
             const ProjView& PS = (q >> 1) ? PU : PG;  // this lane stages (row g + 8 (q & 1), matrix q >> 1)
-            ic_sp = PS.scales + (rowA + 8 * (q & 1)) * (size_t)(H / (fmt == MOE_FMT_NVFP4 ? 16 : 32));
+            ic_sp = PS.scales + (rowA + 8 * (q & 1)) * ic_rs;
             ic_ap = x_src(ic_j);
         } else if (ic_phase == 1) {
             if (ic_j >= npairs) {
@@ -490,13 +511,18 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             const int K = sh ? L.I_shared : L.I;
             const int fmt = sh ? FS : FR;
             const size_t rowA = (size_t)D.expert[slot] * H + (size_t)(cta + tl * G) * 16 + g;
-            ic_c0 = PD.packed + rowA * (size_t)(K / 2) + 16 * q;
-            ic_c1 = ic_c0 + 8 * (size_t)(K / 2);
+            ic_rb = (size_t)(K / 2);
+            ic_c0 = PD.packed + rowA * ic_rb + 16 * q;
             ic_sfb = fmt == MOE_FMT_NVFP4 ? 8 : 4;
-            ic_sp = PD.scales + (rowA + 8 * (q & 1)) * (size_t)(K / (fmt == MOE_FMT_NVFP4 ? 16 : 32));
+            ic_rs = (size_t)(K / (fmt == MOE_FMT_NVFP4 ? 16 : 32));
+            ic_sp = PD.scales + (rowA + 8 * (q & 1)) * ic_rs;
             ic_ap = h_src(slot);
             ic_ns = K / 128;
         }
+    };
+    auto copy_scales = [&](uint32_t dst, const uint8_t* src) {
+        if (ic_sfb == 8) cp_async8(dst, src);
+        else cp_async4(dst, src);
     };
     ic_enter();
     int issued = 0;
@@ -504,13 +530,17 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         const uint32_t st = rbase + (issued % kDecStages) * kDecStageBytes;
         if (ic_phase == 0) {
             const int o = ic_s * 64;
-            cp_async16(st + 0 * 512 + lane * 16, ic_c0 + o);
-            cp_async16(st + 1 * 512 + lane * 16, ic_c1 + o);
-            cp_async16(st + 2 * 512 + lane * 16, ic_c2 + o);
-            cp_async16(st + 3 * 512 + lane * 16, ic_c3 + o);
-            if (ic_sfb == 8) cp_async8(st + kDecStageScales + lane * 8, ic_sp + ic_s * 8);
-            else cp_async4(st + kDecStageScales + lane * 8, ic_sp + ic_s * 4);
-            copy_act(st, ic_ap ? ic_ap + ic_s * 128 : nullptr);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const size_t ro = (size_t)(16 * t + 8 * r) * ic_rb + o;
+                    cp_async16(st + (4 * t + r) * 512 + lane * 16, ic_c0 + ro);
+                    cp_async16(st + (4 * t + 2 + r) * 512 + lane * 16, ic_c1 + ro);
+                }
+                copy_scales(st + kDecStageC + t * 256 + lane * 8, ic_sp + 16 * t * ic_rs + ic_s * ic_sfb);
+            }
+            copy_act(st + kDecStageB, ic_ap ? ic_ap + ic_s * 128 : nullptr);
             ic_s += kDecWarps;
             if (ic_s >= ksteps_g) {
                 ic_s = warp;
@@ -522,15 +552,16 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
                 ic_enter();
             }
         } else if (ic_phase == 1) {
-            const int o = ic_s * 64;
-            cp_async16(st + lane * 16, ic_c0 + o);
-            cp_async16(st + 512 + lane * 16, ic_c1 + o);
-            if (q < 2) {  // scales of row g + 8 q
-                if (ic_sfb == 8) cp_async8(st + kDecStageScales + lane * 8, ic_sp + ic_s * 8);
-                else cp_async4(st + kDecStageScales + lane * 8, ic_sp + ic_s * 4);
+            const int nst = ic_ns - ic_s < 2 ? 1 : 2;
+            for (int u = 0; u < nst; ++u) {
+                const int o = (ic_s + u) * 64;
+                cp_async16(st + kDecStageB + (2 * u) * 512 + lane * 16, ic_c0 + o);
+                cp_async16(st + kDecStageB + (2 * u + 1) * 512 + lane * 16, ic_c0 + 8 * ic_rb + o);
+                if (q < 2) copy_scales(st + kDecStageC + u * 256 + lane * 8, ic_sp + (ic_s + u) * ic_sfb);
+                if (h_ready) copy_act(st + u * 2048, ic_ap ? ic_ap + (ic_s + u) * 128 : nullptr);
             }
-            if (h_ready) copy_act(st, ic_ap ? ic_ap + ic_s * 128 : nullptr);
-            if (++ic_s == ic_ns) {
+            ic_s += 2;
+            if (ic_s >= ic_ns) {
                 ic_s = 0;
                 ic_j += kDecWarps;
                 ic_enter();
@@ -539,11 +570,8 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         cp_async_commit();
         ++issued;
     };
-    // ring invariant: before a warp consumes n (1 or 2) stages from position c, stages
-    // c .. c + S - 3 are issued; it issues n more (into the stages freed by c - 2 and c - 1)
-    // and waits until at most S - 2 groups are pending, so c .. c + n - 1 have landed.
 #pragma unroll 1
-    for (int i = 0; i < kDecStages - 2; ++i) issue_next();
+    for (int i = 0; i < kDecStages - 1; ++i) issue_next();
     int consumed = 0;
     auto stage_ptr = [&](int c) { return ring + (c % kDecStages) * kDecStageBytes; };
 
@@ -552,66 +580,58 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         int slot, n0;
         task_of(j, slot, n0);
         const bool sh = slot == n_active;
-        const int e = D.expert[slot];
-        const ProjView& PG = sh ? L.sh_gate : L.gate;
-        const ProjView& PU = sh ? L.sh_up : L.up;
         const int fmt = sh ? FS : FR;
-        const int mxg = fmt == MOE_FMT_MXFP4 ? 112 + PG.mx_off[e] : 0;
-        const int mxu = fmt == MOE_FMT_MXFP4 ? 112 + PU.mx_off[e] : 0;
+        const int mxg = D.mxb[slot][0], mxu = D.mxb[slot][1];
         const bool has_tok = nth_bit(D.tokmask[slot], g) >= 0;
-        float accG[4][4] = {}, accU[4][4] = {};
-        for (int s = 0; s < n_g; s += 2) {
-            const bool two = s + 1 < n_g;
+        float acc[2][2][2][4] = {};
+        for (int s = 0; s < n_g; ++s) {
             issue_next();
-            if (two) issue_next();
-            cp_async_wait<kDecStages - 2>();
+            cp_async_wait<kDecStages - 1>();
             __syncwarp();
-            const uint8_t *st0 = stage_ptr(consumed), *st1 = stage_ptr(consumed + 1);
-            if (fmt == MOE_FMT_NVFP4) {
-                if (two) gu_steps<MOE_FMT_NVFP4, 2>(st0, st1, has_tok, lane, g, q, mxg, mxu, accG, accU);
-                else gu_steps<MOE_FMT_NVFP4, 1>(st0, st1, has_tok, lane, g, q, mxg, mxu, accG, accU);
-            } else {
-                if (two) gu_steps<MOE_FMT_MXFP4, 2>(st0, st1, has_tok, lane, g, q, mxg, mxu, accG, accU);
-                else gu_steps<MOE_FMT_MXFP4, 1>(st0, st1, has_tok, lane, g, q, mxg, mxu, accG, accU);
-            }
-            consumed += two ? 2 : 1;
+            if (fmt == MOE_FMT_NVFP4) gu_stage<MOE_FMT_NVFP4>(stage_ptr(consumed), has_tok, lane, g, q, mxg, mxu, acc);
+            else gu_stage<MOE_FMT_MXFP4>(stage_ptr(consumed), has_tok, lane, g, q, mxg, mxu, acc);
+            ++consumed;
         }
         // K-split reduction, double-buffered: one CTA barrier per task
-        float* rg = red_g + (j & 1) * kDecWarps * 256;
+        float* rg = red_g + (j & 1) * kDecWarps * 512;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            rg[(warp * 8 + i) * 32 + lane] = sum4(accG, i);
-            rg[(warp * 8 + 4 + i) * 32 + lane] = sum4(accU, i);
-        }
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    rg[(warp * 16 + t * 8 + m * 4 + i) * 32 + lane] = acc[t][m][0][i] + acc[t][m][1][i];
         __syncthreads();
-        if (tid < 128) {
-            const int i = tid >> 5, ln = tid & 31;
+        {   // thread -> (tile, accumulator index, lane) of the MMA layout
+            const int t = tid >> 7, i = (tid >> 5) & 3, ln = tid & 31;
             float Gs = 0.f, Us = 0.f;
 #pragma unroll
             for (int w = 0; w < kDecWarps; ++w) {
-                Gs += rg[(w * 8 + i) * 32 + ln];
-                Us += rg[(w * 8 + 4 + i) * 32 + ln];
+                Gs += rg[(w * 16 + t * 8 + i) * 32 + ln];
+                Us += rg[(w * 16 + t * 8 + 4 + i) * 32 + ln];
             }
-            const int row = (ln >> 2) + 8 * (i >> 1), col = 2 * (ln & 3) + (i & 1);
-            const int t = nth_bit(D.tokmask[slot], col);  // column -> token
-            if (t >= 0) {
-                const float hv = silu_f32(Gs * PG.post[e]) * (Us * PU.post[e]);
-                L.h16[((size_t)slot * kDecMaxT + t) * Imax + n0 + row] = __float2half_rn(hv);
+            const int row = 16 * t + (ln >> 2) + 8 * (i >> 1), col = 2 * (ln & 3) + (i & 1);
+            const int tok = nth_bit(D.tokmask[slot], col);  // column -> token
+            if (tok >= 0) {
+                const float hv = silu_f32(Gs * D.post[slot][0]) * (Us * D.post[slot][1]);
+                L.h16[((size_t)slot * kDecMaxT + tok) * Imax + n0 + row] = __float2half_rn(hv);
             }
         }
     }
     grid_barrier(bar, L.status);  // every h is written (and red_g is no longer read)
 
     // ---- phase 3: down + weighted sum + shared expert ----------------------------------------------
-    // the h chunks of the down steps already in the ring, then every later stage copies its own
+    // the h chunks of the down stages already in the ring, then every later stage copies its own
     h_ready = true;
     for (int p = warp, idx = 0; p < npairs && done_g + idx < issued; p += kDecWarps) {
         int tl, slot;
         pair_of(p, tl, slot);
         const __half* a = h_src(slot);
         const int ns = (slot == n_active ? L.I_shared : L.I) / 128;
-        for (int s = 0; s < ns && done_g + idx < issued; ++s, ++idx)
-            copy_act(rbase + ((done_g + idx) % kDecStages) * kDecStageBytes, a ? a + s * 128 : nullptr);
+        for (int s = 0; s < ns && done_g + idx < issued; s += 2, ++idx) {
+            const uint32_t st = rbase + ((done_g + idx) % kDecStages) * kDecStageBytes;
+            for (int u = 0; u < 2 && s + u < ns; ++u) copy_act(st + u * 2048, a ? a + (s + u) * 128 : nullptr);
+        }
     }
     cp_async_commit();
     cp_async_wait<0>();
@@ -620,31 +640,28 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         int tl, slot;
         pair_of(p, tl, slot);
         const bool sh = slot == n_active;
-        const int e = D.expert[slot];
-        const ProjView& PD = sh ? L.sh_down : L.down;
         const int fmt = sh ? FS : FR;
-        const int mx = fmt == MOE_FMT_MXFP4 ? 112 + PD.mx_off[e] : 0;
+        const int mx = D.mxb[slot][2];
         const int ns = (sh ? L.I_shared : L.I) / 128;
         const bool has_tok = (D.tokmask[slot] >> g) & 1u;
-        float part[4][4] = {};
+        float part[2][2][4] = {};
         for (int s = 0; s < ns; s += 2) {
             const bool two = s + 1 < ns;
             issue_next();
-            if (two) issue_next();
-            cp_async_wait<kDecStages - 2>();
+            cp_async_wait<kDecStages - 1>();
             __syncwarp();
-            const uint8_t *st0 = stage_ptr(consumed), *st1 = stage_ptr(consumed + 1);
+            const uint8_t* st = stage_ptr(consumed);
             if (fmt == MOE_FMT_NVFP4) {
-                if (two) dn_steps<MOE_FMT_NVFP4, 2>(st0, st1, has_tok, lane, g, q, mx, part);
-                else dn_steps<MOE_FMT_NVFP4, 1>(st0, st1, has_tok, lane, g, q, mx, part);
+                if (two) dn_stage<MOE_FMT_NVFP4, 2>(st, has_tok, lane, g, q, mx, part);
+                else dn_stage<MOE_FMT_NVFP4, 1>(st, has_tok, lane, g, q, mx, part);
             } else {
-                if (two) dn_steps<MOE_FMT_MXFP4, 2>(st0, st1, has_tok, lane, g, q, mx, part);
-                else dn_steps<MOE_FMT_MXFP4, 1>(st0, st1, has_tok, lane, g, q, mx, part);
+                if (two) dn_stage<MOE_FMT_MXFP4, 2>(st, has_tok, lane, g, q, mx, part);
+                else dn_stage<MOE_FMT_MXFP4, 1>(st, has_tok, lane, g, q, mx, part);
             }
-            consumed += two ? 2 : 1;
+            ++consumed;
         }
         // expert done: fold in its post-scale and the token weights (MMA column = token)
-        const float post = PD.post[e];
+        const float post = D.post[slot][2];
         const float w0 = D.w[slot][2 * q] * post, w1 = D.w[slot][2 * q + 1] * post;
 #pragma unroll
         for (int t = 0; t < kDecMaxTilesPerCta; ++t) {
