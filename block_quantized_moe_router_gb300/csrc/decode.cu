@@ -292,9 +292,10 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         // router logits of experts e = cta, cta + G, ...: x (bf16) is staged in the idle ring,
         // each thread loads its router chunks of all these experts before any arithmetic
         const int chunks = H / 8;
-        uint4* xs_smem = reinterpret_cast<uint4*>(dsm);
+        const uint4* xs_smem = reinterpret_cast<const uint4*>(dsm);
         const uint4* xg = static_cast<const uint4*>(L.x);
-        for (int c = tid; c < T * chunks; c += kDecThreads) xs_smem[c] = ldg_cached128(xg + c);
+        for (int c = tid; c < T * chunks; c += kDecThreads) cp_async16(smem_addr(dsm + 16 * c), xg + c);
+        cp_async_commit();
         const uint4* wr = static_cast<const uint4*>(R.w_router);
         for (int e0 = cta; e0 < E; e0 += kDecRouterBatch * G) {
             uint4 wv[kDecRouterBatch][kDecRouterChunks];
@@ -306,6 +307,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
                     wv[b][m] = (e < E && c < chunks) ? ldg_stream128(wr + (size_t)e * chunks + c)
                                                      : make_uint4(0, 0, 0, 0);
                 }
+            cp_async_wait<0>();
             __syncthreads();  // x is staged
 #pragma unroll
             for (int b = 0; b < kDecRouterBatch; ++b) {

@@ -70,8 +70,10 @@ CONFIGS: Dict[str, MoeConfig] = {
                          scaling=2.5, I_shared=2048, act=ACT_NVFP4, zipf_s=1.1),
     "hash64": MoeConfig("hash64", T=64, H=4096, I=2048, E=64, k=6, scoring=SCORE_HASH,
                         I_shared=2048, fmt=FMT_MXFP4, shared_fmt=FMT_NVFP4, vocab=32000),
-    # a prefill-shaped case small enough (32 experts, ~0.9 GB of weights) for multi-pass
-    # profiler captures of the tensor-core kernels
+    # decode-shaped (8 tokens, dec8 shapes) and prefill-shaped cases small enough (32 experts,
+    # ~0.9 GB of weights) for multi-pass profiler captures
+    "dec8_e32": MoeConfig("dec8_e32", T=8, H=7168, I=2048, E=32, k=8, scoring=SCORE_SIGMOID,
+                          scaling=2.5, I_shared=2048),
     "pre1024_e32": MoeConfig("pre1024_e32", T=1024, H=7168, I=2048, E=32, k=8,
                              scoring=SCORE_SIGMOID, scaling=2.5, I_shared=2048, act=ACT_NVFP4),
 }
