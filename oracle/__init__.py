@@ -24,7 +24,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libmoe_oracle.so")
 _lib = None
 
-SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_HASH, SCORE_SQRTSOFTPLUS = 0, 1, 2, 3
+SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_HASH, SCORE_SQRTSOFTPLUS, SCORE_SOFTMAX_BIAS = 0, 1, 2, 3, 4
 FMT_NVFP4, FMT_MXFP4 = 0, 1
 
 
@@ -60,8 +60,8 @@ def _load():
     lib.orc_route.argtypes = [i32, i32, i32, i32, i32, i32, f64, vp, vp, vp, vp, vp, i64, vp,
                               vp, vp, vp, vp, vp, i32]
     lib.orc_route.restype = i32
-    lib.orc_moe_ffn.argtypes = [i32, i32, i32, i32, i32, _Proj, _Proj, _Proj, i32, _Proj, _Proj,
-                                _Proj, i32, f32, f32, vp, vp, vp, vp, i32]
+    lib.orc_moe_ffn.argtypes = [i32, i32, i32, i32, i32, i32, _Proj, _Proj, _Proj, i32, _Proj,
+                                _Proj, _Proj, i32, f32, f32, vp, vp, vp, vp, i32]
     lib.orc_moe_ffn.restype = i32
     lib.orc_hardware_threads.restype = i32
     _lib = lib
@@ -165,8 +165,9 @@ def _proj(p):
 
 
 def moe_ffn(*, T, E, H, I, k, gate, up, down, x_bf16, ids, w, sh_I=0, sh_gate=None, sh_up=None,
-            sh_down=None, act_mode=0, g1=1.0, g2=1.0, nthreads=0):
-    """Expert FFN for every (token, slot) pair + weighted sum + shared expert, fp64 [T,H]."""
+            sh_down=None, act_mode=0, g1=1.0, g2=1.0, zero_experts=0, nthreads=0):
+    """Expert FFN for every (token, slot) pair + weighted sum + shared expert, fp64 [T,H].
+    Ids in [E, E + zero_experts) are zero-computation experts (they add w * x)."""
     lib = _load()
     keep = []
     projs = []
@@ -178,7 +179,7 @@ def moe_ffn(*, T, E, H, I, k, gate, up, down, x_bf16, ids, w, sh_I=0, sh_gate=No
     ids = _as(ids, np.int32)
     w = _as(w, np.float64)
     out = np.zeros((T, H), np.float64)
-    rc = lib.orc_moe_ffn(T, E, H, I, k, projs[0], projs[1], projs[2], int(sh_I), projs[3],
+    rc = lib.orc_moe_ffn(T, E, H, I, k, int(zero_experts), projs[0], projs[1], projs[2], int(sh_I), projs[3],
                          projs[4], projs[5], int(act_mode), float(g1), float(g2), _ptr(x_bf16),
                          _ptr(ids), _ptr(w), _ptr(out), int(nthreads))
     if rc != 0:

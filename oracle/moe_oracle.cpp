@@ -12,7 +12,10 @@
 //     with a per-expert correction bias used for selection (moe/mod.rs, `correction_bias_dev`
 //     field doc), sqrt(softplus) scoring (moe/mod.rs, the `moe_topk_sqrtsoftplus` handles of
 //     the DeepSeek-V4 routing), static hash routing through a tid2eid [vocab, top_k] i64
-//     table (moe/init.rs, `new_with_hash` doc; moe/mod.rs, `tid2eid_dev` field doc).
+//     table (moe/init.rs, `new_with_hash` doc; moe/mod.rs, `tid2eid_dev` field doc), and
+//     softmax + bias routing over num_experts + zero_expert_num logits with zero-computation
+//     experts (moe/mod.rs, the LongCat `moe_topk_softmax_bias` / `moe_zero_expert_add` handles
+//     and the `router_logits_n` and `zero_accum_dev` field docs).
 //   * per expert: gate+up projection, SiLU(gate)*up, down projection, then the top-K weighted
 //     sum plus an optional shared expert (moe/mod.rs module doc: "gate+up, silu+down" and
 //     `moe_weighted_sum_blend`).
@@ -33,6 +36,10 @@
 //     renormalised over the selected set and multiplied by the routed scaling factor.
 //   - sqrt(softplus) routing is the sigmoid scheme with the score sqrt(log(1 + e^logit)).
 //   - hash routing weights are 1/top_k.
+//   - softmax + bias routing: p = softmax over all router logits; selection ranks p + bias;
+//     weights are p (renormalised over the selected set when asked) times the routed scaling.
+//   - a zero-computation expert (id in [E, E + Z)) returns its input: it adds w * x, the
+//     bf16 token itself, whatever the activation precision of the real experts.
 //   - the shared expert is added with weight 1.
 //   - Q: per 16 consecutive elements, s = E4M3_rne_satfinite(amax / 6 / g);
 //     code = E2M1_rne_satfinite(v / (e4m3(s) * g)); all-zero codes when s decodes to 0.
@@ -257,7 +264,8 @@ void orc_dequant(const uint8_t* packed, const uint8_t* scales, double global, in
 
 // ----- routing ------------------------------------------------------------------------------
 // scoring: 0 softmax, 1 sigmoid (+ correction bias for selection), 2 hash,
-// 3 sqrt(softplus) (+ correction bias for selection).
+// 3 sqrt(softplus) (+ correction bias for selection), 4 softmax (+ correction bias for
+// selection).  E here is the router width (real + zero-computation experts).
 // Inputs: either x_bf16 [T,H] + w_router_bf16 [E,H] (router GEMM) or logits_in f32 [T,E].
 // Outputs: logits_out [T,E] fp64 (may be null), ids [T,k], w [T,k] fp64, score_out [T,E]
 // fp64 selection score (may be null).  Returns 0, or -1 on an invalid argument.
@@ -271,7 +279,7 @@ int orc_route(int T, int E, int H, int k, int scoring, int renorm, double scalin
               double* logits_out, int32_t* ids, double* w, double* score_out, int32_t* status_out,
               int nthreads) {
     build_tables();
-    if (T < 0 || E <= 0 || k <= 0 || k > E || scoring < 0 || scoring > 3) return -1;
+    if (T < 0 || E <= 0 || k <= 0 || k > E || scoring < 0 || scoring > 4) return -1;
     std::vector<int32_t> tok_status(T, 0);
     if (scoring == 2) {
         for (int t = 0; t < T; ++t) {
@@ -311,10 +319,17 @@ int orc_route(int T, int E, int H, int k, int scoring, int renorm, double scalin
                 if (logits_out) logits_out[t * E + e] = l;
             }
             bool nonfinite = false;
+            double lmax = -INFINITY;
+            for (int e = 0; e < E; ++e)
+                if (std::isfinite(logit[e])) lmax = std::max(lmax, logit[e]);
+            double zall = 0.0;  // softmax denominator over every finite logit
+            for (int e = 0; e < E; ++e)
+                if (std::isfinite(logit[e])) zall += std::exp(logit[e] - lmax);
             for (int e = 0; e < E; ++e) {
                 double l = logit[e];
                 if (!std::isfinite(l)) { nonfinite = true; v[e] = -INFINITY; continue; }
                 if (scoring == 0) v[e] = l;  // softmax is monotone in the logit
+                else if (scoring == 4) v[e] = std::exp(l - lmax) / zall + (bias ? (double)bias[e] : 0.0);
                 else v[e] = gate_score(scoring, l) + (bias ? (double)bias[e] : 0.0);
             }
             if (nonfinite) tok_status[t] |= 4;
@@ -327,14 +342,8 @@ int orc_route(int T, int E, int H, int k, int scoring, int renorm, double scalin
                 if (v[a] != v[b]) return v[a] > v[b];
                 return a < b;
             });
-            double lmax = -INFINITY;
-            for (int e = 0; e < E; ++e)
-                if (std::isfinite(logit[e])) lmax = std::max(lmax, logit[e]);
-            if (scoring == 0) {
+            if (scoring == 0 || scoring == 4) {
                 // softmax over all E, then the selected subset (optionally renormalised)
-                double zall = 0.0;
-                for (int e = 0; e < E; ++e)
-                    if (std::isfinite(logit[e])) zall += std::exp(logit[e] - lmax);
                 double zsel = 0.0;
                 for (int j = 0; j < k; ++j) {
                     double l = logit[order[j]];
@@ -374,7 +383,8 @@ int orc_route(int T, int E, int H, int k, int scoring, int renorm, double scalin
 // globals [E] (NVFP4) or null (MXFP4).  gate/up: N = I, K = H.  down: N = H, K = I.
 // The shared expert (if sh_I > 0) has the same layout with one expert and intermediate sh_I.
 // act_mode: 0 = bf16 activations (A16), 1 = NVFP4 activations (A4) with globals g1 (for x)
-// and g2 (for h).  ids [T,k] (id -1 = dropped pair), w [T,k] fp64.  out [T,H] fp64.
+// and g2 (for h).  ids [T,k] (id -1 = dropped pair; E <= id < E + Z a zero-computation expert
+// that adds w * x), w [T,k] fp64.  out [T,H] fp64.
 struct OrcProj {
     const uint8_t* packed;
     const uint8_t* scales;
@@ -382,14 +392,14 @@ struct OrcProj {
     int fmt;
 };
 
-int orc_moe_ffn(int T, int E, int H, int I, int k,
+int orc_moe_ffn(int T, int E, int H, int I, int k, int Z,
                 OrcProj gate, OrcProj up, OrcProj down,
                 int sh_I, OrcProj sh_gate, OrcProj sh_up, OrcProj sh_down,
                 int act_mode, float g1, float g2,
                 const uint16_t* x_bf16, const int32_t* ids, const double* w,
                 double* out, int nthreads) {
     build_tables();
-    if (T < 0 || E <= 0 || H % 32 || I % 32 || (sh_I % 32)) return -1;
+    if (T < 0 || E <= 0 || Z < 0 || H % 32 || I % 32 || (sh_I % 32)) return -1;
     auto sv = [](int fmt) { return fmt == 0 ? 16 : 32; };
     auto expert_mat = [&](const OrcProj& p, int e, int64_t N, int64_t K) {
         QMat m;
@@ -428,8 +438,12 @@ int orc_moe_ffn(int T, int E, int H, int I, int k,
         for (int h = 0; h < H; ++h) o[h] = 0.0;
         for (int j = 0; j < k; ++j) {
             int e = ids[t * k + j];
-            if (e < 0 || e >= E) continue;
             double wj = w[t * k + j];
+            if (e >= E && e < E + Z) {  // zero-computation expert: the input itself
+                for (int h = 0; h < H; ++h) o[h] += wj * bf16_to_double(x_bf16[t * (int64_t)H + h]);
+                continue;
+            }
+            if (e < 0 || e >= E) continue;
             ffn(expert_mat(gate, e, I, H), expert_mat(up, e, I, H), expert_mat(down, e, H, I),
                 a.data(), I, y.data(), rowbuf);
             for (int h = 0; h < H; ++h) o[h] += wj * y[h];

@@ -134,3 +134,40 @@ def test_linearity_in_routing_weight(orc):
     single[0, 1] = r["w"][0, 1]
     c = _oracle_ffn(orc, cfg, inp, r["ids"], single)
     assert np.allclose(b - a, 2.0 * c, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("act_mode", [0, 1])
+def test_zero_computation_experts_add_the_input(orc, act_mode):
+    """Ids in [E, E + Z) are zero-computation experts (moe/mod.rs, the `moe_zero_expert_add`
+    handle and `zero_accum_dev` field doc): each adds w * x, x the bf16 token."""
+    cfg = synth.CONFIGS["tiny"]
+    inp = synth.make_inputs(cfg, seed=4)
+    rng = np.random.default_rng(9)
+    Z = 3
+    ids = np.stack([rng.permutation(cfg.E + Z)[:cfg.k] for _ in range(cfg.T)]).astype(np.int32)
+    ids[0] = [cfg.E, cfg.E + 2]          # a token routed to zero experts only
+    ids[1, 0] = 1                        # and one with a real expert first
+    w = rng.uniform(0.1, 1.0, (cfg.T, cfg.k))
+    got = orc.moe_ffn(T=cfg.T, E=cfg.E, H=cfg.H, I=cfg.I, k=cfg.k, gate=_np(inp, "gate"),
+                      up=_np(inp, "up"), down=_np(inp, "down"), x_bf16=synth.bf16_bits(inp["x"]),
+                      ids=ids, w=w, sh_I=cfg.I_shared, sh_gate=_np(inp, "sh_gate"),
+                      sh_up=_np(inp, "sh_up"), sh_down=_np(inp, "sh_down"), act_mode=act_mode,
+                      zero_experts=Z)
+    real = np.where(ids < cfg.E, ids, -1)
+    want = _dense_mixture(orc, cfg, inp, real, w, act_mode=act_mode)
+    x = inp["x"].float().double().numpy()
+    zw = np.where(ids >= cfg.E, w, 0.0).sum(1, keepdims=True)
+    want += zw * x
+    assert np.allclose(got, want, rtol=1e-9, atol=1e-12)
+    # ids at or beyond E + Z are still dropped
+    ids2 = ids.copy()
+    ids2[2, 0] = cfg.E + Z
+    got2 = orc.moe_ffn(T=cfg.T, E=cfg.E, H=cfg.H, I=cfg.I, k=cfg.k, gate=_np(inp, "gate"),
+                       up=_np(inp, "up"), down=_np(inp, "down"), x_bf16=synth.bf16_bits(inp["x"]),
+                       ids=ids2, w=w, sh_I=cfg.I_shared, sh_gate=_np(inp, "sh_gate"),
+                       sh_up=_np(inp, "sh_up"), sh_down=_np(inp, "sh_down"), act_mode=act_mode,
+                       zero_experts=Z)
+    real2 = np.where(ids2 < cfg.E, ids2, -1)
+    zw2 = np.where((ids2 >= cfg.E) & (ids2 < cfg.E + Z), w, 0.0).sum(1, keepdims=True)
+    want2 = _dense_mixture(orc, cfg, inp, real2, w, act_mode=act_mode) + zw2 * x
+    assert np.allclose(got2, want2, rtol=1e-9, atol=1e-12)

@@ -3,7 +3,8 @@
 Routing kinds of the spark_model MoE pages: softmax top-K (moe/init.rs `moe_topk_softmax`
 handles), sigmoid scoring with a correction bias used for selection only (moe/mod.rs
 `correction_bias_dev` field doc), static hash routing through tid2eid (moe/init.rs
-`new_with_hash` doc).  Checked against brute force over every k-subset, closed forms and the
+`new_with_hash` doc), softmax + bias routing over the real and zero-computation experts
+(moe/mod.rs, `moe_topk_softmax_bias` handles, `router_logits_n` field doc).  Checked against brute force over every k-subset, closed forms and the
 weight-sum invariant.
 """
 import itertools
@@ -37,10 +38,13 @@ def _score(scoring, l):
         return l
     if scoring == 1:
         return 1 / (1 + np.exp(-l))
+    if scoring == 4:
+        p = np.exp(l - l.max())
+        return p / p.sum()                  # softmax probability (the bias is added on top)
     return np.sqrt(np.log1p(np.exp(l)))   # sqrt(softplus)
 
 
-@pytest.mark.parametrize("scoring", [0, 1, 3])
+@pytest.mark.parametrize("scoring", [0, 1, 3, 4])
 @pytest.mark.parametrize("E,k", [(6, 2), (8, 3), (10, 4), (5, 5)])
 def test_topk_matches_brute_force(orc, scoring, E, k):
     rng = np.random.default_rng(E * 10 + k + scoring)
@@ -118,7 +122,27 @@ def test_sqrt_softplus_special_values(orc):
     assert np.array_equal(a["ids"], b["ids"])
 
 
-@pytest.mark.parametrize("scoring,scaling", [(0, 1.0), (1, 2.5), (3, 1.0)])
+def test_softmax_bias_selects_but_does_not_weight(orc):
+    # p = softmax([2, 1, 0, -1]) = .6439, .2369, .0871, .0321; + bias (0, 0, .6, 0) moves
+    # expert 2 (.6871) above expert 1 (.2369): top-2 = [2, 0], weighted by p alone
+    logits = np.array([[2.0, 1.0, 0.0, -1.0]], np.float32)
+    bias = np.array([0.0, 0.0, 0.6, 0.0], np.float32)
+    e = [math.exp(v) for v in (2.0, 1.0, 0.0, -1.0)]
+    p = [v / sum(e) for v in e]
+    r = orc.route(T=1, E=4, k=2, scoring=4, renorm=True, scaling=1.5, logits_in=logits, bias=bias)
+    assert list(r["ids"][0]) == [2, 0]
+    assert np.allclose(r["w"][0], [p[2] / (p[0] + p[2]) * 1.5, p[0] / (p[0] + p[2]) * 1.5],
+                       rtol=0, atol=1e-12)
+    r_nr = orc.route(T=1, E=4, k=2, scoring=4, renorm=False, scaling=1.0, logits_in=logits,
+                     bias=bias)
+    assert np.allclose(r_nr["w"][0], [p[2], p[0]], rtol=0, atol=1e-12)
+    # with no bias it is plain softmax top-K
+    r0 = orc.route(T=1, E=4, k=2, scoring=4, renorm=False, logits_in=logits)
+    r1 = orc.route(T=1, E=4, k=2, scoring=0, renorm=False, logits_in=logits)
+    assert np.array_equal(r0["ids"], r1["ids"]) and np.allclose(r0["w"], r1["w"], rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("scoring,scaling", [(0, 1.0), (1, 2.5), (3, 1.0), (4, 1.5)])
 def test_weight_sum_invariant(orc, scoring, scaling):
     rng = np.random.default_rng(11)
     T, E, k = 64, 256, 8
