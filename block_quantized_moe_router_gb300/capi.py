@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = range(5)
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_TOKEN_ID, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT = 1, 2, 4, 8
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID, MOE_SCORE_HASH, MOE_SCORE_SQRTSOFTPLUS = 0, 1, 2, 3
+MOE_SCORE_SOFTMAX_BIAS = 4
 MOE_FMT_NVFP4, MOE_FMT_MXFP4 = 0, 1
 MOE_ACT_BF16, MOE_ACT_NVFP4 = 0, 1
 
@@ -43,7 +44,8 @@ class moe_ffn_desc(ctypes.Structure):
     _fields_ = [("E", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("I_shared", ctypes.c_int32),
                 ("gate", moe_qtensor), ("up", moe_qtensor), ("down", moe_qtensor),
-                ("sh_gate", moe_qtensor), ("sh_up", moe_qtensor), ("sh_down", moe_qtensor)]
+                ("sh_gate", moe_qtensor), ("sh_up", moe_qtensor), ("sh_down", moe_qtensor),
+                ("zero_experts", ctypes.c_int32)]
 
 
 class moe_route_desc(ctypes.Structure):
@@ -52,7 +54,7 @@ class moe_route_desc(ctypes.Structure):
                 ("renormalize", ctypes.c_int32), ("routed_scaling", ctypes.c_float),
                 ("w_router", ctypes.c_void_p), ("correction_bias", ctypes.c_void_p),
                 ("tid2eid", ctypes.c_void_p), ("vocab", ctypes.c_int64),
-                ("token_ids", ctypes.c_void_p)]
+                ("token_ids", ctypes.c_void_p), ("zero_experts", ctypes.c_int32)]
 
 
 _lib = None
@@ -129,28 +131,30 @@ def qtensor(p: Optional[dict]) -> moe_qtensor:
                        _dptr(p.get("globals"), torch.float32, "globals"), int(p["fmt"]))
 
 
-def ffn_desc(E, H, I, top_k, I_shared, gate, up, down, sh_gate=None, sh_up=None, sh_down=None):
+def ffn_desc(E, H, I, top_k, I_shared, gate, up, down, sh_gate=None, sh_up=None, sh_down=None,
+             zero_experts=0):
     return moe_ffn_desc(E, H, I, top_k, I_shared, qtensor(gate), qtensor(up), qtensor(down),
-                        qtensor(sh_gate), qtensor(sh_up), qtensor(sh_down))
+                        qtensor(sh_gate), qtensor(sh_up), qtensor(sh_down), int(zero_experts))
 
 
 def route_desc(*, T, E, H, top_k, scoring, renormalize, routed_scaling, w_router=None,
-               correction_bias=None, tid2eid=None, vocab=0, token_ids=None) -> moe_route_desc:
+               correction_bias=None, tid2eid=None, vocab=0, token_ids=None,
+               zero_experts=0) -> moe_route_desc:
     return moe_route_desc(int(T), int(E), int(H), int(top_k), int(scoring), int(bool(renormalize)),
                           float(routed_scaling), _dptr(w_router, torch.bfloat16, "w_router"),
                           _dptr(correction_bias, torch.float32, "correction_bias"),
                           _dptr(tid2eid, torch.int64, "tid2eid"), int(vocab),
-                          _dptr(token_ids, torch.int32, "token_ids"))
+                          _dptr(token_ids, torch.int32, "token_ids"), int(zero_experts))
 
 
 def moe_route(*, T, E, H, top_k, scoring, renormalize, routed_scaling, x=None, w_router=None,
               logits_in=None, logits_out=None, correction_bias=None, tid2eid=None, vocab=0,
-              token_ids=None, topk_ids, topk_w, dev_status=None, stream=None):
+              token_ids=None, topk_ids, topk_w, dev_status=None, stream=None, zero_experts=0):
     lib = load_library()
     d = route_desc(T=T, E=E, H=H, top_k=top_k, scoring=scoring, renormalize=renormalize,
                    routed_scaling=routed_scaling, w_router=w_router,
                    correction_bias=correction_bias, tid2eid=tid2eid, vocab=vocab,
-                   token_ids=token_ids)
+                   token_ids=token_ids, zero_experts=zero_experts)
     st = lib.moe_route(ctypes.byref(d), _dptr(x, torch.bfloat16, "x"),
                        _dptr(logits_in, torch.float32, "logits_in"),
                        _dptr(logits_out, torch.float32, "logits_out"),

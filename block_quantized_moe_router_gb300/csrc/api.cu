@@ -87,8 +87,10 @@ void free_proj(PreparedProj& p) {
 
 moe_status_t validate_ffn_desc(const moe_ffn_desc* d) {
     if (!d) return MOE_ERR_INVALID_ARG;
-    if (d->E < 1 || d->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
-    if (d->top_k < 1 || d->top_k > d->E || d->top_k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+    if (d->E < 1 || d->zero_experts < 0 || d->E + d->zero_experts > kMaxExperts)
+        return MOE_ERR_INVALID_ARG;
+    if (d->top_k < 1 || d->top_k > d->E + d->zero_experts || d->top_k > kMaxTopK)
+        return MOE_ERR_INVALID_ARG;
     if (d->H < 128 || d->H % 128 || d->I < 128 || d->I % 128) return MOE_ERR_INVALID_ARG;
     if (d->I_shared < 0 || d->I_shared % 128) return MOE_ERR_INVALID_ARG;
     if (!valid_qtensor(d->gate) || !valid_qtensor(d->up) || !valid_qtensor(d->down))
@@ -105,11 +107,14 @@ moe_status_t validate_ffn_desc(const moe_ffn_desc* d) {
 
 moe_status_t validate_route(const moe_route_desc* d, const float* logits_in) {
     if (!d) return MOE_ERR_INVALID_ARG;
-    if (d->T < 0 || d->E < 1 || d->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
-    if (d->top_k < 1 || d->top_k > d->E || d->top_k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->E < 1 || d->zero_experts < 0 || d->E + d->zero_experts > kMaxExperts)
+        return MOE_ERR_INVALID_ARG;
+    if (d->top_k < 1 || d->top_k > d->E + d->zero_experts || d->top_k > kMaxTopK)
+        return MOE_ERR_INVALID_ARG;
     if (!std::isfinite(d->routed_scaling)) return MOE_ERR_INVALID_ARG;
     if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID &&
-        d->scoring != MOE_SCORE_HASH && d->scoring != MOE_SCORE_SQRTSOFTPLUS)
+        d->scoring != MOE_SCORE_HASH && d->scoring != MOE_SCORE_SQRTSOFTPLUS &&
+        d->scoring != MOE_SCORE_SOFTMAX_BIAS)
         return MOE_ERR_INVALID_ARG;
     if (d->scoring == MOE_SCORE_HASH && d->vocab < 1) return MOE_ERR_INVALID_ARG;
     if (d->scoring != MOE_SCORE_HASH && !logits_in && (d->H < 32 || d->H % 32))
@@ -124,6 +129,7 @@ FfnLaunch make_launch(const Handle* h, int T, int act, float g1, float g2, int p
     const moe_ffn_desc& d = h->desc;
     FfnLaunch L{};
     L.T = T; L.E = d.E; L.H = d.H; L.I = d.I; L.k = d.top_k; L.I_shared = d.I_shared;
+    L.Z = d.zero_experts;
     L.act = act; L.path = path; L.g1 = g1; L.g2 = g2;
     L.x = x; L.ids = ids; L.w = w; L.out = out; L.status = status;
     L.gate = h->gate.view; L.up = h->up.view; L.down = h->down.view;
@@ -176,22 +182,23 @@ moe_status_t moe_route(const moe_route_desc* d, const void* x_bf16, const float*
     if (d->T == 0) return MOE_OK;
     if (!topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int Er = d->E + d->zero_experts;  // router outputs: real then zero-computation experts
     if (d->scoring == MOE_SCORE_HASH) {
         if (!d->tid2eid || !d->token_ids) return MOE_ERR_INVALID_ARG;
-        return launch_hash_route(d->tid2eid, d->token_ids, d->vocab, d->T, d->E, d->top_k,
+        return launch_hash_route(d->tid2eid, d->token_ids, d->vocab, d->T, Er, d->top_k,
                                  d->routed_scaling, topk_ids, topk_w, dev_status, st) == cudaSuccess
                    ? MOE_OK : MOE_ERR_CUDA;
     }
     const float* logits = logits_in;
     if (!logits) {
         if (!d->w_router || !x_bf16 || !logits_out) return MOE_ERR_INVALID_ARG;
-        if (launch_router_logits(x_bf16, d->w_router, logits_out, d->T, d->E, d->H, st) !=
+        if (launch_router_logits(x_bf16, d->w_router, logits_out, d->T, Er, d->H, st) !=
             cudaSuccess)
             return MOE_ERR_CUDA;
         logits = logits_out;
     }
     const float* bias = d->scoring != MOE_SCORE_SOFTMAX ? d->correction_bias : nullptr;
-    return launch_topk(logits, bias, d->T, d->E, d->top_k, d->scoring, d->renormalize ? 1 : 0,
+    return launch_topk(logits, bias, d->T, Er, d->top_k, d->scoring, d->renormalize ? 1 : 0,
                        d->routed_scaling, topk_ids, topk_w, dev_status, st) == cudaSuccess
                ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -320,7 +327,8 @@ moe_status_t moe_forward(const void* handle, const moe_route_desc* rd, int32_t a
     const moe_status_t v = validate_route(rd, logits_in);
     if (v != MOE_OK) return v;
     const moe_ffn_desc& d = h->desc;
-    if (rd->E != d.E || rd->top_k != d.top_k || rd->H != d.H) return MOE_ERR_INVALID_ARG;
+    if (rd->E != d.E || rd->top_k != d.top_k || rd->H != d.H || rd->zero_experts != d.zero_experts)
+        return MOE_ERR_INVALID_ARG;
     if (act != MOE_ACT_BF16 && act != MOE_ACT_NVFP4) return MOE_ERR_INVALID_ARG;
     if (act == MOE_ACT_NVFP4 && (!pow2_positive(g_act1) || !pow2_positive(g_act2)))
         return MOE_ERR_INVALID_ARG;

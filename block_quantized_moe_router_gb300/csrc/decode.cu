@@ -78,6 +78,7 @@ struct DecShared {
     DecDispatch D;
     int32_t ids[64];
     float w[64];
+    float zw[kDecMaxT];  // per token: summed weight of its zero-computation experts
     float red_router[4][kDecWarps][kDecMaxT];
 };
 
@@ -271,6 +272,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
     const int G = gridDim.x, cta = blockIdx.x;
     const int T = L.T, H = L.H, E = L.E, k = L.k;
+    const int Er = L.E + L.Z;  // router outputs: real experts, then zero-computation experts
     const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
     const int tiles_out = H / 16;
     const int cnt_d = cta < tiles_out ? (tiles_out - cta + G - 1) / G : 0;
@@ -288,7 +290,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
                                bf16x2_to_f16x2(v.w));
         }
     }
-    if (R.mode == DEC_ROUTE_ROUTER && cta < E) {
+    if (R.mode == DEC_ROUTE_ROUTER && cta < Er) {
         // router logits of experts e = cta, cta + G, ...: x (bf16) is staged in the idle ring,
         // each thread loads its router chunks of all these experts before any arithmetic
         const int chunks = H / 8;
@@ -297,14 +299,14 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         for (int c = tid; c < T * chunks; c += kDecThreads) cp_async16(smem_addr(dsm + 16 * c), xg + c);
         cp_async_commit();
         const uint4* wr = static_cast<const uint4*>(R.w_router);
-        for (int e0 = cta; e0 < E; e0 += kDecRouterBatch * G) {
+        for (int e0 = cta; e0 < Er; e0 += kDecRouterBatch * G) {
             uint4 wv[kDecRouterBatch][kDecRouterChunks];
 #pragma unroll
             for (int b = 0; b < kDecRouterBatch; ++b)
 #pragma unroll
                 for (int m = 0; m < kDecRouterChunks; ++m) {
                     const int e = e0 + b * G, c = tid + m * kDecThreads;
-                    wv[b][m] = (e < E && c < chunks) ? ldg_stream128(wr + (size_t)e * chunks + c)
+                    wv[b][m] = (e < Er && c < chunks) ? ldg_stream128(wr + (size_t)e * chunks + c)
                                                      : make_uint4(0, 0, 0, 0);
                 }
             cp_async_wait<0>();
@@ -342,11 +344,11 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             __syncthreads();
             if (tid < kDecRouterBatch * kDecMaxT) {
                 const int b = tid / kDecMaxT, t = tid - b * kDecMaxT, e = e0 + b * G;
-                if (t < T && e < E) {
+                if (t < T && e < Er) {
                     float s = 0.f;
 #pragma unroll
                     for (int w = 0; w < kDecWarps; ++w) s += S.red_router[b][w][t];
-                    R.logits_out[(size_t)t * E + e] = s;
+                    R.logits_out[(size_t)t * Er + e] = s;
                 }
             }
         }
@@ -358,19 +360,19 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
     if (R.mode == DEC_ROUTE_ROUTER || R.mode == DEC_ROUTE_LOGITS) {
         if (warp < T) {
             const bool in_launch = R.mode == DEC_ROUTE_ROUTER;
-            const float* row = (in_launch ? R.logits_out : R.logits_in) + (size_t)warp * E;
+            const float* row = (in_launch ? R.logits_out : R.logits_in) + (size_t)warp * Er;
             int my_e;
             float my_w;
             auto load = [&](int e) { return in_launch ? ld_cg_f32(row + e) : row[e]; };
             bool nonfinite;
-            if (E <= 64)
-                nonfinite = warp_topk<2>(load, R.bias, E, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
-            else if (E <= 128)
-                nonfinite = warp_topk<4>(load, R.bias, E, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
-            else if (E <= 256)
-                nonfinite = warp_topk<8>(load, R.bias, E, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
+            if (Er <= 64)
+                nonfinite = warp_topk<2>(load, R.bias, Er, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
+            else if (Er <= 128)
+                nonfinite = warp_topk<4>(load, R.bias, Er, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
+            else if (Er <= 256)
+                nonfinite = warp_topk<8>(load, R.bias, Er, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
             else
-                nonfinite = warp_topk<16>(load, R.bias, E, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
+                nonfinite = warp_topk<16>(load, R.bias, Er, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
             if (nonfinite && lane == 0 && cta == 0) status_or(L.status, MOE_DEV_NONFINITE);
             if (lane < k) {
                 S.ids[warp * k + lane] = my_e;
@@ -387,7 +389,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
                 if (cta == 0) status_or(L.status, MOE_DEV_BAD_TOKEN_ID);
             } else {
                 const int64_t te = R.tid2eid[tok * k + j];
-                if (te < 0 || te >= E) {
+                if (te < 0 || te >= Er) {
                     if (cta == 0) status_or(L.status, MOE_DEV_BAD_EXPERT_ID);
                 } else {
                     e = (int32_t)te;
@@ -407,6 +409,14 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         R.w_out[tid] = S.w[tid];
     }
     dec_dispatch(T, k, E, L.I_shared, S.ids, S.w, D);
+    if (tid < kDecMaxT) {  // zero-computation experts: their weights fold into one per token
+        float z = 0.f;
+        for (int j = 0; tid < T && j < k; ++j) {
+            const int e = S.ids[tid * k + j];
+            if (e >= E && e < Er) z += S.w[tid * k + j];
+        }
+        S.zw[tid] = z;
+    }
     {
         const int nsl = D.n_active + (L.I_shared > 0 ? 1 : 0);
         for (int i = tid; i < nsl * 3; i += kDecThreads) {
@@ -690,7 +700,12 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
 #pragma unroll
         for (int w = 0; w < kDecWarps; ++w) sum += red_d[(tl * kDecWarps + w) * 128 + r];
         const int row = (ln >> 2) + 8 * (i >> 1), col = 2 * (ln & 3) + (i & 1);
-        if (col < T) out[(size_t)col * H + (size_t)(cta + tl * G) * 16 + row] = __float2bfloat16_rn(sum);
+        if (col < T) {
+            const size_t o = (size_t)col * H + (size_t)(cta + tl * G) * 16 + row;
+            if (S.zw[col] != 0.f)  // zero-computation experts return the token itself
+                sum += S.zw[col] * __bfloat162float(static_cast<const __nv_bfloat16*>(L.x)[o]);
+            out[o] = __float2bfloat16_rn(sum);
+        }
     }
 }
 

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(512) prep_kernel(FfnLaunch L) {
         for (int p = tid; p < P; p += blockDim.x) {
             const int e = L.ids[p];
             if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
-            else if (e != -1) bad = 1;
+            else if (e != -1 && !(e >= E && e < E + L.Z)) bad = 1;  // zero-computation experts are valid
         }
         if (bad) status_or(L.status, MOE_DEV_BAD_EXPERT_ID);
         __syncthreads();
@@ -285,7 +285,8 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots) {
 }
 
 // ------------------------------------------------------------------------------------------
-// Combine: out[t] = sum_j y[pos(t,j)] + y[shared row t], fixed j order, bf16 output.
+// Combine: out[t] = sum_j y[pos(t,j)] + y[shared row t] + (folded weight of the
+// zero-computation experts) * x[t], fixed j order, bf16 output.
 // ------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) combine_kernel(FfnLaunch L) {
     const int H8 = L.H / 8;
@@ -299,11 +300,24 @@ __global__ void __launch_bounds__(256) combine_kernel(FfnLaunch L) {
         acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
         acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
     };
+    float zw = 0.f;
     for (int j = 0; j < L.k; ++j) {
         const int pos = L.pos_of_pair[t * L.k + j];
         if (pos >= 0) add_row(pos);
+        const int e = L.ids[t * L.k + j];
+        if (e >= L.E && e < L.E + L.Z) zw += L.w[t * L.k + j];
     }
     if (L.I_shared > 0) add_row(L.T * L.k + t);
+    if (zw != 0.f) {
+        const uint4 v = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(L.x) +
+                                                         (size_t)t * L.H + c * 8);
+        const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += zw * __uint_as_float(xw[i] << 16);
+            acc[2 * i + 1] += zw * __uint_as_float(xw[i] & 0xFFFF0000u);
+        }
+    }
     uint4 o;
     __nv_bfloat162 v;
     v = __floats2bfloat162_rn(acc[0], acc[1]); o.x = *reinterpret_cast<uint32_t*>(&v);

@@ -32,6 +32,7 @@ struct ProjView {
 
 struct FfnLaunch {
     int T, E, H, I, k, I_shared, act, path;
+    int Z;                  // zero-computation experts: ids E .. E + Z - 1 add w * x
     float g1, g2;
     const void* x;          // bf16 [T][H]
     const int32_t* ids;     // [T][k]
@@ -81,7 +82,7 @@ struct TcBuffers {  // workspace views
 };
 struct TcPrepArgs {
     const int32_t* ids;
-    int T, k, E, H, I, I_shared, has_shared;
+    int T, k, E, Z, H, I, I_shared, has_shared;
     int32_t* status;
     int32_t *meta, *mblock_expert, *padrow_pair;
     int4 *tiles1, *tiles2;
@@ -117,8 +118,10 @@ struct TcGemmParams {
 struct TcCombineArgs {
     const __nv_bfloat16* y;
     const int32_t* ids;
+    const float* w;         // routing weights (zero-computation experts add w * x)
+    const void* x;          // bf16 [T][H]
     void* out;
-    int T, H, k, E, has_shared;
+    int T, H, k, E, Z, has_shared;
 };
 
 bool tc_supported(int E, int H, int I, int I_shared, int fmt_routed, int fmt_shared);

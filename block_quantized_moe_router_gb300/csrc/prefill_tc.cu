@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(1024) tc_prep_kernel(TcPrepArgs a) {
     for (int p = tid; p < P; p += blockDim.x) {
         const int e = a.ids[p];
         if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-        else if (e != -1) bad = 1;
+        else if (e != -1 && !(e >= E && e < E + a.Z)) bad = 1;  // zero-computation experts are valid
     }
     if (bad) status_or(a.status, MOE_DEV_BAD_EXPERT_ID);
     __syncthreads();
@@ -458,11 +458,23 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(TcCombineArgs a) {
             acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
         }
     };
+    float zw = 0.f;  // folded weight of the zero-computation experts
     for (int j = 0; j < a.k; ++j) {
         const int e = a.ids[t * a.k + j];
         if (e >= 0 && e < a.E) add(t * a.k + j);
+        else if (e >= a.E && e < a.E + a.Z) zw += a.w[t * a.k + j];
     }
     if (a.has_shared) add(a.T * a.k + t);
+    if (zw != 0.f) {
+        const uint4 v = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
+                                                         (size_t)t * a.H + c * 8);
+        const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += zw * __uint_as_float(xw[i] << 16);
+            acc[2 * i + 1] += zw * __uint_as_float(xw[i] & 0xFFFF0000u);
+        }
+    }
     uint4 o;
     uint32_t* ow = &o.x;
 #pragma unroll
@@ -619,7 +631,7 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
     if (ev && (err = record_phase_event(ev->end[i], st)) != cudaSuccess) return err;
 
     TcPrepArgs pa{};
-    pa.ids = L.ids; pa.T = L.T; pa.k = L.k; pa.E = L.E; pa.H = L.H; pa.I = L.I;
+    pa.ids = L.ids; pa.T = L.T; pa.k = L.k; pa.E = L.E; pa.Z = L.Z; pa.H = L.H; pa.I = L.I;
     pa.I_shared = L.I_shared; pa.has_shared = L.I_shared > 0; pa.status = L.status;
     pa.meta = B.meta; pa.mblock_expert = B.mblock_expert; pa.padrow_pair = B.padrow_pair;
     pa.tiles1 = B.tiles1; pa.tiles2 = B.tiles2;
@@ -664,6 +676,7 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
 
     TcCombineArgs ca{};
     ca.y = B.y; ca.ids = L.ids; ca.out = L.out; ca.T = L.T; ca.H = L.H; ca.k = L.k; ca.E = L.E;
+    ca.w = L.w; ca.x = L.x; ca.Z = L.Z;
     ca.has_shared = L.I_shared > 0;
     const int64_t n = (int64_t)L.T * (L.H / 8);
     TC_PHASE(3, (tc_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(ca)))

@@ -4,7 +4,8 @@
 // Routing kinds (spark_model MoE pages): softmax top-K (moe/init.rs, `moe_topk_softmax`
 // handles); sigmoid scores with a correction bias that only affects the selection
 // (moe/mod.rs, `correction_bias_dev` field doc); sqrt(softplus) scores in the same scheme
-// (moe/mod.rs, `moe_topk_sqrtsoftplus` handles).
+// (moe/mod.rs, `moe_topk_sqrtsoftplus` handles); softmax probabilities with a selection bias
+// (moe/mod.rs, the LongCat `moe_topk_softmax_bias` handles).
 #pragma once
 #include "common.cuh"
 
@@ -37,6 +38,7 @@ __device__ __forceinline__ bool warp_topk(const Load& load, const float* bias, i
     bool nonfinite = false;
     float lmax = -INFINITY;
     const bool use_bias = bias != nullptr && scoring != MOE_SCORE_SOFTMAX;
+    const bool softmax = scoring == MOE_SCORE_SOFTMAX || scoring == MOE_SCORE_SOFTMAX_BIAS;
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {  // every load issued before any is used
         const int e = lane + 32 * j;
@@ -46,24 +48,43 @@ __device__ __forceinline__ bool warp_topk(const Load& load, const float* bias, i
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
         const int e = lane + 32 * j;
-        key[j] = 0ull;
         lg[j] = -INFINITY;
         if (e < E) {
-            const float l = raw[j];
-            float v = -INFINITY;
-            if (!isfinite(l)) {
-                nonfinite = true;
+            if (isfinite(raw[j])) {
+                lg[j] = raw[j];
+                lmax = fmaxf(lmax, raw[j]);
             } else {
-                lg[j] = l;
-                lmax = fmaxf(lmax, l);
-                v = (scoring == MOE_SCORE_SOFTMAX) ? l : gate_score(scoring, l) + bv[j];
+                nonfinite = true;
             }
-            key[j] = ((unsigned long long)orderable(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
         }
     }
     const bool any_nonfinite = __any_sync(0xffffffffu, nonfinite);
 #pragma unroll
     for (int o = 16; o; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    // softmax denominator over every finite logit (plain softmax needs it only unrenormalised)
+    float zall = 1.f;
+    if (scoring == MOE_SCORE_SOFTMAX_BIAS || (scoring == MOE_SCORE_SOFTMAX && !renorm)) {
+        zall = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j)
+            if (isfinite(lg[j])) zall += expf(lg[j] - lmax);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) zall += __shfl_xor_sync(0xffffffffu, zall, o);
+    }
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        key[j] = 0ull;
+        if (e < E) {
+            float v = -INFINITY;
+            if (isfinite(lg[j])) {
+                if (scoring == MOE_SCORE_SOFTMAX) v = lg[j];  // softmax is monotone in the logit
+                else if (scoring == MOE_SCORE_SOFTMAX_BIAS) v = expf(lg[j] - lmax) / zall + bv[j];
+                else v = gate_score(scoring, lg[j]) + bv[j];
+            }
+            key[j] = ((unsigned long long)orderable(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
+        }
+    }
 
     my_e = 0;
     for (int r = 0; r < k; ++r) {
@@ -87,21 +108,15 @@ __device__ __forceinline__ bool warp_topk(const Load& load, const float* bias, i
     float num = 0.f;
     if (lane < k) {
         const float l = load(my_e);
-        if (isfinite(l)) num = (scoring == MOE_SCORE_SOFTMAX) ? expf(l - lmax) : gate_score(scoring, l);
+        if (isfinite(l)) num = softmax ? expf(l - lmax) : gate_score(scoring, l);
     }
     float den = 1.f;
     if (renorm) {
         den = num;
 #pragma unroll
         for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    } else if (scoring == MOE_SCORE_SOFTMAX) {
-        float z = 0.f;
-#pragma unroll
-        for (int j = 0; j < EPL; ++j)
-            if (isfinite(lg[j])) z += expf(lg[j] - lmax);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        den = z;
+    } else if (softmax) {
+        den = zall;
     }
     my_w = lane < k ? (den > 0.f ? num / den : 0.f) * scaling : 0.f;
     return any_nonfinite;

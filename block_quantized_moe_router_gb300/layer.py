@@ -18,13 +18,15 @@ class MoeLayer:
     def __init__(self, *, E, H, I, top_k, scoring, gate, up, down, I_shared=0, sh_gate=None,
                  sh_up=None, sh_down=None, w_router=None, correction_bias=None, tid2eid=None,
                  renormalize=True, routed_scaling=1.0, act=capi.MOE_ACT_BF16, g_act1=1.0,
-                 g_act2=1.0):
+                 g_act2=1.0, zero_experts=0):
         self.E, self.H, self.I, self.top_k, self.I_shared = E, H, I, top_k, I_shared
+        self.zero_experts = zero_experts
         self.scoring, self.renormalize, self.routed_scaling = scoring, renormalize, routed_scaling
         self.act, self.g_act1, self.g_act2 = act, g_act1, g_act2
         self.w_router, self.correction_bias, self.tid2eid = w_router, correction_bias, tid2eid
         self._weights = (gate, up, down, sh_gate, sh_up, sh_down)  # keep alive
-        self.desc = capi.ffn_desc(E, H, I, top_k, I_shared, gate, up, down, sh_gate, sh_up, sh_down)
+        self.desc = capi.ffn_desc(E, H, I, top_k, I_shared, gate, up, down, sh_gate, sh_up, sh_down,
+                                  zero_experts)
         self.handle = capi.moe_prepare_weights(self.desc)
         self._ws = None
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -46,7 +48,8 @@ class MoeLayer:
                    I_shared=cfg.I_shared, sh_gate=dev(inp.get("sh_gate")),
                    sh_up=dev(inp.get("sh_up")), sh_down=dev(inp.get("sh_down")),
                    w_router=opt("w_router"), correction_bias=opt("bias"), tid2eid=opt("tid2eid"),
-                   renormalize=cfg.renorm, routed_scaling=cfg.scaling, act=cfg.act)
+                   renormalize=cfg.renorm, routed_scaling=cfg.scaling, act=cfg.act,
+                   zero_experts=cfg.zero_experts)
 
     def close(self):
         if self.handle:
@@ -74,7 +77,8 @@ class MoeLayer:
         if topk_w is None:
             topk_w = torch.empty((T, self.top_k), dtype=torch.float32, device="cuda")
         if (logits_out is None and logits_in is None and self.scoring != capi.MOE_SCORE_HASH):
-            logits_out = torch.empty((T, self.E), dtype=torch.float32, device="cuda")
+            logits_out = torch.empty((T, self.E + self.zero_experts), dtype=torch.float32,
+                                     device="cuda")
         capi.moe_route(T=T, E=self.E, H=self.H, top_k=self.top_k, scoring=self.scoring,
                        renormalize=self.renormalize, routed_scaling=self.routed_scaling, x=x,
                        w_router=None if logits_in is not None else self.w_router,
@@ -82,7 +86,7 @@ class MoeLayer:
                        correction_bias=self.correction_bias, tid2eid=self.tid2eid,
                        vocab=0 if self.tid2eid is None else self.tid2eid.shape[0],
                        token_ids=token_ids, topk_ids=topk_ids, topk_w=topk_w,
-                       dev_status=self.status, stream=stream)
+                       dev_status=self.status, stream=stream, zero_experts=self.zero_experts)
         return topk_ids, topk_w, logits_out
 
     def ffn(self, x, topk_ids, topk_w, out=None, stream=None):
@@ -105,13 +109,14 @@ class MoeLayer:
         if topk_w is None:
             topk_w = torch.empty((T, self.top_k), dtype=torch.float32, device="cuda")
         if (logits_out is None and logits_in is None and self.scoring != capi.MOE_SCORE_HASH):
-            logits_out = torch.empty((T, self.E), dtype=torch.float32, device="cuda")
+            logits_out = torch.empty((T, self.E + self.zero_experts), dtype=torch.float32,
+                                     device="cuda")
         d = capi.route_desc(T=T, E=self.E, H=self.H, top_k=self.top_k, scoring=self.scoring,
                             renormalize=self.renormalize, routed_scaling=self.routed_scaling,
                             w_router=None if logits_in is not None else self.w_router,
                             correction_bias=self.correction_bias, tid2eid=self.tid2eid,
                             vocab=0 if self.tid2eid is None else self.tid2eid.shape[0],
-                            token_ids=token_ids)
+                            token_ids=token_ids, zero_experts=self.zero_experts)
         capi.moe_forward(self.handle, d, self.act, self.g_act1, self.g_act2, x, topk_ids, topk_w,
                          out, self.workspace(T), logits_in=logits_in, logits_out=logits_out,
                          dev_status=self.status, stream=stream)

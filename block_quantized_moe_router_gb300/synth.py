@@ -15,11 +15,13 @@ Workloads (all seeded, synthetic):
   hash64   64 tokens, H 4096, I 2048, 64 experts, top-6 from a tid2eid [32000, 6] table,
            weights 1/6; routed experts MXFP4, shared expert NVFP4
 
+Zero-computation experts (ids E .. E + Z - 1, router width E + Z) appear only in test cases.
+
 Distributions: x ~ N(0,1) in bf16; router ~ N(0, 0.02) in bf16; expert weights
 ~ N(0, 0.02) fp32 encoded to NVFP4 (per-tensor global amax/(6*448), E4M3 scale per 16 =
 E4M3(block amax / 6 / global), nearest E2M1 code) or to MXFP4 (E8M0 scale per 32 =
 2^(floor(log2 block amax) - 2), nearest E2M1 code, saturating at 6); correction bias
-~ U(-0.1, 0.1).
+~ U(-0.1, 0.1) (softmax + bias routing: U(-0.01, 0.01)).
 """
 from __future__ import annotations
 
@@ -31,7 +33,7 @@ import numpy as np
 import torch
 
 FMT_NVFP4, FMT_MXFP4 = 0, 1
-SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_HASH, SCORE_SQRTSOFTPLUS = 0, 1, 2, 3
+SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_HASH, SCORE_SQRTSOFTPLUS, SCORE_SOFTMAX_BIAS = 0, 1, 2, 3, 4
 ACT_BF16, ACT_NVFP4 = 0, 1
 
 
@@ -52,6 +54,7 @@ class MoeConfig:
     act: int = ACT_BF16
     vocab: int = 0               # hash routing table rows
     zipf_s: float = 0.0          # > 0: skew router logits so expert counts follow Zipf(s)
+    zero_experts: int = 0        # zero-computation experts (ids E .. E + Z - 1, output = input)
 
     @property
     def pairs(self) -> int:
@@ -175,23 +178,26 @@ def make_inputs(cfg: MoeConfig, seed: int = 0, device="cpu",
     an independent stream (used to enforce a minimum top-K score gap).
     """
     T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    Er = E + cfg.zero_experts  # router outputs: real experts, then zero-computation experts
     inp = {"cfg": cfg}
     x = torch.randn((T, H), generator=_gen(seed, 1), dtype=torch.float32)
     for t, cnt in (resample or {}).items():
         if cnt > 0:
             x[t] = torch.randn((H,), generator=_gen(seed, 2, t, cnt), dtype=torch.float32)
     if cfg.scoring != SCORE_HASH:
-        wr = torch.randn((E, H), generator=_gen(seed, 3), dtype=torch.float32) * 0.02
+        wr = torch.randn((Er, H), generator=_gen(seed, 3), dtype=torch.float32) * 0.02
         if cfg.zipf_s > 0:
             x[:, H - 1] = 1.0
             wr[:, H - 1] = zipf_logit_offsets(cfg, seed).float()
         inp["w_router"] = wr.to(torch.bfloat16)
     inp["x"] = x.to(torch.bfloat16)
-    if cfg.scoring in (SCORE_SIGMOID, SCORE_SQRTSOFTPLUS):
-        inp["bias"] = (torch.rand((E,), generator=_gen(seed, 4), dtype=torch.float32) * 0.2 - 0.1)
+    if cfg.scoring in (SCORE_SIGMOID, SCORE_SQRTSOFTPLUS, SCORE_SOFTMAX_BIAS):
+        u = torch.rand((Er,), generator=_gen(seed, 4), dtype=torch.float32) * 0.2 - 0.1
+        # softmax probabilities are ~1/Er: a bias of +-0.01 is on their scale
+        inp["bias"] = u * 0.1 if cfg.scoring == SCORE_SOFTMAX_BIAS else u
     if cfg.scoring == SCORE_HASH:
         gt = _gen(seed, 5)
-        inp["tid2eid"] = torch.rand((cfg.vocab, E), generator=gt).argsort(dim=1)[:, :k].contiguous().to(torch.int64)
+        inp["tid2eid"] = torch.rand((cfg.vocab, Er), generator=gt).argsort(dim=1)[:, :k].contiguous().to(torch.int64)
         inp["token_ids"] = torch.randint(0, cfg.vocab, (T,), generator=_gen(seed, 6), dtype=torch.int32)
     if with_weights:
         inp["gate"] = _expert_weights(E, I, H, cfg.fmt, seed, 10, device)

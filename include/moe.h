@@ -58,7 +58,8 @@ typedef enum {
     MOE_SCORE_SOFTMAX = 0,
     MOE_SCORE_SIGMOID = 1,
     MOE_SCORE_HASH = 2,
-    MOE_SCORE_SQRTSOFTPLUS = 3
+    MOE_SCORE_SQRTSOFTPLUS = 3,
+    MOE_SCORE_SOFTMAX_BIAS = 4
 } moe_scoring_t;
 typedef enum { MOE_FMT_NVFP4 = 0, MOE_FMT_MXFP4 = 1 } moe_fmt_t;
 /* Activation precision of the expert GEMMs.  BF16: W4A16 (bf16 tokens, dequantized
@@ -74,18 +75,25 @@ typedef struct {
     int32_t fmt;           /* moe_fmt_t                                                     */
 } moe_qtensor;
 
-/* The expert weights of one MoE layer.  Constraints (checked): 1 <= E <= 512;
- * H, I, I_shared multiples of 128; I_shared == 0 means no shared expert.
- * A shared expert is one expert (E = 1 in its tensors) added with weight 1. */
+/* The expert weights of one MoE layer.  Constraints (checked): 1 <= E, E + zero_experts <= 512,
+ * 1 <= top_k <= min(E + zero_experts, 32); H, I, I_shared multiples of 128; I_shared == 0
+ * means no shared expert.  A shared expert is one expert (E = 1 in its tensors) added with
+ * weight 1.  zero_experts (Z >= 0) zero-computation experts have ids E .. E + Z - 1 and no
+ * weights: such an expert returns its input, so a pair routed to it adds w * x[t] (the bf16
+ * token, whatever act is) -- the LongCat zero-computation experts of the spark_model MoE
+ * pages (moe/mod.rs, `moe_zero_expert_add` handle and `zero_accum_dev` field doc). */
 typedef struct {
     int32_t E, H, I, top_k, I_shared;
     moe_qtensor gate, up, down;
     moe_qtensor sh_gate, sh_up, sh_down;
+    int32_t zero_experts;
 } moe_ffn_desc;
 
-/* Routing of T tokens.  Constraints (checked): 1 <= E <= 512, 1 <= top_k <= min(E, 32);
- * softmax/sigmoid: H a multiple of 32 when the router GEMM runs;
- * hash: tid2eid and token_ids non-NULL, vocab >= 1. */
+/* Routing of T tokens over E real experts and zero_experts zero-computation experts (ids
+ * E .. E + zero_experts - 1; see moe_ffn_desc).  The router has E + zero_experts outputs:
+ * w_router [E + Z][H], correction_bias [E + Z], logits [T][E + Z].  Constraints (checked):
+ * 1 <= E, E + Z <= 512, 1 <= top_k <= min(E + Z, 32); learned routers: H a multiple of 32 when
+ * the router GEMM runs; hash: tid2eid and token_ids non-NULL, vocab >= 1. */
 typedef struct {
     int32_t T, E, H, top_k;
     int32_t scoring;           /* moe_scoring_t                                            */
@@ -96,11 +104,15 @@ typedef struct {
     const int64_t* tid2eid;    /* [device] int64 [vocab][top_k] (hash only)               */
     int64_t vocab;
     const int32_t* token_ids;  /* [device] int32 [T] (hash only)                          */
+    int32_t zero_experts;      /* Z >= 0 zero-computation experts after the E real ones    */
 } moe_route_desc;
 
-/* Router GEMM + top-K.
+/* Router GEMM + top-K (every rule below runs over the E + zero_experts router outputs).
  *   Softmax: p = softmax(logits) over all E; the top_k largest are selected; weight =
  *     p / sum(selected p) when renormalize, else p; times routed_scaling.
+ *   Softmax + bias: p = softmax(logits); selection ranks p + correction_bias; weight = p /
+ *     sum(selected p) when renormalize, else p; times routed_scaling (moe/mod.rs, the LongCat
+ *     `moe_topk_softmax_bias` handles, whose router width is num_experts + zero_expert_num).
  *   Sigmoid: s = sigmoid(logits); selection ranks s + correction_bias; weight = s /
  *     sum(selected s) when renormalize, else s; times routed_scaling.  (moe/mod.rs,
  *     `correction_bias_dev` field doc.)
@@ -133,7 +145,9 @@ moe_status_t moe_release_weights(void* handle);
 
 /* Expert FFN + weighted combine:
  *   out[t] = sum_j topk_w[t][j] * FFN_{topk_ids[t][j]}(x[t]) + FFN_shared(x[t]),
- *   FFN_e(a) = W_down,e (SiLU(W_gate,e a) * (W_up,e a)).
+ *   FFN_e(a) = W_down,e (SiLU(W_gate,e a) * (W_up,e a)) for a real expert e < E,
+ *   FFN_e(a) = x[t] for a zero-computation expert E <= e < E + zero_experts;
+ *   pairs with any other id (e.g. -1) are dropped.
  * act = MOE_ACT_NVFP4 quantizes x with global g_act1 and h with global g_act2 (each a
  * power of two) before the FP4 products; MOE_ACT_BF16 ignores both.
  * x_bf16 [device] bf16 [T][H]; topk_ids/topk_w as written by moe_route;
@@ -149,7 +163,8 @@ moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g
  * logits_out, topk_ids, topk_w, dev_status) followed by moe_ffn_forward(handle, route->T, act,
  * g_act1, g_act2, x_bf16, topk_ids, topk_w, out_bf16, workspace, ws_bytes, dev_status), with the
  * same argument rules, outputs and workspace size (moe_workspace_size of the handle's
- * descriptor).  route->E, route->top_k and route->H must equal the handle's E, top_k and H.
+ * descriptor).  route->E, route->top_k, route->H and route->zero_experts must equal the
+ * handle's E, top_k, H and zero_experts.
  * For a few tokens (T <= 8, T * top_k <= 64, act == MOE_ACT_BF16) the router GEMV, the top-K
  * selection (or the hash lookup), the expert FFN and the weighted sum run in ONE persistent
  * kernel launch with one thread block per SM and two device-wide barriers -- the single-launch

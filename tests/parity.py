@@ -18,11 +18,12 @@ W_TOL = 1e-6
 
 
 def oracle_route(cfg, inp):
+    Er = cfg.E + cfg.zero_experts
     if cfg.scoring == synth.SCORE_HASH:
-        return oracle.route(T=cfg.T, E=cfg.E, k=cfg.k, scoring=2, scaling=cfg.scaling,
+        return oracle.route(T=cfg.T, E=Er, k=cfg.k, scoring=2, scaling=cfg.scaling,
                             tid2eid=inp["tid2eid"].numpy(), token_ids=inp["token_ids"].numpy(),
                             vocab=cfg.vocab)
-    return oracle.route(T=cfg.T, E=cfg.E, k=cfg.k, scoring=cfg.scoring, renorm=cfg.renorm,
+    return oracle.route(T=cfg.T, E=Er, k=cfg.k, scoring=cfg.scoring, renorm=cfg.renorm,
                         scaling=cfg.scaling, x_bf16=synth.bf16_bits(inp["x"]),
                         w_router_bf16=synth.bf16_bits(inp["w_router"]),
                         bias=None if "bias" not in inp else inp["bias"].numpy())
@@ -68,7 +69,7 @@ def oracle_ffn(cfg, inp, ids, w, tokens=None):
     return oracle.moe_ffn(T=x.shape[0], E=cfg.E, H=cfg.H, I=cfg.I, k=cfg.k, gate=npj("gate"),
                           up=npj("up"), down=npj("down"), x_bf16=synth.bf16_bits(x), ids=ids, w=w,
                           sh_I=cfg.I_shared, sh_gate=npj("sh_gate"), sh_up=npj("sh_up"),
-                          sh_down=npj("sh_down"), act_mode=cfg.act)
+                          sh_down=npj("sh_down"), act_mode=cfg.act, zero_experts=cfg.zero_experts)
 
 
 def assert_close(gpu: torch.Tensor, ref: np.ndarray, what: str = "out"):
@@ -93,7 +94,8 @@ def assert_routing(cfg, ref, ids, w, gpu_logits=None, inp=None):
     ref_w = ref["w"]
     if gpu_logits is not None and cfg.scoring != synth.SCORE_HASH:
         lg = gpu_logits.float().cpu().numpy()
-        r2 = oracle.route(T=cfg.T, E=cfg.E, k=cfg.k, scoring=cfg.scoring, renorm=cfg.renorm,
+        r2 = oracle.route(T=cfg.T, E=cfg.E + cfg.zero_experts, k=cfg.k, scoring=cfg.scoring,
+                          renorm=cfg.renorm,
                           scaling=cfg.scaling, logits_in=lg,
                           bias=None if inp is None or "bias" not in inp else inp["bias"].numpy())
         assert np.array_equal(r2["ids"], ref["ids"]), "ids from the GPU logits differ"

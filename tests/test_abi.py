@@ -36,11 +36,11 @@ def test_status_strings(lib):
     assert "unknown" in capi.moe_status_string(99)
 
 
-def _fake_desc(E=8, H=256, I=128, k=2, Is=0, fmt=0):
+def _fake_desc(E=8, H=256, I=128, k=2, Is=0, fmt=0, Z=0):
     fake = 0x1000
     q = capi.moe_qtensor(fake, fake, fake if fmt == 0 else None, fmt)
     sq = q if Is else capi.moe_qtensor(None, None, None, 0)
-    return capi.moe_ffn_desc(E, H, I, k, Is, q, q, q, sq, sq, sq)
+    return capi.moe_ffn_desc(E, H, I, k, Is, q, q, q, sq, sq, sq, Z)
 
 
 def test_workspace_size_and_validation(lib):
@@ -53,8 +53,10 @@ def test_workspace_size_and_validation(lib):
         sizes = [capi.moe_workspace_size(_fake_desc(H=512, I=256, Is=256), T, act)
                  for T in (1, 8, 9, 64, 1000)]
         assert all(a <= b for a, b in zip(sizes[2:], sizes[3:]))
+    assert capi.moe_workspace_size(_fake_desc(k=9, Z=2), 4, 0) > 0  # k <= E + Z is fine
     for bad in [_fake_desc(E=0), _fake_desc(E=513), _fake_desc(k=9), _fake_desc(k=0),
-                _fake_desc(H=200), _fake_desc(I=64), _fake_desc(Is=100)]:
+                _fake_desc(H=200), _fake_desc(I=64), _fake_desc(Is=100), _fake_desc(Z=-1),
+                _fake_desc(E=510, Z=3)]:
         with pytest.raises(capi.MoeError) as ei:
             capi.moe_workspace_size(bad, 4, 0)
         assert ei.value.status == capi.MOE_ERR_INVALID_ARG
@@ -73,7 +75,8 @@ def test_route_rejects_before_launch(lib):
 
     def call(**kw):
         args = dict(T=4, E=8, H=64, top_k=2, scoring=0, renormalize=1, routed_scaling=1.0,
-                    w_router=None, correction_bias=None, tid2eid=None, vocab=0, token_ids=None)
+                    w_router=None, correction_bias=None, tid2eid=None, vocab=0, token_ids=None,
+                    zero_experts=0)
         args.update(kw)
         d = capi.moe_route_desc(*[args[f] for f, _ in capi.moe_route_desc._fields_])
         return lib.moe_route(ctypes.byref(d), fake, None, None, fake, fake, None, None)
@@ -82,6 +85,9 @@ def test_route_rejects_before_launch(lib):
     assert call(E=0) == capi.MOE_ERR_INVALID_ARG
     assert call(T=-1) == capi.MOE_ERR_INVALID_ARG
     assert call(scoring=5, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG
+    assert call(zero_experts=-1, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG
+    assert call(E=500, zero_experts=13, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG  # E + Z > 512
+    assert call(top_k=9, zero_experts=1, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG  # k > E + Z
     assert call() == capi.MOE_ERR_INVALID_ARG               # no logits and no router
     assert call(scoring=2) == capi.MOE_ERR_INVALID_ARG      # hash without a table
     assert call(routed_scaling=float("nan"), w_router=0x1000) == capi.MOE_ERR_INVALID_ARG

@@ -49,6 +49,9 @@ SMALL = {
                             I_shared=128, fmt=S.FMT_MXFP4, vocab=50),
     "dec_t1": S.MoeConfig("dec_t1", T=1, H=512, I=128, E=16, k=4, scoring=S.SCORE_SOFTMAX,
                           renorm=False),
+    # softmax + bias over real and zero-computation experts (routing kernel, then the given ids)
+    "dec_zero": S.MoeConfig("dec_zero", T=6, H=256, I=128, E=10, k=3,
+                            scoring=S.SCORE_SOFTMAX_BIAS, I_shared=128, zero_experts=3),
     # NVFP4 activations with 256-multiple shapes: tcgen05 block-scaled path
     "tc_small": S.MoeConfig("tc_small", T=40, H=512, I=256, E=16, k=4, scoring=S.SCORE_SIGMOID,
                             scaling=2.5, I_shared=256, act=S.ACT_NVFP4),

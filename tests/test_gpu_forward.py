@@ -41,11 +41,25 @@ CASES = {
                                 renorm=False),
     "many_experts": S.MoeConfig("fw_many_e", T=2, H=512, I=256, E=512, k=8,
                                 scoring=S.SCORE_SOFTMAX),
+    # softmax + bias routing over real and zero-computation experts (ids >= E add w * x)
+    "zero_softmax_bias": S.MoeConfig("fw_zero_sb", T=5, H=512, I=256, E=12, k=4,
+                                     scoring=S.SCORE_SOFTMAX_BIAS, renorm=False, scaling=1.5,
+                                     I_shared=128, zero_experts=4),
+    "zero_softmax_bias_renorm": S.MoeConfig("fw_zero_sbr", T=8, H=256, I=128, E=20, k=6,
+                                            scoring=S.SCORE_SOFTMAX_BIAS, zero_experts=6),
+    "zero_hash": S.MoeConfig("fw_zero_hash", T=6, H=256, I=256, E=16, k=4, scoring=S.SCORE_HASH,
+                             I_shared=128, fmt=S.FMT_MXFP4, vocab=50, zero_experts=3),
     # more tokens: moe_route + moe_ffn_forward behind the same call
     "fallback_generic": S.MoeConfig("fw_generic", T=20, H=256, I=128, E=16, k=3,
                                     scoring=S.SCORE_SIGMOID, scaling=2.5, I_shared=128),
     "fallback_tc": S.MoeConfig("fw_tc", T=40, H=512, I=256, E=16, k=4, scoring=S.SCORE_SIGMOID,
                                scaling=2.5, I_shared=256, act=S.ACT_NVFP4),
+    "fallback_generic_zero": S.MoeConfig("fw_generic_zero", T=20, H=256, I=128, E=12, k=3,
+                                         scoring=S.SCORE_SOFTMAX_BIAS, I_shared=128,
+                                         zero_experts=4),
+    "fallback_tc_zero": S.MoeConfig("fw_tc_zero", T=40, H=512, I=256, E=16, k=4,
+                                    scoring=S.SCORE_SOFTMAX_BIAS, renorm=False, scaling=2.0,
+                                    I_shared=256, act=S.ACT_NVFP4, zero_experts=4),
 }
 
 
