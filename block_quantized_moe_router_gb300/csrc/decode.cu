@@ -190,9 +190,9 @@ __device__ __forceinline__ void dec_dispatch(int T, int k, int E, int I_shared, 
 }
 
 // ---- the MMAs of one ring stage ---------------------------------------------------------------
-// gate+up: one K-step of 32 rows (tiles t = 0, 1) of gate and up; B = x in f16.
+// gate+up: one K-step of 16 * TPS rows (tiles t < TPS) of gate and up; B = x in f16.
 // acc[t][m][p]: tile t, matrix m (gate, up), MMA chain p (even / odd sub-steps).
-template <int FMT>
+template <int FMT, int TPS>
 __device__ __forceinline__ void gu_stage(const uint8_t* st, bool has_tok, int lane, int g, int q,
                                          int mxg, int mxu, float (&acc)[2][2][2][4]) {
     uint4 bx[4];
@@ -200,9 +200,9 @@ __device__ __forceinline__ void gu_stage(const uint8_t* st, bool has_tok, int la
     for (int c = 0; c < 4; ++c)
         bx[c] = has_tok ? *reinterpret_cast<const uint4*>(st + kDecStageB + c * 512 + lane * 16)
                         : make_uint4(0, 0, 0, 0);
-    ChunkA cw[2][2];
+    ChunkA cw[TPS][2];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < TPS; ++t) {
         const uint2* sc = reinterpret_cast<const uint2*>(st + kDecStageC + t * 256);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
@@ -217,7 +217,7 @@ __device__ __forceinline__ void gu_stage(const uint8_t* st, bool has_tok, int la
     {                                                                                    \
         const uint32_t b0 = word_of(bx[I >> 1], (I & 1) * 2);                            \
         const uint32_t b1 = word_of(bx[I >> 1], (I & 1) * 2 + 1);                        \
-        _Pragma("unroll") for (int t = 0; t < 2; ++t)                                    \
+        _Pragma("unroll") for (int t = 0; t < TPS; ++t)                                  \
         _Pragma("unroll") for (int m = 0; m < 2; ++m) {                                  \
             uint32_t fa[4];                                                              \
             frag_a<I>(cw[t][m], fa);                                                     \
@@ -263,7 +263,9 @@ __device__ __forceinline__ float sum4(const float (&a)[2][2][4], int i) {
 }
 
 // ------------------------------------------------------------------------------------------
-template <int FR, int FS>
+// TPS: MMA tiles (16 rows each) per gate+up ring stage -- 2, or 1 when a layer has too few
+// 32-row tasks to give every CTA at least two.
+template <int FR, int FS, int TPS>
 __global__ void __launch_bounds__(kDecThreads, 1)
 dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
     extern __shared__ __align__(16) uint8_t dsm[];
@@ -436,8 +438,9 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
     // K-steps w, w + 8, ..., so at any time the 8 warps read 512 contiguous bytes of every row.
     const int n_active = D.n_active;
     const bool has_shared = L.I_shared > 0;
-    const int tilesR = L.I / 32;
-    const int ntasks = n_active * tilesR + (has_shared ? L.I_shared / 32 : 0);
+    const int rows_t = 16 * TPS;
+    const int tilesR = L.I / rows_t;
+    const int ntasks = n_active * tilesR + (has_shared ? L.I_shared / rows_t : 0);
     const int cnt_g = cta < ntasks ? (ntasks - cta + G - 1) / G : 0;
     const int ksteps_g = H / 128;
     const int n_g = ksteps_g > warp ? (ksteps_g - warp + kDecWarps - 1) / kDecWarps : 0;
@@ -453,10 +456,10 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         const int tau = cta + j * G;
         if (tau < n_active * tilesR) {
             slot = tau / tilesR;
-            n0 = (tau - slot * tilesR) * 32;
+            n0 = (tau - slot * tilesR) * rows_t;
         } else {
             slot = n_active;
-            n0 = (tau - n_active * tilesR) * 32;
+            n0 = (tau - n_active * tilesR) * rows_t;
         }
     };
     auto pair_of = [&](int p, int& tl, int& slot) {  // pair p of this CTA -> (tile, slot)
@@ -543,7 +546,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         if (ic_phase == 0) {
             const int o = ic_s * 64;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
+            for (int t = 0; t < TPS; ++t) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const size_t ro = (size_t)(16 * t + 8 * r) * ic_rb + o;
@@ -600,8 +603,9 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             issue_next();
             cp_async_wait<kDecStages - 1>();
             __syncwarp();
-            if (fmt == MOE_FMT_NVFP4) gu_stage<MOE_FMT_NVFP4>(stage_ptr(consumed), has_tok, lane, g, q, mxg, mxu, acc);
-            else gu_stage<MOE_FMT_MXFP4>(stage_ptr(consumed), has_tok, lane, g, q, mxg, mxu, acc);
+            const uint8_t* st = stage_ptr(consumed);
+            if (fmt == MOE_FMT_NVFP4) gu_stage<MOE_FMT_NVFP4, TPS>(st, has_tok, lane, g, q, mxg, mxu, acc);
+            else gu_stage<MOE_FMT_MXFP4, TPS>(st, has_tok, lane, g, q, mxg, mxu, acc);
             ++consumed;
         }
         // K-split reduction, double-buffered: one CTA barrier per task
@@ -614,7 +618,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
                 for (int i = 0; i < 4; ++i)
                     rg[(warp * 16 + t * 8 + m * 4 + i) * 32 + lane] = acc[t][m][0][i] + acc[t][m][1][i];
         __syncthreads();
-        {   // thread -> (tile, accumulator index, lane) of the MMA layout
+        if (tid < 128 * TPS) {  // thread -> (tile, accumulator index, lane) of the MMA layout
             const int t = tid >> 7, i = (tid >> 5) & 3, ln = tid & 31;
             float Gs = 0.f, Us = 0.f;
 #pragma unroll
@@ -716,12 +720,12 @@ int decode_smem_bytes(int H, int sms) {
     return kDecRingBytes + (kDecRedG > tpc * kDecRedDTile ? kDecRedG : tpc * kDecRedDTile);
 }
 
-template <int FR, int FS>
-static cudaError_t launch_fused_fmt(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
+template <int FR, int FS, int TPS>
+static cudaError_t launch_fused_tps(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
                                     int sms, cudaStream_t st) {
     const int smem = decode_smem_bytes(L.H, sms);
     if (smem < 0) return cudaErrorInvalidConfiguration;
-    auto kern = dec_fused_kernel<FR, FS>;
+    auto kern = dec_fused_kernel<FR, FS, TPS>;
     cudaError_t err;
     if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
         return err;
@@ -740,6 +744,17 @@ static cudaError_t launch_fused_fmt(const FfnLaunch& L, const DecRoute& R, unsig
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, L, R, bar);
+}
+
+template <int FR, int FS>
+static cudaError_t launch_fused_fmt(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
+                                    int sms, cudaStream_t st) {
+    // 32-row gate+up tasks unless even the most experts the routing can touch give fewer than
+    // two per CTA (then 16-row tasks balance the CTAs better)
+    const int slots = L.E < L.T * L.k ? L.E : L.T * L.k;
+    const int tasks32 = slots * (L.I / 32) + (L.I_shared > 0 ? L.I_shared / 32 : 0);
+    if (tasks32 >= 2 * sms) return launch_fused_tps<FR, FS, 2>(L, R, bar, sms, st);
+    return launch_fused_tps<FR, FS, 1>(L, R, bar, sms, st);
 }
 
 cudaError_t launch_decode_fused(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,

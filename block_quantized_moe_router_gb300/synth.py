@@ -12,6 +12,7 @@ Workloads (all seeded, synthetic):
            1 shared expert (I_s 2048)
   pre4096  4096 tokens with the dec8 shapes and routing, router logits skewed so that the
            per-expert token counts fall off like a Zipf law (s = 1.1); NVFP4 activations
+  pre32768 the same with 32768 tokens (compute-bound: ~1000 rows per expert)
   hash64   64 tokens, H 4096, I 2048, 64 experts, top-6 from a tid2eid [32000, 6] table,
            weights 1/6; routed experts MXFP4, shared expert NVFP4
 
@@ -71,6 +72,10 @@ CONFIGS: Dict[str, MoeConfig] = {
                       scaling=2.5, I_shared=2048),
     "pre4096": MoeConfig("pre4096", T=4096, H=7168, I=2048, E=256, k=8, scoring=SCORE_SIGMOID,
                          scaling=2.5, I_shared=2048, act=ACT_NVFP4, zipf_s=1.1),
+    # the prefill shapes with 8x the tokens: ~1000 rows per expert, above the FP4 ridge
+    # (the compute-bound variant of the 4096-token case)
+    "pre32768": MoeConfig("pre32768", T=32768, H=7168, I=2048, E=256, k=8, scoring=SCORE_SIGMOID,
+                          scaling=2.5, I_shared=2048, act=ACT_NVFP4, zipf_s=1.1),
     "hash64": MoeConfig("hash64", T=64, H=4096, I=2048, E=64, k=6, scoring=SCORE_HASH,
                         I_shared=2048, fmt=FMT_MXFP4, shared_fmt=FMT_NVFP4, vocab=32000),
     # decode-shaped (8 tokens, dec8 shapes) and prefill-shaped cases small enough (32 experts,
