@@ -80,6 +80,8 @@ struct DecShared {
     float w[64];
     float zw[kDecMaxT];  // per token: summed weight of its zero-computation experts
     float red_router[4][kDecWarps][kDecMaxT];
+    float sh_post[3];    // the shared expert's post-scales and MXFP4 biases (gate, up, down)
+    int sh_mxb[3];
 };
 
 // ---- small helpers ---------------------------------------------------------------------------
@@ -282,6 +284,23 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
     float* red_d = red_g;  // reused for the down partial sums after barrier 2
 
     // ---- phase 0 ----------------------------------------------------------------------------
+    // The post-scales (and MXFP4 exponent offsets) of the routed projections for ALL experts
+    // go into the idle partial-sum region now, so that once the routing is known the per-slot
+    // values come from shared memory instead of a dependent global round trip.
+    float* tab_post = red_g;                                                    // [3][kMaxExperts]
+    int32_t* tab_mx = reinterpret_cast<int32_t*>(red_g + 3 * kMaxExperts);     // [3][kMaxExperts]
+    for (int i = tid; i < 3 * E; i += kDecThreads) {
+        const int pj = i / E, e = i - pj * E;
+        const ProjView& PV = pj == 0 ? L.gate : pj == 1 ? L.up : L.down;
+        cp_async4(smem_addr(tab_post + pj * kMaxExperts + e), PV.post + e);
+        if (PV.fmt == MOE_FMT_MXFP4) cp_async4(smem_addr(tab_mx + pj * kMaxExperts + e), PV.mx_off + e);
+    }
+    cp_async_commit();
+    if (tid < 3 && L.I_shared > 0) {
+        const ProjView& PV = tid == 0 ? L.sh_gate : tid == 1 ? L.sh_up : L.sh_down;
+        S.sh_post[tid] = PV.post[0];
+        S.sh_mxb[tid] = PV.fmt == MOE_FMT_MXFP4 ? 112 + PV.mx_off[0] : 0;
+    }
     {   // x -> f16 (this CTA's slice of the flat array)
         const int n8 = T * H / 8;
         const uint4* xs = static_cast<const uint4*>(L.x);
@@ -313,35 +332,46 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
                 }
             cp_async_wait<0>();
             __syncthreads();  // x is staged
+            float acc[kDecRouterBatch][kDecMaxT];
 #pragma unroll
-            for (int b = 0; b < kDecRouterBatch; ++b) {
-                float acc[kDecMaxT];
+            for (int b = 0; b < kDecRouterBatch; ++b)
 #pragma unroll
-                for (int t = 0; t < kDecMaxT; ++t) acc[t] = 0.f;
+                for (int t = 0; t < kDecMaxT; ++t) acc[b][t] = 0.f;
+            const int nb = min(kDecRouterBatch, (Er - e0 + G - 1) / G);  // experts of this batch
 #pragma unroll
-                for (int m = 0; m < kDecRouterChunks; ++m) {
-                    const int c = tid + m * kDecThreads;
-                    if (c < chunks) {
-                        float wf[8];
-                        unpack_bf16x8(wv[b][m], wf);
+            for (int m = 0; m < kDecRouterChunks; ++m) {
+                const int c = tid + m * kDecThreads;
+                if (c < chunks) {
+                    float wf[kDecRouterBatch][8];
 #pragma unroll
-                        for (int t = 0; t < kDecMaxT; ++t) {
-                            if (t < T) {
-                                float xf[8];
-                                unpack_bf16x8(xs_smem[t * chunks + c], xf);
+                    for (int b = 0; b < kDecRouterBatch; ++b) unpack_bf16x8(wv[b][m], wf[b]);
 #pragma unroll
-                                for (int i = 0; i < 8; ++i) acc[t] = fmaf(wf[i], xf[i], acc[t]);
+                    for (int t = 0; t < kDecMaxT; ++t) {
+                        if (t < T) {
+                            float xf[8];
+                            unpack_bf16x8(xs_smem[t * chunks + c], xf);
+#pragma unroll
+                            for (int b = 0; b < kDecRouterBatch; ++b) {
+                                if (b < nb) {
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) acc[b][t] = fmaf(wf[b][i], xf[i], acc[b][t]);
+                                }
                             }
                         }
                     }
                 }
+            }
 #pragma unroll
-                for (int t = 0; t < kDecMaxT; ++t)
+            for (int b = 0; b < kDecRouterBatch; ++b) {
+                if (b < nb) {
 #pragma unroll
-                    for (int o = 16; o; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-                if (lane == 0)
+                    for (int t = 0; t < kDecMaxT; ++t)
 #pragma unroll
-                    for (int t = 0; t < kDecMaxT; ++t) S.red_router[b][warp][t] = acc[t];
+                        for (int o = 16; o; o >>= 1) acc[b][t] += __shfl_xor_sync(0xffffffffu, acc[b][t], o);
+                    if (lane == 0)
+#pragma unroll
+                        for (int t = 0; t < kDecMaxT; ++t) S.red_router[b][warp][t] = acc[b][t];
+                }
             }
             __syncthreads();
             if (tid < kDecRouterBatch * kDecMaxT) {
@@ -355,6 +385,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             }
         }
     }
+    cp_async_wait<0>();           // the post-scale tables are in
     grid_barrier(bar, L.status);  // x16 and the logits are written
 
     // ---- phase 1: routing and dispatch ---------------------------------------------------------
@@ -423,12 +454,15 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         const int nsl = D.n_active + (L.I_shared > 0 ? 1 : 0);
         for (int i = tid; i < nsl * 3; i += kDecThreads) {
             const int slot = i / 3, pj = i - slot * 3;
-            const bool sh = slot == D.n_active;
-            const ProjView& PV = pj == 0 ? (sh ? L.sh_gate : L.gate)
-                                         : pj == 1 ? (sh ? L.sh_up : L.up) : (sh ? L.sh_down : L.down);
-            const int e = D.expert[slot];
-            D.post[slot][pj] = PV.post[e];
-            D.mxb[slot][pj] = PV.fmt == MOE_FMT_MXFP4 ? 112 + PV.mx_off[e] : 0;
+            if (slot == D.n_active) {
+                D.post[slot][pj] = S.sh_post[pj];
+                D.mxb[slot][pj] = S.sh_mxb[pj];
+            } else {
+                const int e = D.expert[slot];
+                const bool mx = (pj == 0 ? L.gate.fmt : pj == 1 ? L.up.fmt : L.down.fmt) == MOE_FMT_MXFP4;
+                D.post[slot][pj] = tab_post[pj * kMaxExperts + e];
+                D.mxb[slot][pj] = mx ? 112 + tab_mx[pj * kMaxExperts + e] : 0;
+            }
         }
         __syncthreads();
     }

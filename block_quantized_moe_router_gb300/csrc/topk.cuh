@@ -87,6 +87,7 @@ __device__ __forceinline__ bool warp_topk(const Load& load, const float* bias, i
     }
 
     my_e = 0;
+    float my_l = 0.f;  // the logit of this lane's pick, passed on by the lane that held it
     for (int r = 0; r < k; ++r) {
         unsigned long long t[EPL];
 #pragma unroll
@@ -101,15 +102,22 @@ __device__ __forceinline__ bool warp_topk(const Load& load, const float* bias, i
         const unsigned long long best = ((unsigned long long)whi << 32) | wlo;
         // keys are unique (they hold the expert index): clear the winner by value, so the key
         // array is never indexed at run time and stays in registers
+        float hit = 0.f;
 #pragma unroll
-        for (int j = 0; j < EPL; ++j) key[j] = key[j] == best ? 0ull : key[j];
-        if (lane == r) my_e = (int)(0xFFFFFFFFu - wlo);
+        for (int j = 0; j < EPL; ++j) {
+            const bool won = key[j] == best;
+            hit = won ? raw[j] : hit;
+            key[j] = won ? 0ull : key[j];
+        }
+        const int e = (int)(0xFFFFFFFFu - wlo);
+        const float l = __shfl_sync(0xffffffffu, hit, e & 31);  // expert e sits in lane e % 32
+        if (lane == r) {
+            my_e = e;
+            my_l = l;
+        }
     }
     float num = 0.f;
-    if (lane < k) {
-        const float l = load(my_e);
-        if (isfinite(l)) num = softmax ? expf(l - lmax) : gate_score(scoring, l);
-    }
+    if (lane < k && isfinite(my_l)) num = softmax ? expf(my_l - lmax) : gate_score(scoring, my_l);
     float den = 1.f;
     if (renorm) {
         den = num;
