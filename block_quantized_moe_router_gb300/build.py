@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["api.cu", "route.cu", "ffn.cu", "decode.cu", "prefill_tc.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "route.cu", "ffn.cu", "decode.cu", "decode_t1.cu", "prefill_tc.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

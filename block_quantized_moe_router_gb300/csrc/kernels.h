@@ -156,7 +156,6 @@ struct DecRoute {
 // only by launches of `sms` CTAs.
 cudaError_t launch_decode_fused(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
                                 int sms, cudaStream_t st);
-int decode_smem_bytes(int H, int sms);
 
 cudaError_t launch_quantize_act(const void* x, int64_t rows, int64_t K, float g, uint8_t* packed,
                                 uint8_t* scales, __half* deq16, cudaStream_t st);

@@ -39,6 +39,12 @@ CASES = {
                         I_shared=128, fmt=S.FMT_MXFP4, vocab=50),
     "t1_no_renorm": S.MoeConfig("fw_t1", T=1, H=512, I=128, E=16, k=4, scoring=S.SCORE_SOFTMAX,
                                 renorm=False),
+    # one token with 32-row gate+up tasks (enough of them for two per CTA), MXFP4 routed
+    # experts and an NVFP4 shared expert
+    "t1_wide": S.MoeConfig("fw_t1_wide", T=1, H=768, I=2048, E=16, k=8, scoring=S.SCORE_SIGMOID,
+                           scaling=2.5, I_shared=1024, fmt=S.FMT_MXFP4, shared_fmt=S.FMT_NVFP4),
+    "t1_zero_hash": S.MoeConfig("fw_t1_zero_hash", T=1, H=256, I=384, E=12, k=4,
+                                scoring=S.SCORE_HASH, I_shared=128, vocab=40, zero_experts=2),
     "many_experts": S.MoeConfig("fw_many_e", T=2, H=512, I=256, E=512, k=8,
                                 scoring=S.SCORE_SOFTMAX),
     # softmax + bias routing over real and zero-computation experts (ids >= E add w * x)
