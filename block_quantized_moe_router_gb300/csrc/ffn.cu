@@ -113,27 +113,45 @@ __global__ void __launch_bounds__(512) prep_kernel(FfnLaunch L) {
 
 // ------------------------------------------------------------------------------------------
 // Grouped expert GEMM on m16n8k16 f16 MMAs.
+//
+// A CTA of kErWarps warps owns 16 * kErWarps rows of one expert's projection (16 per warp)
+// over the whole K, and the expert's tokens in passes of up to NT MMA column tiles of 8.  The
+// operands stream through a CTA ring of kErStages shared-memory stages filled by cp.async,
+// kErStages - 1 K-steps ahead of the MMAs (one flat sequence over all passes): every warp
+// copies its own weight rows, and the token chunks, the same for all warps, are copied once
+// by the whole CTA.  One CTA barrier per K-step both publishes a stage and frees the one the
+// next copies refill.  Stage layout (512 B = 32 lanes x 16 B; MMA row g = lane / 4):
+//   per warp w at w * kErWarpBytes: [0, 1024) codes of matrix A (rows g, g + 8),
+//     [1024, 2048) codes of matrix B (gate+up), [2048, 2304) block scales (lane (g, q) stages
+//     row g + 8 (q & 1) of matrix q >> 1);
+//   token chunks at kErBOff: tile t at t * 2048, 16 B per (8-element group c, column j, q) at
+//     c * 512 + (4 j + q) * 16.
 // ------------------------------------------------------------------------------------------
-template <int MODE, int NT, int FMT>
+constexpr int kErWarps = 4;
+constexpr int kErStages = 4;
+constexpr int kErNT = 4;
+constexpr int kErWarpBytes = 2304;
+constexpr int kErBOff = kErWarps * kErWarpBytes;
+constexpr int kErStageBytes = kErBOff + kErNT * 2048;
+constexpr int kErSmemBytes = kErStages * kErStageBytes;
+
+template <int MODE, int FMT>
 __device__ __forceinline__ void expert_rows(const FfnLaunch& L, bool shared, int e, int row0,
-                                            int cnt, int N, int K, int n0) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+                                            int cnt, int N, int K, int n0, uint8_t* ring) {
+    constexpr int NT = kErNT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+    const bool rows_ok = n0 < N;  // a warp past N still copies token chunks and meets barriers
     const int sv = (FMT == MOE_FMT_NVFP4) ? 16 : 32;
+    const int sfb = 128 / sv;  // scale bytes per row and K-step
     const ProjView& PA = MODE == MODE_GATEUP ? (shared ? L.sh_gate : L.gate)
                                              : (shared ? L.sh_down : L.down);
     const ProjView& PB = shared ? L.sh_up : L.up;
     const size_t rowA = (size_t)e * N + n0 + g;
-    const uint8_t* pa0 = PA.packed + rowA * (K / 2) + 16 * q;
-    const uint8_t* pa1 = pa0 + (size_t)8 * (K / 2);
-    const uint8_t* sa0 = PA.scales + rowA * (K / sv);
-    const uint8_t* sa1 = sa0 + (size_t)8 * (K / sv);
-    const uint8_t *pb0 = nullptr, *pb1 = nullptr, *sb0 = nullptr, *sb1 = nullptr;
-    if (MODE == MODE_GATEUP) {
-        pb0 = PB.packed + rowA * (K / 2) + 16 * q;
-        pb1 = pb0 + (size_t)8 * (K / 2);
-        sb0 = PB.scales + rowA * (K / sv);
-        sb1 = sb0 + (size_t)8 * (K / sv);
-    }
+    const uint8_t* pa = rows_ok ? PA.packed + rowA * (K / 2) + 16 * q : nullptr;
+    const uint8_t* pb = (rows_ok && MODE == MODE_GATEUP) ? PB.packed + rowA * (K / 2) + 16 * q : nullptr;
+    const ProjView& PS = (q >> 1) ? PB : PA;  // this lane stages row g + 8 (q & 1) of matrix q >> 1
+    const uint8_t* ps = (rows_ok && (MODE == MODE_GATEUP || q < 2))
+                            ? PS.scales + (rowA + 8 * (q & 1)) * (size_t)(K / sv) : nullptr;
     const int mxa = (FMT == MOE_FMT_MXFP4) ? 112 + PA.mx_off[e] : 0;
     const int mxb = (FMT == MOE_FMT_MXFP4 && MODE == MODE_GATEUP) ? 112 + PB.mx_off[e] : 0;
     const float postA = PA.post[e];
@@ -141,46 +159,95 @@ __device__ __forceinline__ void expert_rows(const FfnLaunch& L, bool shared, int
     const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
     const int P = L.T * L.k;
     const int steps = K / 128;
-
-    for (int c0 = 0; c0 < cnt; c0 += 8 * NT) {
-        // B operand rows (one column per lane group g)
-        const __half* brow[NT];
-        bool bval[NT];
+    const int passes = (cnt + 8 * NT - 1) / (8 * NT);
+    const int total = passes * steps;
+    const size_t rstride = (size_t)8 * (K / 2);  // rows g -> g + 8
+    const uint32_t rbase = smem_addr(ring);
+    // this thread's token chunk: group c = tid / 32, column j = (tid % 32) / 4, q = tid % 4
+    const int bc = tid >> 5, bj = (tid & 31) >> 2, bq = tid & 3;
+    auto b_src = [&](int col) -> const __half* {  // column col of the expert, at K-step 0
+        if (col >= cnt) return nullptr;
+        if (MODE == MODE_GATEUP) {
+            const int tok = shared ? col : L.sorted_pair[row0 + col] / L.k;
+            return L.x16 + (size_t)tok * L.H + 32 * bq + 8 * bc;
+        }
+        const int r = shared ? P + col : row0 + col;
+        return L.h16 + (size_t)r * Imax + 32 * bq + 8 * bc;
+    };
+    int ip = 0, is = 0, issued = 0;  // issue cursor: pass, K-step
+    const __half* ib[NT];
+    auto enter_pass = [&]() {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int col = c0 + nt * 8 + g;
-            bval[nt] = col < cnt;
-            const int cc = bval[nt] ? col : 0;
-            if (MODE == MODE_GATEUP) {
-                const int tok = shared ? cc : L.sorted_pair[row0 + cc] / L.k;
-                brow[nt] = L.x16 + (size_t)tok * L.H + 32 * q;
-            } else {
-                const int r = shared ? P + cc : row0 + cc;
-                brow[nt] = L.h16 + (size_t)r * Imax + 32 * q;
+        for (int t = 0; t < NT; ++t) ib[t] = b_src(ip * 8 * NT + 8 * t + bj);
+    };
+    enter_pass();
+    auto issue = [&]() {
+        if (issued < total) {
+            const uint32_t st = rbase + (issued % kErStages) * kErStageBytes;
+            const uint32_t sw = st + warp * kErWarpBytes;
+            const int o = is * 64;
+            if (pa) {
+                cp_async16(sw + lane * 16, pa + o);
+                cp_async16(sw + 512 + lane * 16, pa + rstride + o);
+            }
+            if (pb) {
+                cp_async16(sw + 1024 + lane * 16, pb + o);
+                cp_async16(sw + 1536 + lane * 16, pb + rstride + o);
+            }
+            if (ps) {
+                if (FMT == MOE_FMT_NVFP4) cp_async8(sw + 2048 + lane * 8, ps + is * sfb);
+                else cp_async4(sw + 2048 + lane * 8, ps + is * sfb);
+            }
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                if (ib[t]) cp_async16(st + kErBOff + t * 2048 + bc * 512 + (tid & 31) * 16, ib[t] + is * 128);
+            if (++is == steps) {
+                is = 0;
+                ++ip;
+                enter_pass();
             }
         }
+        cp_async_commit();
+        ++issued;
+    };
+#pragma unroll 1
+    for (int i = 0; i < kErStages - 1; ++i) issue();
+    int consumed = 0;
+
+    for (int c0 = 0; c0 < cnt; c0 += 8 * NT) {
+        bool bval[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) bval[nt] = c0 + nt * 8 + g < cnt;
         float accA[NT][4], accB[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) { accA[nt][i] = 0.f; accB[nt][i] = 0.f; }
-
-        ChunkA ca, cb;
-        load_chunk<FMT>(ca, pa0, pa1, sa0, sa1, 0, q, mxa);
-        if (MODE == MODE_GATEUP) load_chunk<FMT>(cb, pb0, pb1, sb0, sb1, 0, q, mxb);
         for (int s = 0; s < steps; ++s) {
-            ChunkA na = ca, nb = cb;
-            if (s + 1 < steps) {
-                load_chunk<FMT>(na, pa0, pa1, sa0, sa1, s + 1, q, mxa);
-                if (MODE == MODE_GATEUP) load_chunk<FMT>(nb, pb0, pb1, sb0, sb1, s + 1, q, mxb);
+            cp_async_wait<kErStages - 2>();
+            __syncthreads();  // stage `consumed` is in; every warp is done with the one refilled next
+            issue();
+            const uint8_t* st = ring + (consumed % kErStages) * kErStageBytes;
+            const uint8_t* sw = st + warp * kErWarpBytes;
+            const uint2* sc = reinterpret_cast<const uint2*>(sw + 2048);
+            ChunkA ca, cb;
+            ca.r0 = *reinterpret_cast<const uint4*>(sw + lane * 16);
+            ca.r1 = *reinterpret_cast<const uint4*>(sw + 512 + lane * 16);
+            scales_from_raw<FMT>(sc[g * 4 + 0], q, mxa, ca.s0lo, ca.s0hi);
+            scales_from_raw<FMT>(sc[g * 4 + 1], q, mxa, ca.s1lo, ca.s1hi);
+            if (MODE == MODE_GATEUP) {
+                cb.r0 = *reinterpret_cast<const uint4*>(sw + 1024 + lane * 16);
+                cb.r1 = *reinterpret_cast<const uint4*>(sw + 1536 + lane * 16);
+                scales_from_raw<FMT>(sc[g * 4 + 2], q, mxb, cb.s0lo, cb.s0hi);
+                scales_from_raw<FMT>(sc[g * 4 + 3], q, mxb, cb.s1lo, cb.s1hi);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                if (c0 + nt * 8 >= cnt) break;  // warp-uniform
+                if (!rows_ok || c0 + nt * 8 >= cnt) break;  // warp-uniform
                 uint4 b[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    b[j] = bval[nt] ? ldg_cached128(brow[nt] + s * 128 + 8 * j)
+                    b[j] = bval[nt] ? *reinterpret_cast<const uint4*>(st + kErBOff + nt * 2048 + j * 512 + lane * 16)
                                     : make_uint4(0, 0, 0, 0);
 #define MOE_STEP(I)                                                                   \
     {                                                                                 \
@@ -199,9 +266,9 @@ __device__ __forceinline__ void expert_rows(const FfnLaunch& L, bool shared, int
                 MOE_STEP(4) MOE_STEP(5) MOE_STEP(6) MOE_STEP(7)
 #undef MOE_STEP
             }
-            ca = na;
-            cb = nb;
+            ++consumed;
         }
+        if (!rows_ok) continue;
 
         // ---- epilogue ----
 #pragma unroll
@@ -259,9 +326,10 @@ __device__ __forceinline__ void expert_rows(const FfnLaunch& L, bool shared, int
     }
 }
 
-template <int MODE, int NT, int WARPS, int FMT_R, int FMT_S>
-__global__ void __launch_bounds__(WARPS * 32)
+template <int MODE, int FMT_R, int FMT_S>
+__global__ void __launch_bounds__(kErWarps * 32)
 expert_mma_kernel(FfnLaunch L, int max_routed_slots) {
+    extern __shared__ __align__(16) uint8_t er_smem[];
     const int slot = blockIdx.y;
     const bool shared = slot == max_routed_slots;
     int e, row0, cnt;
@@ -270,7 +338,7 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots) {
         row0 = 0;
         cnt = L.T;
     } else {
-        if (slot >= L.meta[0]) return;
+        if (slot >= L.meta[0]) return;  // CTA-uniform
         e = L.active[slot];
         row0 = L.offsets[e];
         cnt = L.offsets[e + 1] - row0;
@@ -278,10 +346,10 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots) {
     const int Iexp = shared ? L.I_shared : L.I;
     const int N = MODE == MODE_GATEUP ? Iexp : L.H;
     const int K = MODE == MODE_GATEUP ? L.H : Iexp;
-    const int n0 = (blockIdx.x * WARPS + (threadIdx.x >> 5)) * 16;
-    if (n0 >= N) return;
-    if (shared) expert_rows<MODE, NT, FMT_S>(L, true, e, row0, cnt, N, K, n0);
-    else expert_rows<MODE, NT, FMT_R>(L, false, e, row0, cnt, N, K, n0);
+    if (blockIdx.x * kErWarps * 16 >= N) return;  // CTA-uniform
+    const int n0 = (blockIdx.x * kErWarps + (threadIdx.x >> 5)) * 16;
+    if (shared) expert_rows<MODE, FMT_S>(L, true, e, row0, cnt, N, K, n0, er_smem);
+    else expert_rows<MODE, FMT_R>(L, false, e, row0, cnt, N, K, n0, er_smem);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -373,34 +441,30 @@ cudaError_t record_phase_event(cudaEvent_t ev, cudaStream_t st) {
                : cudaEventRecord(ev, st);
 }
 
-template <int MODE, int NT, int FR, int FS>
-static void launch_expert_gemm(const FfnLaunch& L, int slots_r, cudaStream_t st) {
-    constexpr int WARPS = 4;
+template <int MODE, int FR, int FS>
+static cudaError_t launch_expert_gemm(const FfnLaunch& L, int slots_r, cudaStream_t st) {
     const int slots = slots_r + (L.I_shared > 0 ? 1 : 0);
     const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
     const int N = MODE == MODE_GATEUP ? Imax : L.H;
-    dim3 grid((N / 16 + WARPS - 1) / WARPS, slots);
-    expert_mma_kernel<MODE, NT, WARPS, FR, FS><<<grid, WARPS * 32, 0, st>>>(L, slots_r);
-}
-
-template <int MODE, int NT>
-static void launch_expert_gemm_fmt(const FfnLaunch& L, int slots_r, cudaStream_t st) {
-    const int fr = L.gate.fmt;
-    const int fs = L.I_shared > 0 ? L.sh_gate.fmt : fr;
-    if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_NVFP4)
-        launch_expert_gemm<MODE, NT, MOE_FMT_NVFP4, MOE_FMT_NVFP4>(L, slots_r, st);
-    else if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_MXFP4)
-        launch_expert_gemm<MODE, NT, MOE_FMT_NVFP4, MOE_FMT_MXFP4>(L, slots_r, st);
-    else if (fr == MOE_FMT_MXFP4 && fs == MOE_FMT_NVFP4)
-        launch_expert_gemm<MODE, NT, MOE_FMT_MXFP4, MOE_FMT_NVFP4>(L, slots_r, st);
-    else
-        launch_expert_gemm<MODE, NT, MOE_FMT_MXFP4, MOE_FMT_MXFP4>(L, slots_r, st);
+    auto kern = expert_mma_kernel<MODE, FR, FS>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kErSmemBytes);
+    if (err != cudaSuccess) return err;
+    dim3 grid((N / 16 + kErWarps - 1) / kErWarps, slots);
+    kern<<<grid, kErWarps * 32, kErSmemBytes, st>>>(L, slots_r);
+    return cudaGetLastError();
 }
 
 template <int MODE>
-static void launch_expert_phase(const FfnLaunch& L, int slots_r, cudaStream_t st) {
-    if (L.T <= 8) launch_expert_gemm_fmt<MODE, 1>(L, slots_r, st);
-    else launch_expert_gemm_fmt<MODE, 4>(L, slots_r, st);
+static cudaError_t launch_expert_phase(const FfnLaunch& L, int slots_r, cudaStream_t st) {
+    const int fr = L.gate.fmt;
+    const int fs = L.I_shared > 0 ? L.sh_gate.fmt : fr;
+    if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_NVFP4)
+        return launch_expert_gemm<MODE, MOE_FMT_NVFP4, MOE_FMT_NVFP4>(L, slots_r, st);
+    if (fr == MOE_FMT_NVFP4 && fs == MOE_FMT_MXFP4)
+        return launch_expert_gemm<MODE, MOE_FMT_NVFP4, MOE_FMT_MXFP4>(L, slots_r, st);
+    if (fr == MOE_FMT_MXFP4 && fs == MOE_FMT_NVFP4)
+        return launch_expert_gemm<MODE, MOE_FMT_MXFP4, MOE_FMT_NVFP4>(L, slots_r, st);
+    return launch_expert_gemm<MODE, MOE_FMT_MXFP4, MOE_FMT_MXFP4>(L, slots_r, st);
 }
 
 cudaError_t launch_ffn(const FfnLaunch& L, cudaStream_t st, const PhaseEvents* ev) {
