@@ -21,6 +21,8 @@
 // expert's routed pairs (8 per m16n8k16 MMA tile), so each weight row is read once per
 // launch whatever the number of tokens routed to the expert.  Activations enter as f16
 // (bf16 tokens converted once; the NVFP4-quantized tokens and h are exact in f16).
+#include <type_traits>
+
 #include "common.cuh"
 #include "frag.cuh"
 #include "kernels.h"
@@ -135,76 +137,125 @@ constexpr int kErBOff = kErWarps * kErWarpBytes;
 constexpr int kErStageBytes = kErBOff + kErNT * 2048;
 constexpr int kErSmemBytes = kErStages * kErStageBytes;
 
-template <int MODE, int FMT>
-__device__ __forceinline__ void expert_rows(const FfnLaunch& L, bool shared, int e, int row0,
-                                            int cnt, int N, int K, int n0, uint8_t* ring) {
+// Work item it = (slot, 64-row block): its expert, tokens and matrix shape, or invalid.
+struct ErItem {
+    bool valid, shared;
+    int e, row0, cnt, N, K;
+};
+template <int MODE>
+__device__ __forceinline__ ErItem er_item(const FfnLaunch& L, int max_routed_slots, int xblocks,
+                                          int it) {
+    ErItem w{};
+    const int slot = it / xblocks, xb = it - slot * xblocks;
+    w.shared = slot == max_routed_slots;
+    if (w.shared) {
+        w.e = 0;
+        w.row0 = 0;
+        w.cnt = L.T;
+    } else {
+        if (slot >= L.meta[0]) return w;
+        w.e = L.active[slot];
+        w.row0 = L.offsets[w.e];
+        w.cnt = L.offsets[w.e + 1] - w.row0;
+    }
+    const int Iexp = w.shared ? L.I_shared : L.I;
+    w.N = MODE == MODE_GATEUP ? Iexp : L.H;
+    w.K = MODE == MODE_GATEUP ? L.H : Iexp;
+    w.valid = xb * kErWarps * 16 < w.N && w.cnt > 0;
+    return w;
+}
+
+template <int MODE, int FR, int FS>
+__global__ void __launch_bounds__(kErWarps * 32)
+expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
+    extern __shared__ __align__(16) uint8_t er_smem[];
     constexpr int NT = kErNT;
+    uint8_t* ring = er_smem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
-    const bool rows_ok = n0 < N;  // a warp past N still copies token chunks and meets barriers
-    const int sv = (FMT == MOE_FMT_NVFP4) ? 16 : 32;
-    const int sfb = 128 / sv;  // scale bytes per row and K-step
-    const ProjView& PA = MODE == MODE_GATEUP ? (shared ? L.sh_gate : L.gate)
-                                             : (shared ? L.sh_down : L.down);
-    const ProjView& PB = shared ? L.sh_up : L.up;
-    const size_t rowA = (size_t)e * N + n0 + g;
-    const uint8_t* pa = rows_ok ? PA.packed + rowA * (K / 2) + 16 * q : nullptr;
-    const uint8_t* pb = (rows_ok && MODE == MODE_GATEUP) ? PB.packed + rowA * (K / 2) + 16 * q : nullptr;
-    const ProjView& PS = (q >> 1) ? PB : PA;  // this lane stages row g + 8 (q & 1) of matrix q >> 1
-    const uint8_t* ps = (rows_ok && (MODE == MODE_GATEUP || q < 2))
-                            ? PS.scales + (rowA + 8 * (q & 1)) * (size_t)(K / sv) : nullptr;
-    const int mxa = (FMT == MOE_FMT_MXFP4) ? 112 + PA.mx_off[e] : 0;
-    const int mxb = (FMT == MOE_FMT_MXFP4 && MODE == MODE_GATEUP) ? 112 + PB.mx_off[e] : 0;
-    const float postA = PA.post[e];
-    const float postB = (MODE == MODE_GATEUP) ? PB.post[e] : 1.f;
     const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
     const int P = L.T * L.k;
-    const int steps = K / 128;
-    const int passes = (cnt + 8 * NT - 1) / (8 * NT);
-    const int total = passes * steps;
-    const size_t rstride = (size_t)8 * (K / 2);  // rows g -> g + 8
     const uint32_t rbase = smem_addr(ring);
     // this thread's token chunk: group c = tid / 32, column j = (tid % 32) / 4, q = tid % 4
     const int bc = tid >> 5, bj = (tid & 31) >> 2, bq = tid & 3;
-    auto b_src = [&](int col) -> const __half* {  // column col of the expert, at K-step 0
-        if (col >= cnt) return nullptr;
+    auto b_src = [&](const ErItem& w, int col) -> const __half* {  // column col, K-step 0
+        if (col >= w.cnt) return nullptr;
         if (MODE == MODE_GATEUP) {
-            const int tok = shared ? col : L.sorted_pair[row0 + col] / L.k;
+            const int tok = w.shared ? col : L.sorted_pair[w.row0 + col] / L.k;
             return L.x16 + (size_t)tok * L.H + 32 * bq + 8 * bc;
         }
-        const int r = shared ? P + col : row0 + col;
+        const int r = w.shared ? P + col : w.row0 + col;
         return L.h16 + (size_t)r * Imax + 32 * bq + 8 * bc;
     };
-    int ip = 0, is = 0, issued = 0;  // issue cursor: pass, K-step
+
+    // ---- issue cursor: item, pass, K-step; one flat sequence over this CTA's items ----
+    int ci = blockIdx.x, ip = 0, is = 0;
+    ErItem cw{};
+    int c_steps = 1, c_passes = 0, c_sfb = 8;
+    size_t c_rstride = 0;
+    const uint8_t *pa = nullptr, *pb = nullptr, *ps = nullptr;
     const __half* ib[NT];
     auto enter_pass = [&]() {
 #pragma unroll
-        for (int t = 0; t < NT; ++t) ib[t] = b_src(ip * 8 * NT + 8 * t + bj);
+        for (int t = 0; t < NT; ++t) ib[t] = b_src(cw, ip * 8 * NT + 8 * t + bj);
     };
-    enter_pass();
+    auto enter_item = [&]() {  // the first valid item at or after ci
+        for (; ci < items; ci += gridDim.x) {
+            cw = er_item<MODE>(L, max_routed_slots, xblocks, ci);
+            if (cw.valid) break;
+        }
+        if (ci >= items) return;
+        const int fmt = cw.shared ? FS : FR;
+        const int sv = fmt == MOE_FMT_NVFP4 ? 16 : 32;
+        c_sfb = 128 / sv;
+        c_steps = cw.K / 128;
+        c_passes = (cw.cnt + 8 * NT - 1) / (8 * NT);
+        c_rstride = (size_t)8 * (cw.K / 2);
+        const int xb = ci % xblocks;
+        const int n0 = (xb * kErWarps + warp) * 16;
+        const bool rows_ok = n0 < cw.N;
+        const ProjView& PA = MODE == MODE_GATEUP ? (cw.shared ? L.sh_gate : L.gate)
+                                                 : (cw.shared ? L.sh_down : L.down);
+        const ProjView& PB = cw.shared ? L.sh_up : L.up;
+        const size_t rowA = (size_t)cw.e * cw.N + n0 + g;
+        pa = rows_ok ? PA.packed + rowA * (cw.K / 2) + 16 * q : nullptr;
+        pb = (rows_ok && MODE == MODE_GATEUP) ? PB.packed + rowA * (cw.K / 2) + 16 * q : nullptr;
+        const ProjView& PS = (q >> 1) ? PB : PA;  // row g + 8 (q & 1) of matrix q >> 1
+        ps = (rows_ok && (MODE == MODE_GATEUP || q < 2))
+                 ? PS.scales + (rowA + 8 * (q & 1)) * (size_t)(cw.K / sv) : nullptr;
+        ip = 0;
+        is = 0;
+        enter_pass();
+    };
+    enter_item();
+    int issued = 0;
     auto issue = [&]() {
-        if (issued < total) {
+        if (ci < items) {
             const uint32_t st = rbase + (issued % kErStages) * kErStageBytes;
             const uint32_t sw = st + warp * kErWarpBytes;
             const int o = is * 64;
             if (pa) {
                 cp_async16(sw + lane * 16, pa + o);
-                cp_async16(sw + 512 + lane * 16, pa + rstride + o);
+                cp_async16(sw + 512 + lane * 16, pa + c_rstride + o);
             }
             if (pb) {
                 cp_async16(sw + 1024 + lane * 16, pb + o);
-                cp_async16(sw + 1536 + lane * 16, pb + rstride + o);
+                cp_async16(sw + 1536 + lane * 16, pb + c_rstride + o);
             }
             if (ps) {
-                if (FMT == MOE_FMT_NVFP4) cp_async8(sw + 2048 + lane * 8, ps + is * sfb);
-                else cp_async4(sw + 2048 + lane * 8, ps + is * sfb);
+                if (c_sfb == 8) cp_async8(sw + 2048 + lane * 8, ps + is * c_sfb);
+                else cp_async4(sw + 2048 + lane * 8, ps + is * c_sfb);
             }
 #pragma unroll
             for (int t = 0; t < NT; ++t)
                 if (ib[t]) cp_async16(st + kErBOff + t * 2048 + bc * 512 + (tid & 31) * 16, ib[t] + is * 128);
-            if (++is == steps) {
+            if (++is == c_steps) {
                 is = 0;
-                ++ip;
-                enter_pass();
+                if (++ip == c_passes) {
+                    ci += gridDim.x;
+                    enter_item();
+                } else {
+                    enter_pass();
+                }
             }
         }
         cp_async_commit();
@@ -214,142 +265,139 @@ __device__ __forceinline__ void expert_rows(const FfnLaunch& L, bool shared, int
     for (int i = 0; i < kErStages - 1; ++i) issue();
     int consumed = 0;
 
-    for (int c0 = 0; c0 < cnt; c0 += 8 * NT) {
-        bool bval[NT];
+    // ---- consumer: the same items, passes and K-steps in the same order ----
+    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+        const ErItem w = er_item<MODE>(L, max_routed_slots, xblocks, it);
+        if (!w.valid) continue;  // CTA-uniform
+        const bool shared = w.shared;
+        const int e = w.e, row0 = w.row0, cnt = w.cnt, N = w.N, K = w.K;
+        const int n0 = ((it % xblocks) * kErWarps + warp) * 16;
+        const bool rows_ok = n0 < N;
+        const int steps = K / 128;
+        auto body = [&](auto fmt_c) {
+            constexpr int FMT = decltype(fmt_c)::value;
+            const ProjView& PA = MODE == MODE_GATEUP ? (shared ? L.sh_gate : L.gate)
+                                                     : (shared ? L.sh_down : L.down);
+            const ProjView& PB = shared ? L.sh_up : L.up;
+            const int mxa = (FMT == MOE_FMT_MXFP4) ? 112 + PA.mx_off[e] : 0;
+            const int mxb = (FMT == MOE_FMT_MXFP4 && MODE == MODE_GATEUP) ? 112 + PB.mx_off[e] : 0;
+            const float postA = PA.post[e];
+            const float postB = (MODE == MODE_GATEUP) ? PB.post[e] : 1.f;
+            for (int c0 = 0; c0 < cnt; c0 += 8 * NT) {
+                bool bval[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) bval[nt] = c0 + nt * 8 + g < cnt;
-        float accA[NT][4], accB[NT][4];
+                for (int nt = 0; nt < NT; ++nt) bval[nt] = c0 + nt * 8 + g < cnt;
+                float accA[NT][4], accB[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) { accA[nt][i] = 0.f; accB[nt][i] = 0.f; }
-        for (int s = 0; s < steps; ++s) {
-            cp_async_wait<kErStages - 2>();
-            __syncthreads();  // stage `consumed` is in; every warp is done with the one refilled next
-            issue();
-            const uint8_t* st = ring + (consumed % kErStages) * kErStageBytes;
-            const uint8_t* sw = st + warp * kErWarpBytes;
-            const uint2* sc = reinterpret_cast<const uint2*>(sw + 2048);
-            ChunkA ca, cb;
-            ca.r0 = *reinterpret_cast<const uint4*>(sw + lane * 16);
-            ca.r1 = *reinterpret_cast<const uint4*>(sw + 512 + lane * 16);
-            scales_from_raw<FMT>(sc[g * 4 + 0], q, mxa, ca.s0lo, ca.s0hi);
-            scales_from_raw<FMT>(sc[g * 4 + 1], q, mxa, ca.s1lo, ca.s1hi);
-            if (MODE == MODE_GATEUP) {
-                cb.r0 = *reinterpret_cast<const uint4*>(sw + 1024 + lane * 16);
-                cb.r1 = *reinterpret_cast<const uint4*>(sw + 1536 + lane * 16);
-                scales_from_raw<FMT>(sc[g * 4 + 2], q, mxb, cb.s0lo, cb.s0hi);
-                scales_from_raw<FMT>(sc[g * 4 + 3], q, mxb, cb.s1lo, cb.s1hi);
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                if (!rows_ok || c0 + nt * 8 >= cnt) break;  // warp-uniform
-                uint4 b[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    b[j] = bval[nt] ? *reinterpret_cast<const uint4*>(st + kErBOff + nt * 2048 + j * 512 + lane * 16)
-                                    : make_uint4(0, 0, 0, 0);
-#define MOE_STEP(I)                                                                   \
-    {                                                                                 \
-        uint32_t fa[4];                                                               \
-        frag_a<I>(ca, fa);                                                            \
-        const uint32_t b0 = word_of(b[I >> 1], (I & 1) * 2);                          \
-        const uint32_t b1 = word_of(b[I >> 1], (I & 1) * 2 + 1);                      \
-        mma_f16_16816(accA[nt], fa[0], fa[1], fa[2], fa[3], b0, b1);                  \
-        if (MODE == MODE_GATEUP) {                                                    \
-            uint32_t fb[4];                                                           \
-            frag_a<I>(cb, fb);                                                        \
-            mma_f16_16816(accB[nt], fb[0], fb[1], fb[2], fb[3], b0, b1);              \
-        }                                                                             \
-    }
-                MOE_STEP(0) MOE_STEP(1) MOE_STEP(2) MOE_STEP(3)
-                MOE_STEP(4) MOE_STEP(5) MOE_STEP(6) MOE_STEP(7)
-#undef MOE_STEP
-            }
-            ++consumed;
-        }
-        if (!rows_ok) continue;
-
-        // ---- epilogue ----
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            if (c0 + nt * 8 >= cnt) break;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int col = c0 + nt * 8 + 2 * q + j;
-                const bool valid = col < cnt;
-                const int r = shared ? P + col : row0 + col;
-                if (MODE == MODE_GATEUP) {
-                    const float h0 = silu_f32(accA[nt][j] * postA) * (accB[nt][j] * postB);
-                    const float h1 = silu_f32(accA[nt][2 + j] * postA) * (accB[nt][2 + j] * postB);
-                    if (L.act == MOE_ACT_NVFP4) {
-                        // quantize h over the 16 consecutive rows n0..n0+15 of this column
-                        float amax = fmaxf(fabsf(h0), fabsf(h1));
-                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
-                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-                        float qs = amax / 6.0f;
-                        qs = qs / L.g2;
-                        const uint32_t sbyte = f32_to_e4m3(qs);
-                        const float denom = e4m3_to_f32(sbyte) * L.g2;
-                        uint32_t c0b = 0, c1b = 0;
-                        if (denom != 0.f) {
-                            c0b = f32x2_to_e2m1x2(h0 / denom, 0.f) & 0xF;
-                            c1b = f32x2_to_e2m1x2(h1 / denom, 0.f) & 0xF;
-                        }
-                        const uint32_t n0c = __shfl_down_sync(0xffffffffu, c0b, 4);
-                        const uint32_t n1c = __shfl_down_sync(0xffffffffu, c1b, 4);
-                        if (valid) {
-                            __half* hrow = L.h16 + (size_t)r * Imax + n0;
-                            hrow[g] = __float2half_rn(e2m1_to_f32(c0b) * denom);
-                            hrow[g + 8] = __float2half_rn(e2m1_to_f32(c1b) * denom);
-                            uint8_t* qrow = L.hq + (size_t)r * (Imax / 2) + n0 / 2;
-                            if ((g & 1) == 0) {
-                                qrow[g / 2] = (uint8_t)(c0b | (n0c << 4));
-                                qrow[(g + 8) / 2] = (uint8_t)(c1b | (n1c << 4));
-                            }
-                            if (g == 0) L.hs[(size_t)r * (Imax / 16) + n0 / 16] = (uint8_t)sbyte;
-                        }
-                    } else if (valid) {
-                        __half* hrow = L.h16 + (size_t)r * Imax + n0;
-                        hrow[g] = __float2half_rn(h0);
-                        hrow[g + 8] = __float2half_rn(h1);
+                    for (int i = 0; i < 4; ++i) { accA[nt][i] = 0.f; accB[nt][i] = 0.f; }
+                for (int s = 0; s < steps; ++s) {
+                    cp_async_wait<kErStages - 2>();
+                    __syncthreads();  // stage `consumed` is in; every warp is done with the one refilled next
+                    issue();
+                    const uint8_t* st = ring + (consumed % kErStages) * kErStageBytes;
+                    const uint8_t* sw = st + warp * kErWarpBytes;
+                    const uint2* sc = reinterpret_cast<const uint2*>(sw + 2048);
+                    ChunkA ca, cb;
+                    ca.r0 = *reinterpret_cast<const uint4*>(sw + lane * 16);
+                    ca.r1 = *reinterpret_cast<const uint4*>(sw + 512 + lane * 16);
+                    scales_from_raw<FMT>(sc[g * 4 + 0], q, mxa, ca.s0lo, ca.s0hi);
+                    scales_from_raw<FMT>(sc[g * 4 + 1], q, mxa, ca.s1lo, ca.s1hi);
+                    if (MODE == MODE_GATEUP) {
+                        cb.r0 = *reinterpret_cast<const uint4*>(sw + 1024 + lane * 16);
+                        cb.r1 = *reinterpret_cast<const uint4*>(sw + 1536 + lane * 16);
+                        scales_from_raw<FMT>(sc[g * 4 + 2], q, mxb, cb.s0lo, cb.s0hi);
+                        scales_from_raw<FMT>(sc[g * 4 + 3], q, mxb, cb.s1lo, cb.s1hi);
                     }
-                } else if (valid) {
-                    const float wcol = shared ? 1.f : L.w[L.sorted_pair[row0 + col]];
-                    float* yrow = L.y + (size_t)r * L.H + n0;
-                    yrow[g] = accA[nt][j] * postA * wcol;
-                    yrow[g + 8] = accA[nt][2 + j] * postA * wcol;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (!rows_ok || c0 + nt * 8 >= cnt) break;  // warp-uniform
+                        uint4 b[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            b[j] = bval[nt] ? *reinterpret_cast<const uint4*>(st + kErBOff + nt * 2048 + j * 512 + lane * 16)
+                                            : make_uint4(0, 0, 0, 0);
+#define MOE_STEP(I)                                                                   \
+            {                                                                                 \
+                uint32_t fa[4];                                                               \
+                frag_a<I>(ca, fa);                                                            \
+                const uint32_t b0 = word_of(b[I >> 1], (I & 1) * 2);                          \
+                const uint32_t b1 = word_of(b[I >> 1], (I & 1) * 2 + 1);                      \
+                mma_f16_16816(accA[nt], fa[0], fa[1], fa[2], fa[3], b0, b1);                  \
+                if (MODE == MODE_GATEUP) {                                                    \
+                    uint32_t fb[4];                                                           \
+                    frag_a<I>(cb, fb);                                                        \
+                    mma_f16_16816(accB[nt], fb[0], fb[1], fb[2], fb[3], b0, b1);              \
+                }                                                                             \
+            }
+                        MOE_STEP(0) MOE_STEP(1) MOE_STEP(2) MOE_STEP(3)
+                        MOE_STEP(4) MOE_STEP(5) MOE_STEP(6) MOE_STEP(7)
+#undef MOE_STEP
+                    }
+                    ++consumed;
+                }
+                if (!rows_ok) continue;
+
+                // ---- epilogue ----
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (c0 + nt * 8 >= cnt) break;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int col = c0 + nt * 8 + 2 * q + j;
+                        const bool valid = col < cnt;
+                        const int r = shared ? P + col : row0 + col;
+                        if (MODE == MODE_GATEUP) {
+                            const float h0 = silu_f32(accA[nt][j] * postA) * (accB[nt][j] * postB);
+                            const float h1 = silu_f32(accA[nt][2 + j] * postA) * (accB[nt][2 + j] * postB);
+                            if (L.act == MOE_ACT_NVFP4) {
+                                // quantize h over the 16 consecutive rows n0..n0+15 of this column
+                                float amax = fmaxf(fabsf(h0), fabsf(h1));
+                                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+                                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+                                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+                                float qs = amax / 6.0f;
+                                qs = qs / L.g2;
+                                const uint32_t sbyte = f32_to_e4m3(qs);
+                                const float denom = e4m3_to_f32(sbyte) * L.g2;
+                                uint32_t c0b = 0, c1b = 0;
+                                if (denom != 0.f) {
+                                    c0b = f32x2_to_e2m1x2(h0 / denom, 0.f) & 0xF;
+                                    c1b = f32x2_to_e2m1x2(h1 / denom, 0.f) & 0xF;
+                                }
+                                const uint32_t n0c = __shfl_down_sync(0xffffffffu, c0b, 4);
+                                const uint32_t n1c = __shfl_down_sync(0xffffffffu, c1b, 4);
+                                if (valid) {
+                                    __half* hrow = L.h16 + (size_t)r * Imax + n0;
+                                    hrow[g] = __float2half_rn(e2m1_to_f32(c0b) * denom);
+                                    hrow[g + 8] = __float2half_rn(e2m1_to_f32(c1b) * denom);
+                                    uint8_t* qrow = L.hq + (size_t)r * (Imax / 2) + n0 / 2;
+                                    if ((g & 1) == 0) {
+                                        qrow[g / 2] = (uint8_t)(c0b | (n0c << 4));
+                                        qrow[(g + 8) / 2] = (uint8_t)(c1b | (n1c << 4));
+                                    }
+                                    if (g == 0) L.hs[(size_t)r * (Imax / 16) + n0 / 16] = (uint8_t)sbyte;
+                                }
+                            } else if (valid) {
+                                __half* hrow = L.h16 + (size_t)r * Imax + n0;
+                                hrow[g] = __float2half_rn(h0);
+                                hrow[g + 8] = __float2half_rn(h1);
+                            }
+                        } else if (valid) {
+                            const float wcol = shared ? 1.f : L.w[L.sorted_pair[row0 + col]];
+                            float* yrow = L.y + (size_t)r * L.H + n0;
+                            yrow[g] = accA[nt][j] * postA * wcol;
+                            yrow[g + 8] = accA[nt][2 + j] * postA * wcol;
+                        }
+                    }
                 }
             }
-        }
+        };
+        if (shared) body(std::integral_constant<int, FS>{});
+        else body(std::integral_constant<int, FR>{});
     }
-}
-
-template <int MODE, int FMT_R, int FMT_S>
-__global__ void __launch_bounds__(kErWarps * 32)
-expert_mma_kernel(FfnLaunch L, int max_routed_slots) {
-    extern __shared__ __align__(16) uint8_t er_smem[];
-    const int slot = blockIdx.y;
-    const bool shared = slot == max_routed_slots;
-    int e, row0, cnt;
-    if (shared) {
-        e = 0;
-        row0 = 0;
-        cnt = L.T;
-    } else {
-        if (slot >= L.meta[0]) return;  // CTA-uniform
-        e = L.active[slot];
-        row0 = L.offsets[e];
-        cnt = L.offsets[e + 1] - row0;
-    }
-    const int Iexp = shared ? L.I_shared : L.I;
-    const int N = MODE == MODE_GATEUP ? Iexp : L.H;
-    const int K = MODE == MODE_GATEUP ? L.H : Iexp;
-    if (blockIdx.x * kErWarps * 16 >= N) return;  // CTA-uniform
-    const int n0 = (blockIdx.x * kErWarps + (threadIdx.x >> 5)) * 16;
-    if (shared) expert_rows<MODE, FMT_S>(L, true, e, row0, cnt, N, K, n0, er_smem);
-    else expert_rows<MODE, FMT_R>(L, false, e, row0, cnt, N, K, n0, er_smem);
+    cp_async_wait<0>();  // nothing may be in flight into shared memory when the CTA exits
 }
 
 // ------------------------------------------------------------------------------------------
@@ -449,8 +497,18 @@ static cudaError_t launch_expert_gemm(const FfnLaunch& L, int slots_r, cudaStrea
     auto kern = expert_mma_kernel<MODE, FR, FS>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kErSmemBytes);
     if (err != cudaSuccess) return err;
-    dim3 grid((N / 16 + kErWarps - 1) / kErWarps, slots);
-    kern<<<grid, kErWarps * 32, kErSmemBytes, st>>>(L, slots_r);
+    int per_sm = 0, dev = 0, sms = 0;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kErWarps * 32, kErSmemBytes)) != cudaSuccess)
+        return err;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    // persistent CTAs: work items (slot, 64-row block) strided by the grid, slot-major so that
+    // concurrently running CTAs read neighbouring rows of one expert
+    const int xblocks = (N / 16 + kErWarps - 1) / kErWarps;
+    const int items = xblocks * slots;
+    int grid = (per_sm > 0 ? per_sm : 1) * sms;
+    if (grid > items) grid = items;
+    kern<<<grid, kErWarps * 32, kErSmemBytes, st>>>(L, slots_r, xblocks, items);
     return cudaGetLastError();
 }
 
