@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(512) prep_kernel(FfnLaunch L) {
 //     c * 512 + (4 j + q) * 16.
 // ------------------------------------------------------------------------------------------
 constexpr int kErWarps = 4;
-constexpr int kErStages = 4;
+constexpr int kErStages = 3;
 constexpr int kErNT = 4;
 constexpr int kErWarpBytes = 2304;
 constexpr int kErBOff = kErWarps * kErWarpBytes;
