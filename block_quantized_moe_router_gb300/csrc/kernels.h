@@ -66,6 +66,8 @@ struct TcWeights {
     CUtensorMap gate, up, down, sh_gate, sh_up, sh_down;
     uint8_t *sf_gate = nullptr, *sf_up = nullptr, *sf_down = nullptr;
     uint8_t *sf_sh_gate = nullptr, *sf_sh_up = nullptr, *sf_sh_down = nullptr;
+    // B-operand scales as pair tiles (two 128-row tiles interleaved per 64-element K block)
+    uint8_t *sfp_gu = nullptr, *sfp_dn = nullptr, *sfp_sh_gu = nullptr, *sfp_sh_dn = nullptr;
     // per-expert post-scales seen by the MMA path: the NVFP4 globals, or for MXFP4 the power of
     // two left over after the E8M0 scales were re-expressed as E4M3 (owned when MXFP4)
     const float *post_gate = nullptr, *post_up = nullptr, *post_down = nullptr;
@@ -107,6 +109,7 @@ struct TcGemmParams {
     const uint8_t* sfa;
     int sfa_kblocks;
     const uint8_t *sfb0, *sfb1, *ssfb0, *ssfb1;
+    const uint8_t *sfr, *ssfr;  // B's scales as replicated pair tiles (routed, shared)
     const float *post0, *post1, *spost0, *spost1;
     const float* topk_w;
     uint8_t *hq, *hsf;
