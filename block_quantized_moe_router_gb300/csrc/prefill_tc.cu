@@ -460,18 +460,19 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
             } else {
                 const float pd = (sh ? p.spost0 : p.post0)[es];
                 const float sc = pd * (pair < p.P ? p.topk_w[pair] : 1.f);
-                uint4* dst = reinterpret_cast<uint4*>(p.y + (size_t)pair * p.H + nb * 256 + 128 * half);
+                // 32-byte stores (the row segment is 256 B, 32-byte aligned): half as many
+                // scattered store transactions as 16-byte ones
+                __nv_bfloat16* dst = p.y + (size_t)pair * p.H + nb * 256 + 128 * half;
 #pragma unroll
-                for (int c = 0; c < 128; c += 8) {
-                    uint4 o;
-                    uint32_t* ow = &o.x;
+                for (int c = 0; c < 128; c += 16) {
+                    uint32_t ow[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < 8; ++i) {
                         __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(V[c + 2 * i]) * sc,
                                                                  __uint_as_float(V[c + 2 * i + 1]) * sc);
                         ow[i] = *reinterpret_cast<uint32_t*>(&v);
                     }
-                    dst[c / 8] = o;
+                    st_global_v8(dst + c, ow);
                 }
             }
         }
