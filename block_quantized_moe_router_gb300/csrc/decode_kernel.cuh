@@ -592,9 +592,10 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             ic_ns = K / 128;
         }
     };
+    const uint64_t wpol = l2_evict_first_policy();  // expert weights are read once per launch
     auto copy_scales = [&](uint32_t dst, const uint8_t* src) {
-        if (ic_sfb == 8) cp_async8(dst, src);
-        else cp_async4(dst, src);
+        if (ic_sfb == 8) cp_async8_pol(dst, src, wpol);
+        else cp_async4_pol(dst, src, wpol);
     };
     ic_enter();
     int issued = 0;
@@ -607,8 +608,8 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const size_t ro = (size_t)(16 * t + 8 * r) * ic_rb + o;
-                    cp_async16(st + (4 * t + r) * 512 + lane * 16, ic_c0 + ro);
-                    cp_async16(st + (4 * t + 2 + r) * 512 + lane * 16, ic_c1 + ro);
+                    cp_async16_pol(st + (4 * t + r) * 512 + lane * 16, ic_c0 + ro, wpol);
+                    cp_async16_pol(st + (4 * t + 2 + r) * 512 + lane * 16, ic_c1 + ro, wpol);
                 }
                 copy_scales(st + Geo::kGuSc + t * 256 + lane * 8, ic_sp + 16 * t * ic_rs + ic_s * ic_sfb);
             }
@@ -627,8 +628,8 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             const int nst = ic_ns - ic_s < 2 ? 1 : 2;
             for (int u = 0; u < nst; ++u) {
                 const int o = (ic_s + u) * 64;
-                cp_async16(st + Geo::kDnCodes + (2 * u) * 512 + lane * 16, ic_c0 + o);
-                cp_async16(st + Geo::kDnCodes + (2 * u + 1) * 512 + lane * 16, ic_c0 + 8 * ic_rb + o);
+                cp_async16_pol(st + Geo::kDnCodes + (2 * u) * 512 + lane * 16, ic_c0 + o, wpol);
+                cp_async16_pol(st + Geo::kDnCodes + (2 * u + 1) * 512 + lane * 16, ic_c0 + 8 * ic_rb + o, wpol);
                 if (q < 2) copy_scales(st + Geo::kDnSc + u * 256 + lane * 8, ic_sp + (ic_s + u) * ic_sfb);
                 if (h_ready) copy_act(st + u * Geo::kAct, ic_ap ? ic_ap + (ic_s + u) * 128 : nullptr);
             }

@@ -75,6 +75,28 @@ __device__ __forceinline__ void cp_async8(uint32_t saddr, const void* g) {
 __device__ __forceinline__ void cp_async4(uint32_t saddr, const void* g) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr), "l"(g) : "memory");
 }
+// The same copies with an L2 cache policy (streamed weights: evict first, so that they do not
+// push the kernel's code and the small per-step tensors out of L2).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void cp_async16_pol(uint32_t saddr, const void* g, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g),
+                 "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async8_pol(uint32_t saddr, const void* g, uint64_t pol) {
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2;" ::"r"(saddr), "l"(g),
+                 "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4_pol(uint32_t saddr, const void* g, uint64_t pol) {
+    asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2;" ::"r"(saddr), "l"(g),
+                 "l"(pol)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
