@@ -191,6 +191,10 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
     int ci = blockIdx.x, ip = 0, is = 0;
     ErItem cw{};
     int c_steps = 1, c_passes = 0, c_sfb = 8;
+    // weight rows read once (one pass over the item's tokens) stream with an L2 evict-first
+    // policy; rows read again in a later pass stay at the normal priority
+    const uint64_t pol_once = l2_evict_first_policy(), pol_again = l2_evict_normal_policy();
+    uint64_t c_pol = pol_once;
     size_t c_rstride = 0;
     const uint8_t *pa = nullptr, *pb = nullptr, *ps = nullptr;
     const __half* ib[NT];
@@ -209,6 +213,7 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
         c_sfb = 128 / sv;
         c_steps = cw.K / 128;
         c_passes = (cw.cnt + 8 * NT - 1) / (8 * NT);
+        c_pol = c_passes > 1 ? pol_again : pol_once;
         c_rstride = (size_t)8 * (cw.K / 2);
         const int xb = ci % xblocks;
         const int n0 = (xb * kErWarps + warp) * 16;
@@ -234,16 +239,16 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
             const uint32_t sw = st + warp * kErWarpBytes;
             const int o = is * 64;
             if (pa) {
-                cp_async16(sw + lane * 16, pa + o);
-                cp_async16(sw + 512 + lane * 16, pa + c_rstride + o);
+                cp_async16_pol(sw + lane * 16, pa + o, c_pol);
+                cp_async16_pol(sw + 512 + lane * 16, pa + c_rstride + o, c_pol);
             }
             if (pb) {
-                cp_async16(sw + 1024 + lane * 16, pb + o);
-                cp_async16(sw + 1536 + lane * 16, pb + c_rstride + o);
+                cp_async16_pol(sw + 1024 + lane * 16, pb + o, c_pol);
+                cp_async16_pol(sw + 1536 + lane * 16, pb + c_rstride + o, c_pol);
             }
             if (ps) {
-                if (c_sfb == 8) cp_async8(sw + 2048 + lane * 8, ps + is * c_sfb);
-                else cp_async4(sw + 2048 + lane * 8, ps + is * c_sfb);
+                if (c_sfb == 8) cp_async8_pol(sw + 2048 + lane * 8, ps + is * c_sfb, c_pol);
+                else cp_async4_pol(sw + 2048 + lane * 8, ps + is * c_sfb, c_pol);
             }
 #pragma unroll
             for (int t = 0; t < NT; ++t)
