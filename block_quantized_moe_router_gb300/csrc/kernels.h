@@ -128,7 +128,9 @@ struct TcCombineArgs {
 };
 
 bool tc_supported(int E, int H, int I, int I_shared, int fmt_routed, int fmt_shared);
-cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, cudaStream_t st);
+// replicated: also build B's scales as replicated pair tiles (used by launches with >= 512
+// routed pairs per expert)
+cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, bool replicated, cudaStream_t st);
 void tc_release(TcWeights* tw);
 cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffers& B,
                           cudaStream_t st, const PhaseEvents* ev);

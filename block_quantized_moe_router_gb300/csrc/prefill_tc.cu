@@ -656,7 +656,7 @@ bool tc_supported(int E, int H, int I, int I_shared, int fmt_routed, int fmt_sha
     return tc_shape_ok(H, I, I_shared, fmt_routed, fmt_shared) && encode_fn() != nullptr;
 }
 
-cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, cudaStream_t st) {
+cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, bool replicated, cudaStream_t st) {
     *tw = TcWeights{};
     const int E = L.E, H = L.H, I = L.I, Is = L.I_shared;
     cudaError_t err;
@@ -675,10 +675,11 @@ cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, cudaStream_t st) {
              encode_rows(&tw->sh_down, L.sh_down.packed, Is / 2, H, 256);
     }
     if (!ok) return cudaErrorInvalidValue;
-    // B's scales also as replicated pair tiles: gate | up per 128-row block, 256-row blocks of down
-    if ((err = make_pairs(&tw->sfp_gu, tw->sf_gate, tw->sf_up, (int64_t)E * (I / 128), H, 1, 0, 0, st)) != cudaSuccess) return err;
-    if ((err = make_pairs(&tw->sfp_dn, tw->sf_down, tw->sf_down, (int64_t)E * (H / 256), I, 2, 0, 1, st)) != cudaSuccess) return err;
-    if (Is > 0) {
+    // B's scales also as replicated pair tiles (when asked for): gate | up per 128-row block,
+    // 256-row blocks of down
+    if (replicated && (err = make_pairs(&tw->sfp_gu, tw->sf_gate, tw->sf_up, (int64_t)E * (I / 128), H, 1, 0, 0, st)) != cudaSuccess) return err;
+    if (replicated && (err = make_pairs(&tw->sfp_dn, tw->sf_down, tw->sf_down, (int64_t)E * (H / 256), I, 2, 0, 1, st)) != cudaSuccess) return err;
+    if (replicated && Is > 0) {
         if ((err = make_pairs(&tw->sfp_sh_gu, tw->sf_sh_gate, tw->sf_sh_up, Is / 128, H, 1, 0, 0, st)) != cudaSuccess) return err;
         if ((err = make_pairs(&tw->sfp_sh_dn, tw->sf_sh_down, tw->sf_sh_down, H / 256, Is, 2, 0, 1, st)) != cudaSuccess) return err;
     }
@@ -707,9 +708,9 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
                           cudaStream_t st, const PhaseEvents* ev) {
     const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
     const int P = L.T * L.k;
-    // replicated B scales once an expert's weight tiles serve >= 4 row blocks on average
-    // (the tensor pipe, not HBM, is then the limit)
-    const bool rep = (int64_t)P >= (int64_t)512 * L.E;
+    // replicated B scales (if the handle keeps them) once an expert's weight tiles serve >= 4
+    // row blocks on average: the tensor pipe, not HBM, is then the limit
+    const bool rep = tw.sfp_gu != nullptr && (int64_t)P >= (int64_t)512 * L.E;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -78,7 +78,8 @@ SMALL = {
 
 
 def _run(cfg, inp, with_logits=False):
-    layer = MoeLayer.from_inputs(inp)
+    # the handle keeps replicated scale tiles for the cases meant to use them
+    layer = MoeLayer.from_inputs(inp, tc_replicated_scales=cfg.name.startswith("tc_rep"))
     x = inp["x"].cuda()
     tok = inp["token_ids"].cuda() if "token_ids" in inp else None
     ids, w, logits = layer.route(x, token_ids=tok)
