@@ -202,11 +202,27 @@ __global__ void __launch_bounds__(256) tc_gather_rows_kernel(TcQuantArgs a) {
         const uint4* src = reinterpret_cast<const uint4*>(a.tokq + (size_t)t * (a.H / 2));
         uint4* dst = reinterpret_cast<uint4*>(a.xq + (size_t)prow * (a.H / 2));
         for (int c = lane; c < a.H / 32; c += 32) dst[c] = src[c];
-        const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(a.toks + (size_t)t * (a.H / 16));
-        const int mb = prow >> 7, r = prow & 127;
-        for (int kb = lane; kb < a.H / 64; kb += 32)  // 4 scales (one 64-element K block)
-            *reinterpret_cast<uint32_t*>(a.xsf + ((size_t)mb * (a.H / 64) + kb) * 512 +
-                                         sf_tile_offset(r, 0)) = ssrc[kb];
+    }
+    // scale tiles: one thread per 16-byte line (line l of K block kb holds the 4 scales of rows
+    // l, l + 32, l + 64, l + 96), so a warp writes 512 contiguous bytes; rows without a pair
+    // get zero scales
+    const int KB = a.H / 64;
+    const int64_t lines = (int64_t)a.meta[3] * KB * 32;
+    const uint32_t* toks32 = reinterpret_cast<const uint32_t*>(a.toks);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < lines;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int l = (int)(i & 31);
+        const int64_t bk = i >> 5;
+        const int mb = (int)(bk / KB), kb = (int)(bk - (int64_t)mb * KB);
+        uint32_t w[4];
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+            const int p = a.padrow_pair[mb * 128 + 32 * qd + l];
+            const int t = p < a.P ? p / a.k : p - a.P;
+            w[qd] = p < 0 ? 0u : toks32[(size_t)t * KB + kb];
+        }
+        *reinterpret_cast<uint4*>(a.xsf + ((size_t)mb * KB + kb) * 512 + l * 16) =
+            make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
