@@ -193,9 +193,11 @@ moe_status_t moe_route(const moe_route_desc* d, const void* x_bf16, const float*
     const float* logits = logits_in;
     if (!logits) {
         if (!d->w_router || !x_bf16 || !logits_out) return MOE_ERR_INVALID_ARG;
-        if (launch_router_logits(x_bf16, d->w_router, logits_out, d->T, Er, d->H, st) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
+        cudaError_t err = launch_router_tc(x_bf16, d->w_router, logits_out, d->T, Er, d->H,
+                                           dev_status, st);
+        if (err == cudaErrorNotSupported)
+            err = launch_router_logits(x_bf16, d->w_router, logits_out, d->T, Er, d->H, st);
+        if (err != cudaSuccess) return MOE_ERR_CUDA;
         logits = logits_out;
     }
     const float* bias = d->scoring != MOE_SCORE_SOFTMAX ? d->correction_bias : nullptr;

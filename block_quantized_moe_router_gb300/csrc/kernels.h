@@ -11,6 +11,10 @@ namespace moe {
 // ---- routing (route.cu) -------------------------------------------------------------------
 cudaError_t launch_router_logits(const void* x, const void* wr, float* logits, int T, int E,
                                  int H, cudaStream_t st);
+// The same on the tensor cores (prefill_tc.cu): T >= 128 tokens, E a multiple of 128;
+// cudaErrorNotSupported (nothing launched) otherwise.
+cudaError_t launch_router_tc(const void* x, const void* wr, float* logits, int T, int E, int H,
+                             int32_t* status, cudaStream_t st);
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int scoring,
                         int renorm, float scaling, int32_t* ids, float* w, int32_t* status,
                         cudaStream_t st);

@@ -720,6 +720,156 @@ void tc_release(TcWeights* tw) {
 }
 
 // ------------------------------------------------------------------------------------------
+// Router logits of many tokens on the tensor cores: logits[t][e] = x[t] . W_r[e] (bf16 in,
+// fp32 out), one 128-token x 128-expert tile per CTA over the whole K = H.  Warp 0 issues the
+// TMA loads into a 4-stage ring (64 elements of K per stage, 128-byte swizzled rows), one lane
+// of warp 1 issues tcgen05.mma.kind::f16 (M 128, N 128, K 16; four per stage) into a 128-column
+// TMEM accumulator, warps 2-5 (one per lane quarter) read it back and write fp32 rows.  Every
+// wait is bounded: a wait that gives up sets MOE_DEV_TIMEOUT and the CTA winds down.
+// ------------------------------------------------------------------------------------------
+constexpr int kRtStages = 4;
+constexpr int kRtStageBytes = 2 * 128 * 128;  // A and B: 128 rows x 128 B each
+constexpr int kRtSmemBytes = kRtStages * kRtStageBytes + 1024 + 256;
+constexpr int kRtThreads = 192;
+
+struct RtMaps {
+    CUtensorMap x, w;
+};
+
+__global__ void __launch_bounds__(kRtThreads, 1)
+router_tc_kernel(const __grid_constant__ RtMaps maps, float* __restrict__ logits, int T, int E,
+                 int H, int32_t* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRtStages * kRtStageBytes);
+    uint64_t* empty = full + kRtStages;
+    uint64_t* acc_full = empty + kRtStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * 128, e0 = blockIdx.y * 128, nk = H / 64;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRtStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&maps.x);
+        prefetch_tmap(&maps.w);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        if (status) status_or(status, MOE_DEV_TIMEOUT);
+    };
+    if (warp == 0 && lane == 0) {  // TMA producer
+        int issued = 0;
+        for (int ks = 0; ks < nk && !*abort_flag; ++ks) {
+            const int s = ks % kRtStages;
+            const uint32_t ph = (ks / kRtStages) & 1u;
+            if (!mbar_wait_bounded(&empty[s], ph ^ 1u, kTcWaitLimit)) {
+                give_up();
+                break;
+            }
+            uint8_t* base = smem + s * kRtStageBytes;
+            mbar_arrive_expect_tx(&full[s], kRtStageBytes);
+            tma_load_2d(base, &maps.x, ks * 128, t0, &full[s]);
+            tma_load_2d(base + 128 * 128, &maps.w, ks * 128, e0, &full[s]);
+            ++issued;
+        }
+        if (*abort_flag)  // wait (bounded) for the copies still in flight
+            for (int i = issued - 1; i >= 0 && i >= issued - kRtStages; --i)
+                mbar_wait_bounded(&full[i % kRtStages], (i / kRtStages) & 1u, kTcWaitLimit);
+    } else if (warp == 1 && lane == 0) {  // MMA issuer
+        const uint32_t idesc = idesc_bf16(128, 128);
+        bool any = false;
+        for (int ks = 0; ks < nk; ++ks) {
+            const int s = ks % kRtStages;
+            if (!mbar_wait_bounded(&full[s], (ks / kRtStages) & 1u, kTcWaitLimit) || *abort_flag) {
+                give_up();
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sbase = smem_u32(smem + s * kRtStageBytes);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // K 16 per MMA: 32 bytes along the swizzled row
+                const uint64_t ad = smem_desc(sbase + 32 * j, 16, 1024, kLayoutSw128);
+                const uint64_t bd = smem_desc(sbase + 128 * 128 + 32 * j, 16, 1024, kLayoutSw128);
+                tc_mma_bf16(tmem, ad, bd, idesc, (ks | j) != 0 ? 1u : 0u);
+            }
+            any = true;
+            tc_commit(&empty[s]);
+        }
+        if (any) {
+            tc_commit(acc_full);  // every MMA has completed when this arrives
+            mbar_wait_bounded(acc_full, 0, kTcWaitLimit);  // before TMEM can be freed
+        } else if (!*abort_flag) {
+            give_up();
+        }
+    } else if (warp >= 2) {  // epilogue: lane quarter q reads rows 32 q .. 32 q + 31
+        const int q = warp & 3;
+        const int t = t0 + 32 * q + lane;
+        bool ok = mbar_wait_bounded(acc_full, 0, kTcWaitLimit);
+        if (ok && !*abort_flag) {
+            tc_fence_after();
+            const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+#pragma unroll
+            for (int c = 0; c < 128; c += 32) {
+                uint32_t v[32];
+                tmem_ld_16(trow + c, *reinterpret_cast<uint32_t(*)[16]>(v));
+                tmem_ld_16(trow + c + 16, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+                tmem_ld_wait();
+                if (t < T) {
+                    float* dst = logits + (size_t)t * E + e0 + c;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        const uint32_t (&w8)[8] = *reinterpret_cast<const uint32_t(*)[8]>(v + i);
+                        st_global_v8(dst + i, w8);
+                    }
+                }
+            }
+        } else if (!ok) {
+            give_up();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+cudaError_t launch_router_tc(const void* x, const void* wr, float* logits, int T, int E, int H,
+                             int32_t* status, cudaStream_t st) {
+    if (T < 128 || E % 128 != 0 || H % 128 != 0 || encode_fn() == nullptr) return cudaErrorNotSupported;
+    // TMA sources 16-byte aligned, 32-byte row stores
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(wr)) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(logits) % 32 != 0)
+        return cudaErrorNotSupported;
+    RtMaps m{};
+    if (!encode_rows(&m.x, x, (uint64_t)H * 2, (uint64_t)T, 128) ||
+        !encode_rows(&m.w, wr, (uint64_t)H * 2, (uint64_t)E, 128))
+        return cudaErrorNotSupported;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kRtSmemBytes);
+        if (err != cudaSuccess) return err;
+        attr_set = true;
+    }
+    router_tc_kernel<<<dim3((T + 127) / 128, E / 128), kRtThreads, kRtSmemBytes, st>>>(m, logits, T, E, H, status);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
 cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffers& B,
                           cudaStream_t st, const PhaseEvents* ev) {
     const int Imax = L.I > L.I_shared ? L.I : L.I_shared;

@@ -123,6 +123,15 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uin
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[smem] x B[smem]^T with bf16 operands, fp32 accumulate (kind::f16).
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // 32 lanes x 32 bits, 16 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld_16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -156,6 +165,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 // M >> 4 in bits 24-28, scale-factor ids 0.
 __host__ __device__ constexpr uint32_t idesc_fp4(uint32_t M, uint32_t N, uint32_t scale_ue8m0) {
     return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (scale_ue8m0 << 23) | ((M >> 4) << 24);
+}
+// Instruction descriptor of kind::f16 with bf16 A and B (format code 1 in bits 7-9 and 10-12),
+// fp32 D (format code 1 in bits 4-5), K-major A and B, N >> 3 in bits 17-22, M >> 4 in 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 }  // namespace tc

@@ -43,6 +43,11 @@ CASES = {
     "sqrt_softplus": synth.MoeConfig("sq", T=21, H=1024, I=128, E=96, k=6,
                                      scoring=synth.SCORE_SQRTSOFTPLUS, scaling=1.5),
     "pre4096": synth.CONFIGS["pre4096"],
+    # >= 128 tokens, experts a multiple of 128: the tensor-core router GEMM, with a ragged
+    # last token block
+    "tc_router": synth.MoeConfig("tr", T=300, H=384, I=128, E=128, k=6, scoring=synth.SCORE_SOFTMAX),
+    "tc_router_sig": synth.MoeConfig("trs", T=129, H=1152, I=128, E=256, k=8,
+                                     scoring=synth.SCORE_SIGMOID, scaling=2.5),
 }
 
 
