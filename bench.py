@@ -287,8 +287,7 @@ def run_ours(args, cfg):
 
     inp = synth.make_inputs(cfg, seed=rank, device="cuda")
     # compute-bound prefill (>= 512 routed pairs per expert) keeps replicated scale tiles
-    rep_scales = cfg.act == synth.ACT_NVFP4 and cfg.T * cfg.k >= 512 * cfg.E
-    base = MoeLayer.from_inputs(inp, tc_replicated_scales=rep_scales)
+    base = MoeLayer.from_inputs(inp)
     x = inp["x"].cuda()
     tok = inp["token_ids"].cuda() if "token_ids" in inp else None
     T = cfg.T
@@ -305,7 +304,7 @@ def run_ours(args, cfg):
         clone = {k: ({kk: (vv.clone() if isinstance(vv, torch.Tensor) else vv)
                       for kk, vv in v.items()} if isinstance(v, dict) else v)
                  for k, v in inp.items()}
-        layers.append(MoeLayer.from_inputs(clone, tc_replicated_scales=rep_scales))
+        layers.append(MoeLayer.from_inputs(clone))
     bufs = []
     for layer in layers:
         layer.workspace(T)
@@ -459,9 +458,7 @@ def run_ours(args, cfg):
                        "l2_policy": f"inputs larger than L2: {replicas} weight replicas cycled, "
                                     f"{replicas * nbytes['total'] / 1e6:.0f} MB touched per cycle",
                        "launch": f"CUDA graph of {replicas} layer steps (one per replica), replayed",
-                       "touched_experts": touched,
-                       "tc_scales": ("replicated" if rep_scales else "compact")
-                       if cfg.act == synth.ACT_NVFP4 else None},
+                       "touched_experts": touched},
             "gpu_launches": args.steps * launches_per_step(cfg),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "kernel": dom_name,

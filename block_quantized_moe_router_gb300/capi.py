@@ -45,7 +45,7 @@ class moe_ffn_desc(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("I_shared", ctypes.c_int32),
                 ("gate", moe_qtensor), ("up", moe_qtensor), ("down", moe_qtensor),
                 ("sh_gate", moe_qtensor), ("sh_up", moe_qtensor), ("sh_down", moe_qtensor),
-                ("zero_experts", ctypes.c_int32), ("tc_replicated_scales", ctypes.c_int32)]
+                ("zero_experts", ctypes.c_int32)]
 
 
 class moe_route_desc(ctypes.Structure):
@@ -132,10 +132,9 @@ def qtensor(p: Optional[dict]) -> moe_qtensor:
 
 
 def ffn_desc(E, H, I, top_k, I_shared, gate, up, down, sh_gate=None, sh_up=None, sh_down=None,
-             zero_experts=0, tc_replicated_scales=False):
+             zero_experts=0):
     return moe_ffn_desc(E, H, I, top_k, I_shared, qtensor(gate), qtensor(up), qtensor(down),
-                        qtensor(sh_gate), qtensor(sh_up), qtensor(sh_down), int(zero_experts),
-                        int(bool(tc_replicated_scales)))
+                        qtensor(sh_gate), qtensor(sh_up), qtensor(sh_down), int(zero_experts))
 
 
 def route_desc(*, T, E, H, top_k, scoring, renormalize, routed_scaling, w_router=None,

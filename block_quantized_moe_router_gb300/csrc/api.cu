@@ -89,7 +89,6 @@ moe_status_t validate_ffn_desc(const moe_ffn_desc* d) {
     if (!d) return MOE_ERR_INVALID_ARG;
     if (d->E < 1 || d->zero_experts < 0 || d->E + d->zero_experts > kMaxExperts)
         return MOE_ERR_INVALID_ARG;
-    if (d->tc_replicated_scales != 0 && d->tc_replicated_scales != 1) return MOE_ERR_INVALID_ARG;
     if (d->top_k < 1 || d->top_k > d->E + d->zero_experts || d->top_k > kMaxTopK)
         return MOE_ERR_INVALID_ARG;
     if (d->H < 128 || d->H % 128 || d->I < 128 || d->I % 128) return MOE_ERR_INVALID_ARG;
@@ -248,7 +247,7 @@ moe_status_t moe_prepare_weights(const moe_ffn_desc* d, void** handle_out, void*
         L.E = E; L.H = H; L.I = I; L.I_shared = Is;
         L.gate = h->gate.view; L.up = h->up.view; L.down = h->down.view;
         L.sh_gate = h->sh_gate.view; L.sh_up = h->sh_up.view; L.sh_down = h->sh_down.view;
-        if (tc_prepare(L, &h->tc, d->tc_replicated_scales != 0, st) != cudaSuccess) s = MOE_ERR_CUDA;
+        if (tc_prepare(L, &h->tc, st) != cudaSuccess) s = MOE_ERR_CUDA;
     }
     if (s == MOE_OK && cudaStreamSynchronize(st) != cudaSuccess) s = MOE_ERR_CUDA;
     if (s != MOE_OK) {

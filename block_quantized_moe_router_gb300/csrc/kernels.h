@@ -70,7 +70,7 @@ struct TcWeights {
     CUtensorMap gate, up, down, sh_gate, sh_up, sh_down;
     uint8_t *sf_gate = nullptr, *sf_up = nullptr, *sf_down = nullptr;
     uint8_t *sf_sh_gate = nullptr, *sf_sh_up = nullptr, *sf_sh_down = nullptr;
-    // B-operand scales as pair tiles (two 128-row tiles interleaved per 64-element K block)
+    // B-operand scales as quarter tiles (the compact tiles above are freed once these exist)
     uint8_t *sfp_gu = nullptr, *sfp_dn = nullptr, *sfp_sh_gu = nullptr, *sfp_sh_dn = nullptr;
     // per-expert post-scales seen by the MMA path: the NVFP4 globals, or for MXFP4 the power of
     // two left over after the E8M0 scales were re-expressed as E4M3 (owned when MXFP4)
@@ -112,8 +112,7 @@ struct TcGemmParams {
     const int32_t *mblock_expert, *padrow_pair;
     const uint8_t* sfa;
     int sfa_kblocks;
-    const uint8_t *sfb0, *sfb1, *ssfb0, *ssfb1;
-    const uint8_t *sfr, *ssfr;  // B's scales as replicated pair tiles (routed, shared)
+    const uint8_t *sfb0, *ssfb0;  // B's scales as quarter tiles (routed, shared)
     const float *post0, *post1, *spost0, *spost1;
     const float* topk_w;
     uint8_t *hq, *hsf;
@@ -132,9 +131,7 @@ struct TcCombineArgs {
 };
 
 bool tc_supported(int E, int H, int I, int I_shared, int fmt_routed, int fmt_shared);
-// replicated: also build B's scales as replicated pair tiles (used by launches with >= 512
-// routed pairs per expert)
-cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, bool replicated, cudaStream_t st);
+cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, cudaStream_t st);
 void tc_release(TcWeights* tw);
 cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffers& B,
                           cudaStream_t st, const PhaseEvents* ev);

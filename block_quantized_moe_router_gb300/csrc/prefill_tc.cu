@@ -44,23 +44,17 @@ constexpr int kTcBBytes = 256 * 128;          // 256 rows x 128 B
 constexpr int kTcSfaBytes = 4 * 512;          // 4 K blocks of 64 x one 128-row scale tile
 constexpr int kTcSfaOff = kTcABytes + kTcBBytes;
 constexpr uint32_t kTcTmemCols = 512;         // 256 accumulator + up to 4 stages x 48 scale columns
-// Two ways to bring B's scales into TMEM, chosen per launch:
-//   compact (REP = false): per K block the two 128-row scale tiles of the 256 B rows (512 B
-//     each) as loaded from HBM, each spread over the 4 lane quarters by a replicating 32-lane
-//     copy; 4 stages of 54 KiB.  Least HBM traffic: for layers that stream their weights.
-//   replicated (REP = true): per K block one 1 KB pair tile (the two tiles interleaved in
-//     128-byte groups) for each of the 4 lane quarters, stored so in HBM, one bulk copy per
-//     stage and one 128-lane copy per K block (a replicating copy costs the tensor pipe several
-//     times more); 3 stages of 66 KiB.  For layers whose expert tiles are reused by many row
-//     blocks, where the tensor pipe rather than HBM is the limit.
-template <bool REP>
-struct TcGeom {
-    static constexpr int kStages = REP ? 3 : 4;
-    static constexpr int kSfbBytes = REP ? 4 * 4096 : 8 * 512;
-    static constexpr int kSfbOff = kTcSfaOff + kTcSfaBytes;
-    static constexpr int kStageBytes = kSfbOff + kSfbBytes;  // 66 / 54 KiB, 1 KiB multiples
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
-};
+// B's scales reach TMEM as quarter tiles: a stage's scales, prepared once as one 4 KB tile
+// (the lines of both 128-row scale tiles of the 256 B rows for its 4 K blocks, as the 32 TMEM
+// lanes of one lane quarter read them), bulk-copied into each of the four lane quarters'
+// shared-memory slices (the three repeats hit L2), then one 128-lane copy per K block.  A
+// copy that replicates 32 lanes to the four quarters (`32x128b.warpx4`, used for A's scales)
+// costs the tensor pipe several times more.  3 stages of 66 KiB.
+constexpr int kTcStages = 3;
+constexpr int kTcSfbBytes = 4 * 4096;
+constexpr int kTcSfbOff = kTcSfaOff + kTcSfaBytes;
+constexpr int kTcStageBytes = kTcSfbOff + kTcSfbBytes;  // 67584 (66 KiB, 1 KiB multiple)
+constexpr int kTcSmemBytes = kTcStages * kTcStageBytes + 1024 + 256;
 constexpr int kTcThreads = 320;    // producer warp, MMA warp, 8 epilogue warps
 constexpr int kTcEpiThreads = 256;
 constexpr uint64_t kTcWaitLimit = 1ull << 26;  // polls before a wait is declared stuck
@@ -234,12 +228,8 @@ __device__ __forceinline__ void tc_abort(TcGemmParams const& p, volatile int* fl
     status_or(p.status, MOE_DEV_TIMEOUT);
 }
 
-template <bool REP>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) {
-    using Geo = TcGeom<REP>;
-    constexpr int kTcStages = Geo::kStages, kTcStageBytes = Geo::kStageBytes;
-    constexpr int kTcSfbOff = Geo::kSfbOff, kTcSfbBytes = Geo::kSfbBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -307,31 +297,17 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                         tma_load_2d(base + kTcABytes + 16384, sh ? &maps.sb1 : &maps.b1, xb, row,
                                     &full[stage]);
                         const size_t tix = ((size_t)es * (N / 128) + nb) * (p.H / 64) + 4 * ks;
-                        if constexpr (REP) {
-                            bulk_load(base + kTcSfbOff, (sh ? p.ssfr : p.sfr) + tix * 4096, kTcSfbBytes,
-                                      &full[stage]);
-                        } else {
-                            bulk_load(base + kTcSfbOff, (sh ? p.ssfb0 : p.sfb0) + tix * 512, 2048,
-                                      &full[stage]);
-                            bulk_load(base + kTcSfbOff + 2048, (sh ? p.ssfb1 : p.sfb1) + tix * 512,
-                                      2048, &full[stage]);
-                        }
+                        const uint8_t* q4 = (sh ? p.ssfb0 : p.sfb0) + tix * 1024;  // quarter tile
+                        for (int qd = 0; qd < 4; ++qd)
+                            bulk_load(base + kTcSfbOff + qd * (kTcSfbBytes / 4), q4, kTcSfbBytes / 4, &full[stage]);
                     } else {
                         const int K = sh ? p.I_shared : p.I;
                         const int row = es * p.H + nb * 256;
                         tma_load_2d(base + kTcABytes, sh ? &maps.sb0 : &maps.b0, xb, row, &full[stage]);
-                        if constexpr (REP) {
-                            bulk_load(base + kTcSfbOff,
-                                      (sh ? p.ssfr : p.sfr) +
-                                          (((size_t)es * (p.H / 256) + nb) * (K / 64) + 4 * ks) * 4096,
-                                      kTcSfbBytes, &full[stage]);
-                        } else {
-                            const uint8_t* sfb = sh ? p.ssfb0 : p.sfb0;
-                            const size_t t0 = ((size_t)es * (p.H / 128) + 2 * nb) * (K / 64) + 4 * ks;
-                            const size_t t1 = ((size_t)es * (p.H / 128) + 2 * nb + 1) * (K / 64) + 4 * ks;
-                            bulk_load(base + kTcSfbOff, sfb + t0 * 512, 2048, &full[stage]);
-                            bulk_load(base + kTcSfbOff + 2048, sfb + t1 * 512, 2048, &full[stage]);
-                        }
+                        const uint8_t* q4 = (sh ? p.ssfb0 : p.sfb0) +
+                                            (((size_t)es * (p.H / 256) + nb) * (K / 64) + 4 * ks) * 1024;
+                        for (int qd = 0; qd < 4; ++qd)
+                            bulk_load(base + kTcSfbOff + qd * (kTcSfbBytes / 4), q4, kTcSfbBytes / 4, &full[stage]);
                     }
                     ++issued;
                     if (++stage == kTcStages) { stage = 0; phase ^= 1u; }
@@ -374,27 +350,16 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                     const uint32_t sfcol = 256 + stage * 48;
                     // scale columns of the stage, per K block j: B's 8 and A's 4
                     uint32_t sfa_c[4], sfb_c[4];
-                    if constexpr (REP) {
-                        // B: one 128-lane copy of 128 rows x 32 B (row 32 Q + l = lines l of both
-                        // tiles; core matrices of 8 rows x 16 B, 128 B between a row's halves,
-                        // 256 B between 8-row groups) at +8 j; A: a replicating copy at +32 + 4 j
+                    // B: one 128-lane copy per K block j of 128 rows x 32 B (row 32 Q + l =
+                    // line l of both tiles; core matrices of 8 rows x 16 B, 128 B between a
+                    // row's halves, 1 KB between 8-row groups, K block j at +256 j) into columns
+                    // +8 j; A: a replicating copy at +32 + 4 j
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            sfb_c[j] = tmem + sfcol + 8 * j;
-                            sfa_c[j] = tmem + sfcol + 32 + 4 * j;
-                            tc_cp_128x256b(sfb_c[j], smem_desc(sbase + kTcSfbOff + 4096 * j, 128, 256, kLayoutNone));
-                            tc_cp_32x128b_warpx4(sfa_c[j], smem_desc(sbase + kTcSfaOff + 512 * j, 0, 128, kLayoutNone));
-                        }
-                    } else {
-                        // A at +12 j, B's two tiles at +12 j + 4 and + 8, all replicating copies
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            sfa_c[j] = tmem + sfcol + 12 * j;
-                            sfb_c[j] = sfa_c[j] + 4;
-                            tc_cp_32x128b_warpx4(sfa_c[j], smem_desc(sbase + kTcSfaOff + 512 * j, 0, 128, kLayoutNone));
-                            tc_cp_32x128b_warpx4(sfb_c[j], smem_desc(sbase + kTcSfbOff + 512 * j, 0, 128, kLayoutNone));
-                            tc_cp_32x128b_warpx4(sfb_c[j] + 4, smem_desc(sbase + kTcSfbOff + 2048 + 512 * j, 0, 128, kLayoutNone));
-                        }
+                    for (int j = 0; j < 4; ++j) {
+                        sfb_c[j] = tmem + sfcol + 8 * j;
+                        sfa_c[j] = tmem + sfcol + 32 + 4 * j;
+                        tc_cp_128x256b(sfb_c[j], smem_desc(sbase + kTcSfbOff + 256 * j, 128, 1024, kLayoutNone));
+                        tc_cp_32x128b_warpx4(sfa_c[j], smem_desc(sbase + kTcSfaOff + 512 * j, 0, 128, kLayoutNone));
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -591,26 +556,28 @@ __global__ void sf_tiles_mx_kernel(const uint8_t* __restrict__ in, const int32_t
     }
 }
 
-// Pair tiles of B's scales: for pair pidx and K block kb, 1 KB interleaving (in 128-byte
-// groups) the scale tiles t = 0, 1 at tile index pidx * mul + add_t of src_t, stored four
-// times in a row (one copy per TMEM lane quarter, so a stage's scales are one bulk copy).
+// Quarter tiles of B's scales: the lines of the two 128-row scale tiles t = 0, 1 (tile index
+// pidx * mul + add_t of src_t) of a pair's four K blocks of a K-stage, laid out as the 32 TMEM
+// lanes of one lane quarter read them (4 KB): a stage's scales are this 4 KB copied to each of
+// the four quarters' shared-memory slices.
 __global__ void sf_pair_kernel(const uint8_t* __restrict__ src0, const uint8_t* __restrict__ src1,
                                uint8_t* __restrict__ out, int64_t npairs, int kblocks, int mul,
                                int add0, int add1) {
     const int64_t total = npairs * kblocks * 64;  // 16-byte pieces
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int piece = (int)(i & 63);
-        const int64_t pk = i >> 6;  // pair * kblocks + kb
+        const int piece = (int)(i & 63);  // line l of tile t
+        const int64_t pk = i >> 6;          // pair * kblocks + kb
         const int64_t pidx = pk / kblocks;
         const int kb = (int)(pk - pidx * kblocks);
-        const int grp = piece >> 4, t = (piece >> 3) & 1, b16 = piece & 7;
+        const int t = piece >> 5, l = piece & 31;
         const uint8_t* src = t ? src1 : src0;
         const int64_t tile = pidx * mul + (t ? add1 : add0);
-        const uint4 v = *reinterpret_cast<const uint4*>(src + (tile * kblocks + kb) * 512 + grp * 128 + b16 * 16);
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd)
-            *reinterpret_cast<uint4*>(out + pk * 4096 + qd * 1024 + grp * 256 + t * 128 + b16 * 16) = v;
+        const uint4 v = *reinterpret_cast<const uint4*>(src + (tile * kblocks + kb) * 512 + l * 16);
+        // per pair and K-stage (4 K blocks) 4 KB: 8-line group g = l / 8 at 1 KB steps, K block
+        // at 256 B, tile at 128 B, line in group at 16 B
+        *reinterpret_cast<uint4*>(out + (pidx * kblocks + (kb & ~3)) * 1024 + (l >> 3) * 1024 +
+                                  (kb & 3) * 256 + t * 128 + (l & 7) * 16) = v;
     }
 }
 
@@ -658,10 +625,10 @@ static cudaError_t make_sf_tiles(const ProjView& pv, int E, int N, int K, uint8_
     return cudaGetLastError();
 }
 
-// Replicated pair tiles from compact tiles: npairs pairs of K / 64 blocks.
+// Quarter tiles from compact tiles: npairs pairs of K / 64 blocks.
 static cudaError_t make_pairs(uint8_t** out, uint8_t* src0, uint8_t* src1, int64_t npairs, int K,
                               int mul, int add0, int add1, cudaStream_t st) {
-    cudaError_t err = cudaMalloc(out, (size_t)npairs * (K / 64) * 4096);
+    cudaError_t err = cudaMalloc(out, (size_t)npairs * (K / 64) * 1024);
     if (err != cudaSuccess) return err;
     sf_pair_kernel<<<1024, 256, 0, st>>>(src0, src1, *out, npairs, K / 64, mul, add0, add1);
     return cudaGetLastError();
@@ -672,7 +639,7 @@ bool tc_supported(int E, int H, int I, int I_shared, int fmt_routed, int fmt_sha
     return tc_shape_ok(H, I, I_shared, fmt_routed, fmt_shared) && encode_fn() != nullptr;
 }
 
-cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, bool replicated, cudaStream_t st) {
+cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, cudaStream_t st) {
     *tw = TcWeights{};
     const int E = L.E, H = L.H, I = L.I, Is = L.I_shared;
     cudaError_t err;
@@ -691,19 +658,21 @@ cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, bool replicated, cudaS
              encode_rows(&tw->sh_down, L.sh_down.packed, Is / 2, H, 256);
     }
     if (!ok) return cudaErrorInvalidValue;
-    // B's scales also as replicated pair tiles (when asked for): gate | up per 128-row block,
-    // 256-row blocks of down
-    if (replicated && (err = make_pairs(&tw->sfp_gu, tw->sf_gate, tw->sf_up, (int64_t)E * (I / 128), H, 1, 0, 0, st)) != cudaSuccess) return err;
-    if (replicated && (err = make_pairs(&tw->sfp_dn, tw->sf_down, tw->sf_down, (int64_t)E * (H / 256), I, 2, 0, 1, st)) != cudaSuccess) return err;
-    if (replicated && Is > 0) {
+    // B's scales as quarter tiles: gate | up per 128-row block, 256-row blocks of down; the
+    // compact tiles they are built from are freed
+    if ((err = make_pairs(&tw->sfp_gu, tw->sf_gate, tw->sf_up, (int64_t)E * (I / 128), H, 1, 0, 0, st)) != cudaSuccess) return err;
+    if ((err = make_pairs(&tw->sfp_dn, tw->sf_down, tw->sf_down, (int64_t)E * (H / 256), I, 2, 0, 1, st)) != cudaSuccess) return err;
+    if (Is > 0) {
         if ((err = make_pairs(&tw->sfp_sh_gu, tw->sf_sh_gate, tw->sf_sh_up, Is / 128, H, 1, 0, 0, st)) != cudaSuccess) return err;
         if ((err = make_pairs(&tw->sfp_sh_dn, tw->sf_sh_down, tw->sf_sh_down, H / 256, Is, 2, 0, 1, st)) != cudaSuccess) return err;
     }
-    err = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               TcGeom<false>::kSmemBytes);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               TcGeom<true>::kSmemBytes);
+    if ((err = cudaStreamSynchronize(st)) != cudaSuccess) return err;
+    for (uint8_t** b : {&tw->sf_gate, &tw->sf_up, &tw->sf_down, &tw->sf_sh_gate, &tw->sf_sh_up, &tw->sf_sh_down}) {
+        if (*b) cudaFree(*b);
+        *b = nullptr;
+    }
+    err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTcSmemBytes);
     if (err != cudaSuccess) return err;
     tw->ready = true;
     return cudaSuccess;
@@ -874,9 +843,6 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
                           cudaStream_t st, const PhaseEvents* ev) {
     const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
     const int P = L.T * L.k;
-    // replicated B scales (if the handle keeps them) once an expert's weight tiles serve >= 4
-    // row blocks on average: the tensor pipe, not HBM, is then the limit
-    const bool rep = tw.sfp_gu != nullptr && (int64_t)P >= (int64_t)512 * L.E;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -919,21 +885,17 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
     g1.mode = 0;
     g1.tiles = B.tiles1; g1.num_tiles = B.meta + 0;
     g1.sfa = B.xsf; g1.sfa_kblocks = L.H / 64;
-    g1.sfb0 = tw.sf_gate; g1.sfb1 = tw.sf_up; g1.ssfb0 = tw.sf_sh_gate; g1.ssfb1 = tw.sf_sh_up;
-    g1.sfr = tw.sfp_gu; g1.ssfr = tw.sfp_sh_gu;
+    g1.sfb0 = tw.sfp_gu; g1.ssfb0 = tw.sfp_sh_gu;  // quarter tiles of gate | up
     g1.post0 = tw.post_gate; g1.post1 = tw.post_up; g1.spost0 = tw.post_sh_gate; g1.spost1 = tw.post_sh_up;
-    TC_PHASE(1, (rep ? tc_gemm_kernel<true><<<sms, kTcThreads, TcGeom<true>::kSmemBytes, st>>>(m1, g1)
-                     : tc_gemm_kernel<false><<<sms, kTcThreads, TcGeom<false>::kSmemBytes, st>>>(m1, g1)))
+    TC_PHASE(1, (tc_gemm_kernel<<<sms, kTcThreads, kTcSmemBytes, st>>>(m1, g1)))
 
     TcGemmParams g2 = g;
     g2.mode = 1;
     g2.tiles = B.tiles2; g2.num_tiles = B.meta + 1;
     g2.sfa = B.hsf; g2.sfa_kblocks = Imax / 64;
-    g2.sfb0 = tw.sf_down; g2.sfb1 = tw.sf_down; g2.ssfb0 = tw.sf_sh_down; g2.ssfb1 = tw.sf_sh_down;
-    g2.sfr = tw.sfp_dn; g2.ssfr = tw.sfp_sh_dn;
+    g2.sfb0 = tw.sfp_dn; g2.ssfb0 = tw.sfp_sh_dn;  // quarter tiles of down
     g2.post0 = tw.post_down; g2.post1 = tw.post_down; g2.spost0 = tw.post_sh_down; g2.spost1 = tw.post_sh_down;
-    TC_PHASE(2, (rep ? tc_gemm_kernel<true><<<sms, kTcThreads, TcGeom<true>::kSmemBytes, st>>>(m2, g2)
-                     : tc_gemm_kernel<false><<<sms, kTcThreads, TcGeom<false>::kSmemBytes, st>>>(m2, g2)))
+    TC_PHASE(2, (tc_gemm_kernel<<<sms, kTcThreads, kTcSmemBytes, st>>>(m2, g2)))
 
     TcCombineArgs ca{};
     ca.y = B.y; ca.ids = L.ids; ca.out = L.out; ca.T = L.T; ca.H = L.H; ca.k = L.k; ca.E = L.E;

@@ -18,7 +18,7 @@ class MoeLayer:
     def __init__(self, *, E, H, I, top_k, scoring, gate, up, down, I_shared=0, sh_gate=None,
                  sh_up=None, sh_down=None, w_router=None, correction_bias=None, tid2eid=None,
                  renormalize=True, routed_scaling=1.0, act=capi.MOE_ACT_BF16, g_act1=1.0,
-                 g_act2=1.0, zero_experts=0, tc_replicated_scales=False):
+                 g_act2=1.0, zero_experts=0):
         self.E, self.H, self.I, self.top_k, self.I_shared = E, H, I, top_k, I_shared
         self.zero_experts = zero_experts
         self.scoring, self.renormalize, self.routed_scaling = scoring, renormalize, routed_scaling
@@ -26,13 +26,13 @@ class MoeLayer:
         self.w_router, self.correction_bias, self.tid2eid = w_router, correction_bias, tid2eid
         self._weights = (gate, up, down, sh_gate, sh_up, sh_down)  # keep alive
         self.desc = capi.ffn_desc(E, H, I, top_k, I_shared, gate, up, down, sh_gate, sh_up, sh_down,
-                                  zero_experts, tc_replicated_scales)
+                                  zero_experts)
         self.handle = capi.moe_prepare_weights(self.desc)
         self._ws = None
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     @classmethod
-    def from_inputs(cls, inp: dict, device="cuda", tc_replicated_scales=False):
+    def from_inputs(cls, inp: dict, device="cuda"):
         """Build from a synth.make_inputs() dict (tensors moved to `device`)."""
         cfg = inp["cfg"]
 
@@ -49,7 +49,7 @@ class MoeLayer:
                    sh_up=dev(inp.get("sh_up")), sh_down=dev(inp.get("sh_down")),
                    w_router=opt("w_router"), correction_bias=opt("bias"), tid2eid=opt("tid2eid"),
                    renormalize=cfg.renorm, routed_scaling=cfg.scaling, act=cfg.act,
-                   zero_experts=cfg.zero_experts, tc_replicated_scales=tc_replicated_scales)
+                   zero_experts=cfg.zero_experts)
 
     def close(self):
         if self.handle:

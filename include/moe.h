@@ -87,12 +87,6 @@ typedef struct {
     moe_qtensor gate, up, down;
     moe_qtensor sh_gate, sh_up, sh_down;
     int32_t zero_experts;
-    /* 0 or 1.  1: moe_prepare_weights also keeps the FP4 tensor-core path's scale factors of the
-     * weights replicated for the four TMEM lane quarters -- 0.75 * E * I * H bytes more, half
-     * the packed weight size -- and launches with >= 512 routed pairs per expert on average
-     * (T * top_k >= 512 * E: compute-bound prefill) use them, trading memory for tensor-pipe
-     * time.  0: only the compact tiles (0.1875 * E * I * H bytes). */
-    int32_t tc_replicated_scales;
 } moe_ffn_desc;
 
 /* Routing of T tokens over E real experts and zero_experts zero-computation experts (ids
@@ -144,7 +138,8 @@ moe_status_t moe_workspace_size(const moe_ffn_desc* desc, int32_t T, int32_t act
 
 /* One-time weight preparation: validates the descriptor, derives per-tensor post-scales
  * (the NVFP4 globals; for MXFP4 a power-of-two exponent offset) and the scale-factor
- * tiles of the FP4 tensor-core path (compact, and replicated when desc->tc_replicated_scales).  The weight buffers must stay alive and unchanged until
+ * tiles of the FP4 tensor-core path (3 * E * I * H / 16 bytes: the weights' scales in the
+ * order the tensor-core kernel copies them to TMEM).  The weight buffers must stay alive and unchanged until
  * moe_release_weights.  Allocates device memory and synchronises `stream` before returning. */
 moe_status_t moe_prepare_weights(const moe_ffn_desc* desc, void** handle_out, void* stream);
 moe_status_t moe_release_weights(void* handle);

@@ -54,11 +54,9 @@ def test_workspace_size_and_validation(lib):
                  for T in (1, 8, 9, 64, 1000)]
         assert all(a <= b for a, b in zip(sizes[2:], sizes[3:]))
     assert capi.moe_workspace_size(_fake_desc(k=9, Z=2), 4, 0) > 0  # k <= E + Z is fine
-    rep2 = _fake_desc()
-    rep2.tc_replicated_scales = 2  # only 0 or 1
     for bad in [_fake_desc(E=0), _fake_desc(E=513), _fake_desc(k=9), _fake_desc(k=0),
                 _fake_desc(H=200), _fake_desc(I=64), _fake_desc(Is=100), _fake_desc(Z=-1),
-                _fake_desc(E=510, Z=3), rep2]:
+                _fake_desc(E=510, Z=3)]:
         with pytest.raises(capi.MoeError) as ei:
             capi.moe_workspace_size(bad, 4, 0)
         assert ei.value.status == capi.MOE_ERR_INVALID_ARG

@@ -68,18 +68,17 @@ SMALL = {
     "tc_mx_hash": S.MoeConfig("tc_mx_hash", T=64, H=512, I=512, E=16, k=6, scoring=S.SCORE_HASH,
                               I_shared=512, fmt=S.FMT_MXFP4, shared_fmt=S.FMT_NVFP4, vocab=500,
                               act=S.ACT_NVFP4),
-    # >= 512 routed rows per expert: B's scales come as replicated pair tiles
-    "tc_rep": S.MoeConfig("tc_rep", T=1100, H=512, I=256, E=4, k=2, scoring=S.SCORE_SIGMOID,
+    # >= 512 routed rows per expert: each expert's weight tiles serve several row blocks
+    "tc_many": S.MoeConfig("tc_many", T=1100, H=512, I=256, E=4, k=2, scoring=S.SCORE_SIGMOID,
                           scaling=2.5, I_shared=256, act=S.ACT_NVFP4),
-    "tc_rep_mx": S.MoeConfig("tc_rep_mx", T=1040, H=768, I=512, E=4, k=2,
+    "tc_many_mx": S.MoeConfig("tc_many_mx", T=1040, H=768, I=512, E=4, k=2,
                              scoring=S.SCORE_SOFTMAX, I_shared=256, fmt=S.FMT_MXFP4,
                              shared_fmt=S.FMT_NVFP4, act=S.ACT_NVFP4),
 }
 
 
 def _run(cfg, inp, with_logits=False):
-    # the handle keeps replicated scale tiles for the cases meant to use them
-    layer = MoeLayer.from_inputs(inp, tc_replicated_scales=cfg.name.startswith("tc_rep"))
+    layer = MoeLayer.from_inputs(inp)
     x = inp["x"].cuda()
     tok = inp["token_ids"].cuda() if "token_ids" in inp else None
     ids, w, logits = layer.route(x, token_ids=tok)
