@@ -42,13 +42,14 @@ DEFAULT_CONFIG = "dec1"
 FALLBACK_HBM_GBS = 6800.0
 
 # ncu DRAM traffic (read + write bytes per launch) of the dominant kernel, keyed by workload,
-# with the hash of the kernel source it was captured on; reported only while the hash matches.
-TRAFFIC = {"dec1": (14213376, "1be2f2ccf2feb1fc")}  # profiles/expert_mma_dec1.md
+# with the hash of that kernel's sources when it was captured; reported only while it matches.
+DECODE_SOURCES = ("decode_kernel.cuh", "decode_t1.cu", "topk.cuh", "frag.cuh", "common.cuh")
+TRAFFIC = {"dec1": (21877760 + 1536, "df65e1498ea2565c", DECODE_SOURCES)}  # profiles/dec_fused_dec1.md
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files) -> str:
     h = hashlib.sha256()
-    for f in ("ffn.cu", "common.cuh", "kernels.h"):
+    for f in files:
         with open(os.path.join(ROOT, "block_quantized_moe_router_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -443,9 +444,8 @@ def run_ours(args, cfg):
         fp4_peak = bf16_peak * FP4_OVER_BF16
         tflops = dom_flops / (dom_ms * 1e-3) / 1e12
         layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
-        src = kernel_source_hash()
         tr = TRAFFIC.get(cfg.name)
-        traffic = tr[0] if tr and tr[1] == src else None
+        traffic = tr[0] if tr and tr[1] == kernel_source_hash(tr[2]) else None
         line = {
             "metric": METRIC, "value": job_tokens_per_s(T, world, ms * 1e-3), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
