@@ -43,8 +43,12 @@ FALLBACK_HBM_GBS = 6800.0
 
 # ncu DRAM traffic (read + write bytes per launch) of the dominant kernel, keyed by workload,
 # with the hash of that kernel's sources when it was captured; reported only while it matches.
-DECODE_SOURCES = ("decode_kernel.cuh", "decode_t1.cu", "topk.cuh", "frag.cuh", "common.cuh")
-TRAFFIC = {"dec1": (21877760 + 1536, "df65e1498ea2565c", DECODE_SOURCES)}  # profiles/dec_fused_dec1.md
+KERNEL_SOURCES = {
+    "decode": ("decode_kernel.cuh", "decode_t1.cu", "topk.cuh", "frag.cuh", "common.cuh"),
+    "tc": ("prefill_tc.cu", "tc_ptx.cuh", "common.cuh"),
+    "mma": ("ffn.cu", "frag.cuh", "common.cuh"),
+}
+TRAFFIC = {"dec1": (21877760 + 1536, "df65e1498ea2565c")}  # profiles/dec_fused_dec1.md
 
 
 def kernel_source_hash(files) -> str:
@@ -444,8 +448,10 @@ def run_ours(args, cfg):
         fp4_peak = bf16_peak * FP4_OVER_BF16
         tflops = dom_flops / (dom_ms * 1e-3) / 1e12
         layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
+        src = kernel_source_hash(KERNEL_SOURCES["decode" if dec else
+                                                "tc" if cfg.act == synth.ACT_NVFP4 else "mma"])
         tr = TRAFFIC.get(cfg.name)
-        traffic = tr[0] if tr and tr[1] == kernel_source_hash(tr[2]) else None
+        traffic = tr[0] if tr and tr[1] == src else None
         line = {
             "metric": METRIC, "value": job_tokens_per_s(T, world, ms * 1e-3), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
