@@ -227,7 +227,7 @@ def cpu_baseline(cfg, inp_np, budget_s=10.0):
     while True:
         oracle_step(cfg, inp_np, tokens)
         done += len(tokens)
-        if time.perf_counter() - t0 >= budget_s or done >= 64 * cfg.T:
+        if time.perf_counter() - t0 >= budget_s:  # the same tokens again until the budget is spent
             break
     dt = time.perf_counter() - t0
     return {"value": done / dt, "unit": "tokens/s", "cores": min(threads, len(tokens)), "kind": "oracle",
