@@ -510,12 +510,13 @@ def host_inputs_from(inp):
 
 def launches_per_step(cfg):
     """Kernels one step launches.  A few tokens: one persistent kernel.  Otherwise router
-    GEMM + top-K (or the hash lookup), then the FFN: tcgen05 path -- prep, token quantizer,
-    row gather, gate+up GEMM, down GEMM, combine; mma path -- prep, gate+up, down, combine."""
+    GEMM + top-K (or the hash lookup), then the FFN: tcgen05 path -- histogram, scan, scatter,
+    token quantizer, row gather, gate+up GEMM, down GEMM, combine; mma path -- prep, gate+up,
+    down, combine."""
     if is_decode(cfg):
         return 1
     route = 1 if cfg.scoring == synth.SCORE_HASH else 2
-    return route + (6 if cfg.act == synth.ACT_NVFP4 else 4)
+    return route + (8 if cfg.act == synth.ACT_NVFP4 else 4)
 
 
 def main():

@@ -302,6 +302,7 @@ moe_status_t moe_ffn_forward(const void* handle, int32_t T, int32_t act, float g
         TcBuffers B{};
         B.meta = L.meta;
         B.mblock_expert = reinterpret_cast<int32_t*>(base + ws.mblock_expert);
+        B.scan = reinterpret_cast<int32_t*>(base + ws.tscan);
         B.padrow_pair = reinterpret_cast<int32_t*>(base + ws.padrow_pair);
         B.tiles1 = reinterpret_cast<int4*>(base + ws.tiles1);
         B.tiles2 = reinterpret_cast<int4*>(base + ws.tiles2);

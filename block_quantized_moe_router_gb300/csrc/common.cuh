@@ -184,7 +184,7 @@ inline int select_path(int T, int H, int top_k, int act, bool tc_shape) {
 struct Workspace {
     size_t counts, offsets, active, meta, sorted_pair, pos_of_pair, x16, xq, xs, h16, hq, hs, y;
     // tcgen05 path
-    size_t mblock_expert, padrow_pair, tiles1, tiles2, tokq, toks, txq, txsf, thq, thsf, ybf;
+    size_t mblock_expert, padrow_pair, tiles1, tiles2, tokq, toks, txq, txsf, thq, thsf, ybf, tscan;
     int max_blocks;
     size_t total;
     static Workspace plan(int E, int H, int I, int I_shared, int top_k, int T, int act, int path) {
@@ -222,6 +222,7 @@ struct Workspace {
             const size_t active = (size_t)E < P ? (size_t)E : P;
             w.max_blocks = (int)((P + 127) / 128 + active + (I_shared > 0 ? (T + 127) / 128 : 0));
             const size_t rows = (size_t)w.max_blocks * 128;
+            w.tscan = take(sizeof(int32_t) * 5 * ((size_t)E + 2));  // counts, bases, cursors
             w.mblock_expert = take(sizeof(int32_t) * w.max_blocks);
             w.padrow_pair = take(sizeof(int32_t) * rows);
             w.tiles1 = take(16 * (size_t)w.max_blocks * (Imax / 128));

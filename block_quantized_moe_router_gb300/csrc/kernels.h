@@ -80,6 +80,7 @@ struct TcWeights {
 };
 struct TcBuffers {  // workspace views
     int32_t *meta, *mblock_expert, *padrow_pair;
+    int32_t* scan;  // 5 x (E + 2): counts, 128-row block bases, tile bases (gate+up, down), cursors
     int4 *tiles1, *tiles2;
     uint8_t *tokq, *toks;  // tokens quantized once: codes [T][H/2], scales [T][H/16]
     uint8_t *xq, *xsf, *hq, *hsf;
@@ -92,6 +93,7 @@ struct TcPrepArgs {
     int32_t* status;
     int32_t *meta, *mblock_expert, *padrow_pair;
     int4 *tiles1, *tiles2;
+    int32_t* scan;
 };
 struct TcQuantArgs {
     const void* x;

@@ -7,10 +7,11 @@
 // run it as warp-level MMAs on GB10, here it is tcgen05 with operands staged by TMA.
 //
 // Data flow (every step on the device, no host synchronisation):
-//   tc_prep_kernel   histogram of the routed pairs, expert rows padded to 128 (one MMA M tile),
-//                    padded-row -> pair map, per-128-row block -> expert map, and the two tile
-//                    lists (expert-major, then N block, then M block, so that concurrently
-//                    running CTAs share one expert's weight tile through L2);
+//   tc_hist_kernel / tc_scan_kernel / tc_scatter_kernel  histogram of the routed pairs,
+//                    expert rows padded to 128 (one MMA M tile), padded-row -> pair map,
+//                    per-128-row block -> expert map, and the two tile lists (expert-major,
+//                    then N block, then M block, so that concurrently running CTAs share one
+//                    expert's weight tile through L2);
 //   tc_quant_tokens_kernel / tc_gather_rows_kernel  NVFP4 quantization of every token once,
 //                    then a copy of each pair's token row into its padded row with the scales
 //                    rearranged into the 128 x 4 scale-factor tile layout of the MMA;
@@ -22,13 +23,16 @@
 //   tc_combine_kernel  out[t] = sum_j y[t, j] + y_shared[t].
 //
 // The GEMM kernel is persistent (one CTA per SM, tiles strided by the grid) and warp
-// specialised: warp 0 issues TMA / bulk copies into a 4-stage shared-memory ring, warp 1
+// specialised: warp 0 issues TMA / bulk copies into a 3-stage shared-memory ring, warp 1
 // allocates TMEM and one of its lanes issues tcgen05.cp (scale factors) and tcgen05.mma,
-// warps 2-5 drain the accumulator with tcgen05.ld.  Every mbarrier wait is bounded; a wait
+// warps 2-9 drain the accumulator with tcgen05.ld.  Every mbarrier wait is bounded; a wait
 // that gives up sets MOE_DEV_TIMEOUT, the CTA stops issuing work, waits (bounded) for its
-// copies and MMAs in flight, frees TMEM and returns.
+// copies and MMAs in flight, frees TMEM and returns.  The file also holds the many-token
+// router GEMM on the tensor cores (tcgen05.mma.kind::f16, bf16 in, fp32 logits).
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -67,72 +71,124 @@ __host__ __device__ __forceinline__ int sf_tile_offset(int r, int j) {
 }
 
 // ------------------------------------------------------------------------------------------
-// dispatch + tile lists (one CTA)
+// dispatch + tile lists: a histogram over many CTAs, a one-warp scan, then the scatter of the
+// pairs into their experts' padded rows, the padding marks, the block -> expert map and both
+// tile lists over many CTAs.  a.scan holds 5 arrays of E + 2: per-expert counts (zeroed before
+// the histogram; entry E = the shared expert), 128-row block bases, gate+up and down tile
+// bases, and row cursors.
 // ------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) tc_prep_kernel(TcPrepArgs a) {
-    __shared__ int cnt[kMaxExperts + 1];
-    __shared__ int cursor[kMaxExperts + 1];
-    __shared__ int mbase[kMaxExperts + 2];
-    __shared__ int tb1[kMaxExperts + 2];
-    __shared__ int tb2[kMaxExperts + 2];
-    const int tid = threadIdx.x, E = a.E, P = a.T * a.k;
-    for (int e = tid; e <= E; e += blockDim.x) cnt[e] = 0;
+struct TcScan {
+    int32_t *cnt, *mbase, *tb1, *tb2, *cursor;
+    __device__ TcScan(int32_t* s, int E)
+        : cnt(s), mbase(s + (E + 2)), tb1(s + 2 * (E + 2)), tb2(s + 3 * (E + 2)), cursor(s + 4 * (E + 2)) {}
+};
+
+__device__ __forceinline__ bool tc_routed(int e, int E) { return e >= 0 && e < E; }
+
+__global__ void __launch_bounds__(1024) tc_hist_kernel(TcPrepArgs a) {
+    __shared__ int cnt[kMaxExperts];
+    const int E = a.E, P = a.T * a.k;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     int bad = 0;
-    for (int p = tid; p < P; p += blockDim.x) {
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
         const int e = a.ids[p];
-        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        if (tc_routed(e, E)) atomicAdd(&cnt[e], 1);
         else if (e != -1 && !(e >= E && e < E + a.Z)) bad = 1;  // zero-computation experts are valid
     }
     if (bad) status_or(a.status, MOE_DEV_BAD_EXPERT_ID);
     __syncthreads();
-    if (tid == 0) cnt[E] = a.has_shared ? a.T : 0;  // the shared expert takes every token
-    __syncthreads();
-    if (tid < 32) {  // exclusive scans over E + 1 entries (routed experts, then shared)
-        const int lane = tid, n = E + 1, per = (n + 31) / 32;
-        const int lo = min(n, lane * per), hi = min(n, lo + per);
-        int smb = 0, st1 = 0, st2 = 0;
-        for (int e = lo; e < hi; ++e) {
-            const int nmb = (cnt[e] + 127) / 128;
-            const int nb1 = (e < E ? a.I : a.I_shared) / 128;
-            smb += nmb;
-            st1 += nmb * nb1;
-            st2 += nmb * (a.H / 256);
-        }
-        int i_mb = smb, i_t1 = st1, i_t2 = st2;
+    TcScan S(a.scan, E);
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (cnt[e]) atomicAdd(&S.cnt[e], cnt[e]);
+}
+
+// one warp: exclusive scans over E + 1 entries (routed experts, then the shared one)
+__global__ void __launch_bounds__(32) tc_scan_kernel(TcPrepArgs a) {
+    const int E = a.E, lane = threadIdx.x, n = E + 1, per = (n + 31) / 32;
+    TcScan S(a.scan, E);
+    if (lane == 0) S.cnt[E] = a.has_shared ? a.T : 0;  // the shared expert takes every token
+    __syncwarp();
+    const int lo = min(n, lane * per), hi = min(n, lo + per);
+    int smb = 0, st1 = 0, st2 = 0;
+    for (int e = lo; e < hi; ++e) {
+        const int nmb = (S.cnt[e] + 127) / 128;
+        smb += nmb;
+        st1 += nmb * ((e < E ? a.I : a.I_shared) / 128);
+        st2 += nmb * (a.H / 256);
+    }
+    int i_mb = smb, i_t1 = st1, i_t2 = st2;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, i_mb, o);
-            const int y = __shfl_up_sync(0xffffffffu, i_t1, o);
-            const int z = __shfl_up_sync(0xffffffffu, i_t2, o);
-            if (lane >= o) { i_mb += x; i_t1 += y; i_t2 += z; }
-        }
-        int b = i_mb - smb, t1 = i_t1 - st1, t2 = i_t2 - st2;
-        for (int e = lo; e < hi; ++e) {
-            const int nmb = (cnt[e] + 127) / 128;
-            const int nb1 = (e < E ? a.I : a.I_shared) / 128;
-            mbase[e] = b;
-            tb1[e] = t1;
-            tb2[e] = t2;
-            cursor[e] = b * 128;
-            b += nmb;
-            t1 += nmb * nb1;
-            t2 += nmb * (a.H / 256);
-        }
-        if (lane == 31) {
-            mbase[n] = i_mb;
-            tb1[n] = i_t1;
-            tb2[n] = i_t2;
-            a.meta[0] = i_t1;       // gate+up tiles
-            a.meta[1] = i_t2;       // down tiles
-            a.meta[2] = i_mb * 128; // padded rows in use
-            a.meta[3] = i_mb;       // 128-row blocks in use
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, i_mb, o);
+        const int y = __shfl_up_sync(0xffffffffu, i_t1, o);
+        const int z = __shfl_up_sync(0xffffffffu, i_t2, o);
+        if (lane >= o) { i_mb += x; i_t1 += y; i_t2 += z; }
+    }
+    int b = i_mb - smb, t1 = i_t1 - st1, t2 = i_t2 - st2;
+    for (int e = lo; e < hi; ++e) {
+        const int nmb = (S.cnt[e] + 127) / 128;
+        S.mbase[e] = b;
+        S.tb1[e] = t1;
+        S.tb2[e] = t2;
+        S.cursor[e] = b * 128;
+        b += nmb;
+        t1 += nmb * ((e < E ? a.I : a.I_shared) / 128);
+        t2 += nmb * (a.H / 256);
+    }
+    if (lane == 31) {
+        S.mbase[n] = i_mb;
+        S.tb1[n] = i_t1;
+        S.tb2[n] = i_t2;
+        a.meta[0] = i_t1;        // gate+up tiles
+        a.meta[1] = i_t2;        // down tiles
+        a.meta[2] = i_mb * 128;  // padded rows in use
+        a.meta[3] = i_mb;        // 128-row blocks in use
+    }
+}
+
+__global__ void __launch_bounds__(1024) tc_scatter_kernel(TcPrepArgs a) {
+    __shared__ int cnt[kMaxExperts + 1];
+    __shared__ int mbase[kMaxExperts + 2];
+    __shared__ int tb1[kMaxExperts + 2];
+    __shared__ int tb2[kMaxExperts + 2];
+    __shared__ int lcur[kMaxExperts];
+    const int tid = threadIdx.x, E = a.E, P = a.T * a.k;
+    TcScan S(a.scan, E);
+    for (int e = tid; e <= E + 1; e += blockDim.x) {
+        if (e <= E) cnt[e] = S.cnt[e];
+        mbase[e] = S.mbase[e];
+        tb1[e] = S.tb1[e];
+        tb2[e] = S.tb2[e];
+        if (e < E) lcur[e] = 0;
     }
     __syncthreads();
+    // this CTA's contiguous share of the pairs: count per expert, reserve a range of rows per
+    // expert with one global atomic, then place each pair inside its range
+    const int chunk = (P + gridDim.x - 1) / gridDim.x;
+    const int p0 = min(P, blockIdx.x * chunk), p1 = min(P, p0 + chunk);
+    for (int p = p0 + tid; p < p1; p += blockDim.x) {
+        const int e = a.ids[p];
+        if (tc_routed(e, E)) atomicAdd(&lcur[e], 1);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x)
+        if (lcur[e]) lcur[e] = atomicAdd(&S.cursor[e], lcur[e]);
+    __syncthreads();
+    for (int p = p0 + tid; p < p1; p += blockDim.x) {
+        const int e = a.ids[p];
+        if (tc_routed(e, E)) a.padrow_pair[atomicAdd(&lcur[e], 1)] = p;
+    }
+    const int g = blockIdx.x * blockDim.x + tid, G = gridDim.x * blockDim.x;
+    if (a.has_shared)
+        for (int t = g; t < a.T; t += G) a.padrow_pair[mbase[E] * 128 + t] = P + t;
+    // the unused tail of each expert's last block (fewer than 128 rows)
+    for (int i = g; i < (E + 1) * 128; i += G) {
+        const int e = i >> 7, row = mbase[e] * 128 + cnt[e] + (i & 127);
+        if (row < mbase[e + 1] * 128) a.padrow_pair[row] = -1;
+    }
     const int nblocks = mbase[E + 1];
-    for (int r = tid; r < nblocks * 128; r += blockDim.x) a.padrow_pair[r] = -1;
-    for (int b = tid; b < nblocks; b += blockDim.x) {
+    for (int b = g; b < nblocks; b += G) {
         int lo = 0, hi = E + 1;  // largest e with mbase[e] <= b
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -140,19 +196,12 @@ __global__ void __launch_bounds__(1024) tc_prep_kernel(TcPrepArgs a) {
         }
         a.mblock_expert[b] = lo;
     }
-    __syncthreads();
-    for (int p = tid; p < P; p += blockDim.x) {
-        const int e = a.ids[p];
-        if (e >= 0 && e < E) a.padrow_pair[atomicAdd(&cursor[e], 1)] = p;
-    }
-    if (a.has_shared)
-        for (int t = tid; t < a.T; t += blockDim.x) a.padrow_pair[mbase[E] * 128 + t] = P + t;
     // tile lists: entry = (128-row block, N block, expert (E = shared), K stages)
     for (int pass = 0; pass < 2; ++pass) {
         const int* tb = pass == 0 ? tb1 : tb2;
         int4* out = pass == 0 ? a.tiles1 : a.tiles2;
         const int total = tb[E + 1];
-        for (int t = tid; t < total; t += blockDim.x) {
+        for (int t = g; t < total; t += G) {
             int lo = 0, hi = E + 1;  // largest e with tb[e] <= t and a nonzero range
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
@@ -184,39 +233,64 @@ __global__ void __launch_bounds__(256) tc_quant_tokens_kernel(TcQuantArgs a) {
     }
 }
 
-// one warp per padded row: 16-byte copies of the codes, 4-byte scale groups into the tiles
-__global__ void __launch_bounds__(256) tc_gather_rows_kernel(TcQuantArgs a) {
-    const int rows = a.meta[2];
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    const int lane = threadIdx.x & 31;
-    for (int prow = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); prow < rows; prow += warps) {
-        const int p = a.padrow_pair[prow];
-        if (p < 0) continue;
-        const int t = p < a.P ? p / a.k : p - a.P;
-        const uint4* src = reinterpret_cast<const uint4*>(a.tokq + (size_t)t * (a.H / 2));
-        uint4* dst = reinterpret_cast<uint4*>(a.xq + (size_t)prow * (a.H / 2));
-        for (int c = lane; c < a.H / 32; c += 32) dst[c] = src[c];
-    }
-    // scale tiles: one thread per 16-byte line (line l of K block kb holds the 4 scales of rows
-    // l, l + 32, l + 64, l + 96), so a warp writes 512 contiguous bytes; rows without a pair
-    // get zero scales
-    const int KB = a.H / 64;
-    const int64_t lines = (int64_t)a.meta[3] * KB * 32;
+// One CTA per 128-row block in use (grid-strided).  Codes: the block's rows are one flat range
+// of 16-byte words, each thread keeping 8 loads in flight.  Scales: per chunk of 32 K blocks,
+// each row's 4-byte scale groups are read as one 128-byte run into shared memory and written
+// out as the tile lines (line l of K block kb holds the scales of rows l, l + 32, l + 64,
+// l + 96; 512 contiguous bytes per K block).  Rows without a pair keep whatever codes they
+// had and get zero scales, so they contribute nothing.
+constexpr int kGatherThreads = 256;
+__global__ void __launch_bounds__(kGatherThreads) tc_gather_rows_kernel(TcQuantArgs a) {
+    __shared__ int tok[128];
+    __shared__ uint32_t sw[128][33];
+    const int nblk = a.meta[3];
+    const int KB = a.H / 64, wpr = a.H / 32;  // K blocks, 16-byte code words per row
+    const int total = 128 * wpr;
     const uint32_t* toks32 = reinterpret_cast<const uint32_t*>(a.toks);
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < lines;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int l = (int)(i & 31);
-        const int64_t bk = i >> 5;
-        const int mb = (int)(bk / KB), kb = (int)(bk - (int64_t)mb * KB);
-        uint32_t w[4];
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
-            const int p = a.padrow_pair[mb * 128 + 32 * qd + l];
-            const int t = p < a.P ? p / a.k : p - a.P;
-            w[qd] = p < 0 ? 0u : toks32[(size_t)t * KB + kb];
+    const uint4* src = reinterpret_cast<const uint4*>(a.tokq);
+    for (int mb = blockIdx.x; mb < nblk; mb += gridDim.x) {
+        __syncthreads();  // the previous block's reads of tok[] and sw[] are done
+        if (threadIdx.x < 128) {
+            const int p = a.padrow_pair[mb * 128 + threadIdx.x];
+            tok[threadIdx.x] = p < 0 ? -1 : (p < a.P ? p / a.k : p - a.P);
         }
-        *reinterpret_cast<uint4*>(a.xsf + ((size_t)mb * KB + kb) * 512 + l * 16) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        __syncthreads();
+        uint4* dst = reinterpret_cast<uint4*>(a.xq + (size_t)mb * 128 * (a.H / 2));
+        for (int j0 = threadIdx.x; j0 < total; j0 += 8 * kGatherThreads) {
+            uint4 v[8];
+            int dj[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u * kGatherThreads;
+                dj[u] = -1;
+                if (j < total) {
+                    const int r = j / wpr;
+                    const int t = tok[r];
+                    if (t >= 0) {
+                        v[u] = src[(size_t)t * wpr + (j - r * wpr)];
+                        dj[u] = j;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (dj[u] >= 0) dst[dj[u]] = v[u];
+        }
+        for (int k0 = 0; k0 < KB; k0 += 32) {
+            const int nk = min(32, KB - k0);
+            for (int i = threadIdx.x; i < 128 * 32; i += kGatherThreads) {
+                const int r = i >> 5, kk = i & 31;
+                const int t = tok[r];
+                sw[r][kk] = (t < 0 || kk >= nk) ? 0u : toks32[(size_t)t * KB + k0 + kk];
+            }
+            __syncthreads();
+            for (int i = threadIdx.x; i < nk * 32; i += kGatherThreads) {
+                const int kk = i >> 5, l = i & 31;
+                *reinterpret_cast<uint4*>(a.xsf + ((size_t)mb * KB + k0 + kk) * 512 + l * 16) =
+                    make_uint4(sw[l][kk], sw[32 + l][kk], sw[64 + l][kk], sw[96 + l][kk]);
+            }
+            __syncthreads();
+        }
     }
 }
 
@@ -857,13 +931,17 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
     pa.ids = L.ids; pa.T = L.T; pa.k = L.k; pa.E = L.E; pa.Z = L.Z; pa.H = L.H; pa.I = L.I;
     pa.I_shared = L.I_shared; pa.has_shared = L.I_shared > 0; pa.status = L.status;
     pa.meta = B.meta; pa.mblock_expert = B.mblock_expert; pa.padrow_pair = B.padrow_pair;
-    pa.tiles1 = B.tiles1; pa.tiles2 = B.tiles2;
+    pa.tiles1 = B.tiles1; pa.tiles2 = B.tiles2; pa.scan = B.scan;
     TcQuantArgs qa{};
     qa.x = L.x; qa.T = L.T; qa.H = L.H; qa.k = L.k; qa.P = P; qa.g1 = L.g1; qa.meta = B.meta;
     qa.padrow_pair = B.padrow_pair; qa.tokq = B.tokq; qa.toks = B.toks; qa.xq = B.xq; qa.xsf = B.xsf;
-    TC_PHASE(0, (tc_prep_kernel<<<1, 1024, 0, st>>>(pa),
+    const int hist_ctas = (int)std::min<int64_t>(2 * sms, std::max<int64_t>(1, ((int64_t)P + 4095) / 4096));
+    if ((err = cudaMemsetAsync(B.scan, 0, sizeof(int32_t) * (L.E + 2), st)) != cudaSuccess) return err;
+    TC_PHASE(0, (tc_hist_kernel<<<hist_ctas, 1024, 0, st>>>(pa),
+                 tc_scan_kernel<<<1, 32, 0, st>>>(pa),
+                 tc_scatter_kernel<<<sms, 1024, 0, st>>>(pa),
                  tc_quant_tokens_kernel<<<sms * 8, 256, 0, st>>>(qa),
-                 tc_gather_rows_kernel<<<sms * 8, 256, 0, st>>>(qa)))
+                 tc_gather_rows_kernel<<<sms * 8, kGatherThreads, 0, st>>>(qa)))
 
     TcTensorMaps m1{}, m2{};
     const uint64_t rows = (uint64_t)B.max_blocks * 128;
