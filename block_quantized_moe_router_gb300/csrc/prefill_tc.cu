@@ -233,29 +233,34 @@ __global__ void __launch_bounds__(256) tc_quant_tokens_kernel(TcQuantArgs a) {
     }
 }
 
-// One CTA per 128-row block in use (grid-strided).  Codes: the block's rows are one flat range
-// of 16-byte words, each thread keeping 8 loads in flight.  Scales: per chunk of 32 K blocks,
-// each row's 4-byte scale groups are read as one 128-byte run into shared memory and written
-// out as the tile lines (line l of K block kb holds the scales of rows l, l + 32, l + 64,
-// l + 96; 512 contiguous bytes per K block).  Rows without a pair keep whatever codes they
-// had and get zero scales, so they contribute nothing.
+// Work items of (128-row block in use, chunk c of 32 K blocks), CTA-strided; with n chunks per
+// row an item copies the codes of rows [128 c / n, 128 (c + 1) / n) of its block and the
+// scales of its chunk.  Codes: one flat range of 16-byte words, each thread keeping 8 loads in
+// flight.  Scales: each row's 4-byte scale groups are read as one 128-byte run into shared
+// memory and written out as the tile lines (line l of K block kb holds the scales of rows l,
+// l + 32, l + 64, l + 96; 512 contiguous bytes per K block).  Rows without a pair keep
+// whatever codes they had and get zero scales, so they contribute nothing.
 constexpr int kGatherThreads = 256;
 __global__ void __launch_bounds__(kGatherThreads) tc_gather_rows_kernel(TcQuantArgs a) {
     __shared__ int tok[128];
     __shared__ uint32_t sw[128][33];
     const int nblk = a.meta[3];
     const int KB = a.H / 64, wpr = a.H / 32;  // K blocks, 16-byte code words per row
-    const int total = 128 * wpr;
+    const int nchunk = (KB + 31) / 32;
     const uint32_t* toks32 = reinterpret_cast<const uint32_t*>(a.toks);
     const uint4* src = reinterpret_cast<const uint4*>(a.tokq);
-    for (int mb = blockIdx.x; mb < nblk; mb += gridDim.x) {
-        __syncthreads();  // the previous block's reads of tok[] and sw[] are done
+    for (int item = blockIdx.x; item < nblk * nchunk; item += gridDim.x) {
+        const int mb = item / nchunk, c = item - mb * nchunk;
+        const int r0 = 128 * c / nchunk, r1 = 128 * (c + 1) / nchunk;
+        const int k0 = 32 * c, nk = min(32, KB - k0);
+        __syncthreads();  // the previous item's reads of tok[] and sw[] are done
         if (threadIdx.x < 128) {
             const int p = a.padrow_pair[mb * 128 + threadIdx.x];
             tok[threadIdx.x] = p < 0 ? -1 : (p < a.P ? p / a.k : p - a.P);
         }
         __syncthreads();
-        uint4* dst = reinterpret_cast<uint4*>(a.xq + (size_t)mb * 128 * (a.H / 2));
+        const int total = (r1 - r0) * wpr;
+        uint4* dst = reinterpret_cast<uint4*>(a.xq + ((size_t)mb * 128 + r0) * (a.H / 2));
         for (int j0 = threadIdx.x; j0 < total; j0 += 8 * kGatherThreads) {
             uint4 v[8];
             int dj[8];
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(kGatherThreads) tc_gather_rows_kernel(TcQuantA
                 dj[u] = -1;
                 if (j < total) {
                     const int r = j / wpr;
-                    const int t = tok[r];
+                    const int t = tok[r0 + r];
                     if (t >= 0) {
                         v[u] = src[(size_t)t * wpr + (j - r * wpr)];
                         dj[u] = j;
@@ -276,20 +281,16 @@ __global__ void __launch_bounds__(kGatherThreads) tc_gather_rows_kernel(TcQuantA
             for (int u = 0; u < 8; ++u)
                 if (dj[u] >= 0) dst[dj[u]] = v[u];
         }
-        for (int k0 = 0; k0 < KB; k0 += 32) {
-            const int nk = min(32, KB - k0);
-            for (int i = threadIdx.x; i < 128 * 32; i += kGatherThreads) {
-                const int r = i >> 5, kk = i & 31;
-                const int t = tok[r];
-                sw[r][kk] = (t < 0 || kk >= nk) ? 0u : toks32[(size_t)t * KB + k0 + kk];
-            }
-            __syncthreads();
-            for (int i = threadIdx.x; i < nk * 32; i += kGatherThreads) {
-                const int kk = i >> 5, l = i & 31;
-                *reinterpret_cast<uint4*>(a.xsf + ((size_t)mb * KB + k0 + kk) * 512 + l * 16) =
-                    make_uint4(sw[l][kk], sw[32 + l][kk], sw[64 + l][kk], sw[96 + l][kk]);
-            }
-            __syncthreads();
+        for (int i = threadIdx.x; i < 128 * 32; i += kGatherThreads) {
+            const int r = i >> 5, kk = i & 31;
+            const int t = tok[r];
+            sw[r][kk] = (t < 0 || kk >= nk) ? 0u : toks32[(size_t)t * KB + k0 + kk];
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < nk * 32; i += kGatherThreads) {
+            const int kk = i >> 5, l = i & 31;
+            *reinterpret_cast<uint4*>(a.xsf + ((size_t)mb * KB + k0 + kk) * 512 + l * 16) =
+                make_uint4(sw[l][kk], sw[32 + l][kk], sw[64 + l][kk], sw[96 + l][kk]);
         }
     }
 }
