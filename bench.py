@@ -291,7 +291,6 @@ def run_ours(args, cfg):
     l2 = getattr(props, "L2_cache_size", 0) or 128 * 2 ** 20
 
     inp = synth.make_inputs(cfg, seed=rank, device="cuda")
-    # compute-bound prefill (>= 512 routed pairs per expert) keeps replicated scale tiles
     base = MoeLayer.from_inputs(inp)
     x = inp["x"].cuda()
     tok = inp["token_ids"].cuda() if "token_ids" in inp else None
