@@ -95,6 +95,18 @@ def max_over_ranks(values, dist=None, device="cpu"):
     return [float(v) for v in t.tolist()]
 
 
+def auto_steps(step_s, replicas, target_s=1.0, floor=2000, cap=2_000_000):
+    """Timed steps for about target_s of device time, given the seconds one step took in the
+    warm-up: at least floor, at most cap, a multiple of the replica count."""
+    try:
+        n = int(math.ceil(target_s / step_s))
+    except (ValueError, OverflowError, ZeroDivisionError):
+        n = floor
+    n = min(cap, max(floor, n))
+    r = max(1, int(replicas))
+    return -(-n // r) * r
+
+
 def job_tokens_per_s(tokens_per_rank, world, seconds):
     """Whole-job throughput under weak scaling: every rank processed its own batch."""
     return tokens_per_rank * world / seconds
@@ -112,8 +124,10 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.marks = []
 
     def start(self):
+        self.marks = []
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
@@ -123,6 +137,18 @@ class ClockSampler:
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            os.unlink(self.path)
+
+    def mark(self):
+        """Notes how many samples have been written so far; two marks bound the timed region."""
+        n = 0
+        try:
+            if self.proc is not None:
+                with open(self.path) as fh:
+                    n = sum(1 for line in fh if line.endswith("\n"))
+        except Exception:
+            n = 0
+        self.marks.append(n)
 
     def stop(self):
         if self.proc is None:
@@ -132,13 +158,18 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        rows = []
         with open(self.path) as fh:
-            for line in fh:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+            lines = fh.read().splitlines()
         os.unlink(self.path)
+        # the samples written between the two marks, if any landed there (nvidia-smi may
+        # buffer its output); otherwise every sample of the run
+        inside = len(self.marks) >= 2 and self.marks[1] > self.marks[0]
+        window = lines[self.marks[0]:self.marks[1]] if inside else lines
+        rows = []
+        for line in window:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -146,7 +177,8 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "window": "timed region" if inside else "whole run"}
 
 
 # ------------------------------------------------------------------------------------------
@@ -362,16 +394,25 @@ def run_ours(args, cfg):
     clocks = ClockSampler(local)
     clocks.start()
     with torch.cuda.stream(stream):
+        w0 = torch.cuda.Event(enable_timing=True)
+        w1 = torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
         run_steps(0, args.warmup)
+        w1.record(stream)
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        if args.steps is None:  # about one second of timed work, the same on every rank
+            steps = auto_steps(w0.elapsed_time(w1) * 1e-3 / args.warmup, replicas)
+            args.steps = int(max_over_ranks([steps], dist, device="cuda")[0])
         barrier()
         torch.cuda.synchronize()
+        clocks.mark()
         ev0.record(stream)
         run_steps(args.warmup, args.steps)
         ev1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark()
     barrier()
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -521,7 +562,8 @@ def launches_per_step(cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about one second of device time, at least 2000)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(synth.CONFIGS))
@@ -534,6 +576,8 @@ def main():
     args.warmup = max(3, args.warmup)
     cfg = synth.CONFIGS[args.config]
     if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 20
         run_reference(args, cfg)
     else:
         run_ours(args, cfg)
