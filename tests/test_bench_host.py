@@ -1,8 +1,7 @@
 """The benchmark's host-side helpers on CPU: the default step count (about one second of timed
-work) and the clock sampler's timed-region window, driven by a stand-in `nvidia-smi` that
-writes one CSV sample every 50 ms."""
+work) and the clock sampler's timed-region window, driven by a stand-in for `nvidia-smi` (a
+Python script run by this interpreter) that writes one CSV sample every 50 ms."""
 import os
-import stat
 import sys
 import time
 
@@ -27,28 +26,24 @@ def test_auto_steps():
 
 
 def _fake_smi(tmp_path, mhz_of_line):
-    """An executable named nvidia-smi that prints 9 CSV fields per line, one line per 50 ms,
-    flushing each (the SM clock of line i is mhz_of_line(i))."""
-    script = tmp_path / "nvidia-smi"
+    """The sampler command of a script that prints 9 CSV fields per line, one line per 50 ms,
+    flushing each (the SM clock of line i is mhz_of_line(i)); it ignores its arguments."""
+    script = tmp_path / "fake_smi.py"
     clocks = ", ".join(str(mhz_of_line(i)) for i in range(400))
     script.write_text(
-        "#!" + sys.executable + "\n"
         "import sys, time\n"
         f"clocks = [{clocks}]\n"
         "for i, c in enumerate(clocks):\n"
         "    print(f'0, {c}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, "
         "{\"Active\" if c < 1000 else \"Not Active\"}', flush=True)\n"
         "    time.sleep(0.05)\n")
-    script.chmod(script.stat().st_mode | stat.S_IEXEC)
-    return str(tmp_path)
+    return (sys.executable, str(script))
 
 
-def test_clock_window_keeps_the_timed_region(tmp_path, monkeypatch):
+def test_clock_window_keeps_the_timed_region(tmp_path):
     # idle clocks before the region, full clocks after line 10 (the sampler is started, then
     # the region is marked once the load runs)
-    d = _fake_smi(tmp_path, lambda i: 2070 if i >= 10 else 345)
-    monkeypatch.setenv("PATH", d + os.pathsep + os.environ.get("PATH", ""))
-    s = bench.ClockSampler(0)
+    s = bench.ClockSampler(0, cmd=_fake_smi(tmp_path, lambda i: 2070 if i >= 10 else 345))
     s.start()
     deadline = time.time() + 10
     while time.time() < deadline:  # wait until the idle lines have been written
@@ -66,13 +61,11 @@ def test_clock_window_keeps_the_timed_region(tmp_path, monkeypatch):
     assert out["reasons"] == []
 
 
-def test_clock_window_falls_back_to_the_whole_run(tmp_path, monkeypatch):
-    d = _fake_smi(tmp_path, lambda i: 345 if i == 0 else 2070)
-    monkeypatch.setenv("PATH", d + os.pathsep + os.environ.get("PATH", ""))
-    s = bench.ClockSampler(0)
+def test_clock_window_falls_back_to_the_whole_run(tmp_path):
+    s = bench.ClockSampler(0, cmd=_fake_smi(tmp_path, lambda i: 345 if i == 0 else 2070))
     s.start()
     s.mark()
-    s.mark()  # no sample between the marks
+    s.marks.append(s.marks[-1])  # no sample between the marks
     time.sleep(0.4)
     out = s.stop()
     assert out["window"] == "whole run"
@@ -80,9 +73,8 @@ def test_clock_window_falls_back_to_the_whole_run(tmp_path, monkeypatch):
     assert out["reasons"] == ["sw_power_cap"]  # line 0 reported it
 
 
-def test_clock_sampler_without_nvidia_smi(monkeypatch, tmp_path):
-    monkeypatch.setenv("PATH", str(tmp_path))
-    s = bench.ClockSampler(0)
+def test_clock_sampler_without_nvidia_smi(tmp_path):
+    s = bench.ClockSampler(0, cmd=(str(tmp_path / "no_such_program"),))
     s.start()
     s.mark()
     s.mark()
