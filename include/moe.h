@@ -190,7 +190,7 @@ moe_status_t moe_forward(const void* handle, const moe_route_desc* route, int32_
 moe_status_t moe_quantize_act_nvfp4(const void* x_bf16, int64_t rows, int64_t K, float g,
                                     uint8_t* packed, uint8_t* scales, void* stream);
 
-/* moe_ffn_forward without a caller-provided workspace.  The paper has no counterpart: this is
+/* moe_ffn_forward without a caller-provided workspace.  The pages have no counterpart: this is
  * for callers that cannot give the library device memory -- a host that freezes its device
  * memory plan at start-up and must see no cudaMalloc afterwards (cudaMalloc can synchronise
  * the device), or a plugin interface that passes tensors but no workspace or allocator.
