@@ -137,10 +137,11 @@ moe_status_t moe_route(const moe_route_desc* desc, const void* x_bf16, const flo
 moe_status_t moe_workspace_size(const moe_ffn_desc* desc, int32_t T, int32_t act, size_t* bytes);
 
 /* One-time weight preparation: validates the descriptor, derives per-tensor post-scales
- * (the NVFP4 globals; for MXFP4 a power-of-two exponent offset) and the scale-factor
- * tiles of the FP4 tensor-core path (3 * E * I * H / 16 bytes: the weights' scales in the
- * order the tensor-core kernel copies them to TMEM).  The weight buffers must stay alive and unchanged until
- * moe_release_weights.  Allocates device memory and synchronises `stream` before returning. */
+ * (the NVFP4 globals; for MXFP4 a power-of-two exponent offset) and the scale-factor tiles
+ * of the FP4 tensor-core path (3 * (E * I + I_shared) * H / 16 bytes: the weights' scales in
+ * the order the tensor-core kernel copies them to TMEM).  The weight buffers must stay alive
+ * and unchanged until moe_release_weights.  Allocates device memory and synchronises
+ * `stream` before returning. */
 moe_status_t moe_prepare_weights(const moe_ffn_desc* desc, void** handle_out, void* stream);
 moe_status_t moe_release_weights(void* handle);
 
