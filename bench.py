@@ -404,7 +404,10 @@ def run_ours(args, cfg):
         ev1 = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         if args.steps is None:  # about one second of timed work, the same on every rank
-            steps = auto_steps(w0.elapsed_time(w1) * 1e-3 / args.warmup, replicas)
+            try:
+                steps = auto_steps(w0.elapsed_time(w1) * 1e-3 / args.warmup, replicas)
+            except Exception:  # no usable warm-up timing: the fixed default
+                steps = 2000
             args.steps = int(max_over_ranks([steps], dist, device="cuda")[0])
         barrier()
         torch.cuda.synchronize()
