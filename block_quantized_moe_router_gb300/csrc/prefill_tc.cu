@@ -47,13 +47,15 @@ constexpr int kTcABytes = 128 * 128;          // 128 rows x 128 B (256 E2M1 code
 constexpr int kTcBBytes = 256 * 128;          // 256 rows x 128 B
 constexpr int kTcSfaBytes = 4 * 512;          // 4 K blocks of 64 x one 128-row scale tile
 constexpr int kTcSfaOff = kTcABytes + kTcBBytes;
-constexpr uint32_t kTcTmemCols = 512;         // 256 accumulator + up to 4 stages x 48 scale columns
-// B's scales reach TMEM as quarter tiles: a stage's scales, prepared once as one 4 KB tile
-// (the lines of both 128-row scale tiles of the 256 B rows for its 4 K blocks, as the 32 TMEM
-// lanes of one lane quarter read them), bulk-copied into each of the four lane quarters'
-// shared-memory slices (the three repeats hit L2), then one 128-lane copy per K block.  A
-// copy that replicates 32 lanes to the four quarters (`32x128b.warpx4`, used for A's scales)
-// costs the tensor pipe several times more.  3 stages of 66 KiB.
+constexpr uint32_t kTcTmemCols = 512;  // 256 accumulator + 3 stages x 48 scale columns, rounded
+                                       // up to the power of two an allocation takes
+// B's scales reach TMEM as quarter tiles: a stage's scales (for a 256-row block of B and its 4
+// K blocks, the 16-byte lines of both 128-row scale tiles in the order the 32 TMEM lanes of
+// one lane quarter read them) are prepared once as one 4 KB tile, bulk-copied into each of
+// the four lane quarters' shared-memory slices (the three repeats hit L2), then moved by one
+// 128-lane copy per K block.  A copy that replicates 32 lanes to the four quarters
+// (`32x128b.warpx4`, used for A's scales) costs the tensor pipe several times more.  3 stages
+// of 66 KiB.
 constexpr int kTcStages = 3;
 constexpr int kTcSfbBytes = 4 * 4096;
 constexpr int kTcSfbOff = kTcSfaOff + kTcSfaBytes;
