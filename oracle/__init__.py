@@ -25,6 +25,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "libmoe_oracle.so")
 _lib = None
 
 SCORE_SOFTMAX, SCORE_SIGMOID, SCORE_HASH, SCORE_SQRTSOFTPLUS, SCORE_SOFTMAX_BIAS = 0, 1, 2, 3, 4
+SCORE_HASH_SQRTSOFTPLUS = 5  # ids from the hash table, weights from sqrt(softplus) router scores
 FMT_NVFP4, FMT_MXFP4 = 0, 1
 
 

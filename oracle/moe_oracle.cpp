@@ -36,6 +36,10 @@
 //     renormalised over the selected set and multiplied by the routed scaling factor.
 //   - sqrt(softplus) routing is the sigmoid scheme with the score sqrt(log(1 + e^logit)).
 //   - hash routing weights are 1/top_k.
+//   - score-weighted hash routing (the hash layers of the family that ships both the hash and
+//     the sqrt(softplus) routing handles): ids from the table in table order, weight of pair
+//     j = sqrt(softplus(logit at id j)), renormalised over the token's kept pairs when asked,
+//     times the routed scaling; no correction bias, since nothing is selected.
 //   - softmax + bias routing: p = softmax over all router logits; selection ranks p + bias;
 //     weights are p (renormalised over the selected set when asked) times the routed scaling.
 //   - a zero-computation expert (id in [E, E + Z)) returns its input: it adds w * x, the
@@ -265,7 +269,8 @@ void orc_dequant(const uint8_t* packed, const uint8_t* scales, double global, in
 // ----- routing ------------------------------------------------------------------------------
 // scoring: 0 softmax, 1 sigmoid (+ correction bias for selection), 2 hash,
 // 3 sqrt(softplus) (+ correction bias for selection), 4 softmax (+ correction bias for
-// selection).  E here is the router width (real + zero-computation experts).
+// selection), 5 hash ids with sqrt(softplus) router-score weights.  E here is the router
+// width (real + zero-computation experts).
 // Inputs: either x_bf16 [T,H] + w_router_bf16 [E,H] (router GEMM) or logits_in f32 [T,E].
 // Outputs: logits_out [T,E] fp64 (may be null), ids [T,k], w [T,k] fp64, score_out [T,E]
 // fp64 selection score (may be null).  Returns 0, or -1 on an invalid argument.
@@ -279,7 +284,7 @@ int orc_route(int T, int E, int H, int k, int scoring, int renorm, double scalin
               double* logits_out, int32_t* ids, double* w, double* score_out, int32_t* status_out,
               int nthreads) {
     build_tables();
-    if (T < 0 || E <= 0 || k <= 0 || k > E || scoring < 0 || scoring > 4) return -1;
+    if (T < 0 || E <= 0 || k <= 0 || k > E || scoring < 0 || scoring > 5) return -1;
     std::vector<int32_t> tok_status(T, 0);
     if (scoring == 2) {
         for (int t = 0; t < T; ++t) {
@@ -317,6 +322,38 @@ int orc_route(int T, int E, int H, int k, int scoring, int renorm, double scalin
                 }
                 logit[e] = l;
                 if (logits_out) logits_out[t * E + e] = l;
+            }
+            if (scoring == 5) {
+                // the table chooses the experts (in its order); the router's sqrt(softplus)
+                // scores of those experts give the weights
+                const int64_t tok = token_ids[t];
+                if (score_out)
+                    for (int e = 0; e < E; ++e)
+                        score_out[t * E + e] = std::isfinite(logit[e]) ? sqrt_softplus(logit[e]) : 0.0;
+                if (tok < 0 || tok >= vocab) {
+                    tok_status[t] |= 2;
+                    for (int j = 0; j < k; ++j) { ids[t * k + j] = -1; w[t * k + j] = 0.0; }
+                    return;
+                }
+                std::vector<double> sj(k, 0.0);
+                double ssum = 0.0;
+                for (int j = 0; j < k; ++j) {
+                    const int64_t e = tid2eid[tok * k + j];
+                    if (e < 0 || e >= E) {
+                        tok_status[t] |= 1;
+                        ids[t * k + j] = -1;
+                        continue;
+                    }
+                    ids[t * k + j] = (int32_t)e;
+                    if (std::isfinite(logit[e])) sj[j] = sqrt_softplus(logit[e]);
+                    else tok_status[t] |= 4;
+                    ssum += sj[j];
+                }
+                for (int j = 0; j < k; ++j) {
+                    const double v = renorm ? (ssum > 0.0 ? sj[j] / ssum : 0.0) : sj[j];
+                    w[t * k + j] = v * scaling;
+                }
+                return;
             }
             bool nonfinite = false;
             double lmax = -INFINITY;

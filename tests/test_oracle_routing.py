@@ -189,3 +189,58 @@ def test_nonfinite_logits_rank_last(orc):
     assert r["status"] == 4
     r = orc.route(T=1, E=5, k=4, scoring=1, scaling=1.0, logits_in=logits)
     assert list(r["ids"][0])[:3] == [1, 4, 3] and r["w"][0][3] == 0.0
+
+
+def test_hash_with_sqrtsoftplus_weights(orc):
+    """Score-weighted hash routing (scoring 5): the table picks the experts, the router's
+    sqrt(softplus) scores weight them.  softplus(l) = a exactly when l = ln(e^a - 1), so the
+    scores of a = 1, 4, 9 are 1, 2, 3 and the renormalised weights are 1/6, 2/6, 3/6 (to the
+    float32 rounding of the logits, a few 1e-8)."""
+    a = np.array([1.0, 4.0, 9.0])
+    l = np.log(np.expm1(a))
+    E, k = 6, 3
+    logits = np.full((4, E), -3.0, np.float32)
+    logits[:, 4], logits[:, 1], logits[:, 5] = l[0], l[1], l[2]
+    tid2eid = np.array([[4, 1, 5], [5, 4, 1], [1, 9, 5], [4, 1, 5]], np.int64)  # row 2: a bad id
+    tok = np.array([0, 1, 2, 3], np.int32)
+    logits[3, 1] = np.nan                                   # a non-finite score at a chosen id
+    r = orc.route(T=4, E=E, k=k, scoring=5, renorm=True, scaling=2.0, logits_in=logits,
+                  tid2eid=tid2eid, token_ids=tok, vocab=4)
+    # ids in table order, bad entries dropped
+    assert r["ids"].tolist() == [[4, 1, 5], [5, 4, 1], [1, -1, 5], [4, 1, 5]]
+    assert np.allclose(r["w"][0], np.array([1, 2, 3]) / 6 * 2.0, rtol=0, atol=1e-6)
+    assert np.allclose(r["w"][1], np.array([3, 1, 2]) / 6 * 2.0, rtol=0, atol=1e-6)
+    # the dropped pair is left out of the renormalisation: scores 2 and 3 -> 2/5, 3/5
+    assert np.allclose(r["w"][2], np.array([2, 0, 3]) / 5 * 2.0, rtol=0, atol=1e-6)
+    # a NaN logit weighs 0 and the others renormalise among themselves: 1/4, 3/4
+    assert np.allclose(r["w"][3], np.array([1, 0, 3]) / 4 * 2.0, rtol=0, atol=1e-6)
+    assert r["status"] == (1 | 4)
+    # without renormalisation the weight is the score itself times the scaling
+    r_nr = orc.route(T=1, E=E, k=k, scoring=5, renorm=False, scaling=1.5, logits_in=logits[:1],
+                     tid2eid=tid2eid, token_ids=tok[:1], vocab=4)
+    assert np.allclose(r_nr["w"][0], np.array([1, 2, 3]) * 1.5, rtol=0, atol=1e-6)
+
+
+def test_hash_sqrtsoftplus_reduces_to_plain_hash(orc):
+    """With equal logits every kept pair scores alike, so the weights are the plain hash
+    weights scaling / k (the same ids, from the table path that uses no logits), and the
+    weights of every token sum to the scaling."""
+    rng = np.random.default_rng(21)
+    V, E, k, T = 50, 16, 4, 30
+    tid2eid = np.stack([rng.permutation(E)[:k] for _ in range(V)]).astype(np.int64)
+    tok = rng.integers(0, V, T).astype(np.int32)
+    flat = np.full((T, E), 0.7, np.float32)
+    a = orc.route(T=T, E=E, k=k, scoring=5, renorm=True, scaling=1.0, logits_in=flat,
+                  tid2eid=tid2eid, token_ids=tok, vocab=V)
+    b = orc.route(T=T, E=E, k=k, scoring=2, scaling=1.0, tid2eid=tid2eid, token_ids=tok, vocab=V)
+    assert np.array_equal(a["ids"], b["ids"])
+    assert np.allclose(a["w"], b["w"], rtol=0, atol=1e-15)
+    lg = (rng.standard_normal((T, E)) * 2).astype(np.float32)
+    c = orc.route(T=T, E=E, k=k, scoring=5, renorm=True, scaling=2.5, logits_in=lg,
+                  tid2eid=tid2eid, token_ids=tok, vocab=V)
+    assert np.array_equal(c["ids"], b["ids"])
+    assert np.allclose(c["w"].sum(1), 2.5, rtol=0, atol=1e-12)
+    # the weights follow the logits' order within a token (sqrt(softplus) is increasing)
+    for t in range(T):
+        lsel = lg[t, c["ids"][t]]
+        assert np.array_equal(np.argsort(lsel, kind="stable"), np.argsort(c["w"][t], kind="stable"))
