@@ -4,17 +4,20 @@ One step = one MoE layer forward (moe_forward: route + FFN) over one batch of T 
 tokens.  Steps cycle through L replicas of the layer's weights (distinct device copies, as the
 layers of a model would be) with L * touched-bytes >= 4 * L2, so every step streams its expert
 weights from HBM.  One CUDA graph holds one step of each replica in turn (as a serving engine
-captures the layers of a decode step in one graph) and is replayed; single-step graphs make
-up any remainder, so the timed region is exactly K steps, between a barrier + device
-synchronisation on both sides, timed with CUDA events on the launching stream, max over
-ranks.
+captures the layers of a step in one graph) and is replayed; single-step graphs make up any
+remainder, so a timed region is exactly K steps, between a barrier + device synchronisation on
+both sides, timed with CUDA events on the launching stream, max over ranks.  When K steps take
+less than about a second the region is repeated (each repetition again exactly K steps) and the
+median region is reported, so that the clock sampler sees the load.
 
-Prints one JSON line: MoE-layer tokens/s (whole job), the roofline of the dominant kernel
-(algorithmic bytes / its CUDA-event duration measured inside the timed region), the clocks
-seen during the timed region, an end-to-end figure through the public API with host buffers,
-and the CPU oracle's throughput on a bounded sample.
+The headline workload is the 4096-token prefill (the largest configuration); the same run adds
+one line per other workload (dec1, dec8, hash64, pre32768) under "per_workload".  Each line
+carries MoE-layer tokens/s (whole job), the roofline of the dominant kernel (algorithmic bytes
+or FLOPs / its CUDA-event duration inside the timed regions), the clocks seen during the timed
+regions, an end-to-end figure through the public API with host buffers, and (headline only) the
+CPU oracle's throughput on a bounded sample.
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config dec1] [--impl reference]
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config pre4096] [--impl reference]
 """
 from __future__ import annotations
 
@@ -38,17 +41,20 @@ import torch  # noqa: E402
 from block_quantized_moe_router_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s and achieved HBM GB/s or FP4 TFLOP/s vs GB300 peak"
-DEFAULT_CONFIG = "dec1"
+DEFAULT_CONFIG = "pre4096"
+PER_WORKLOAD = ("dec1", "dec8", "hash64", "pre32768")
 FALLBACK_HBM_GBS = 6800.0
 
-# ncu DRAM traffic (read + write bytes per launch) of the dominant kernel, keyed by workload,
-# with the hash of that kernel's sources when it was captured; reported only while it matches.
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum per launch) of each workload's
+# dominant kernel, with the hash of that kernel's sources when it was captured; reported only
+# while the hash still matches (null once the kernel has changed).
 KERNEL_SOURCES = {
-    "decode": ("decode_kernel.cuh", "decode_t1.cu", "topk.cuh", "frag.cuh", "common.cuh"),
-    "tc": ("prefill_tc.cu", "tc_ptx.cuh", "common.cuh"),
-    "mma": ("ffn.cu", "frag.cuh", "common.cuh"),
+    "decode": ("decode_kernel.cuh", "decode_t1.cu", "decode.cu", "topk.cuh", "frag.cuh",
+               "common.cuh"),
+    "tc": ("prefill_tc.cu", "tc_ptx.cuh", "quant.cuh", "common.cuh"),
+    "mma": ("ffn.cu", "frag.cuh", "quant.cuh", "common.cuh"),
 }
-TRAFFIC = {"dec1": (21877760 + 1536, "df65e1498ea2565c")}  # profiles/dec_fused_dec1.md
+TRAFFIC = {}
 
 
 def kernel_source_hash(files) -> str:
@@ -63,24 +69,26 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio (13.5 vs 2.25 PFLOP/s)
 
 
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
 def measured_peaks():
-    """(HBM GB/s, dense bf16 TFLOP/s burst, source) from MEASURED_PEAKS.json, else fallback."""
+    """HBM GB/s, dense bf16 TFLOP/s (burst and sustained) and their source, from
+    MEASURED_PEAKS.json, else the fallback figures."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    hbm, bf16, src = FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+    out = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+           "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS_SUSTAINED, "source": "fallback"}
     try:
         with open(path) as fh:
             d = json.load(fh)
-        for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+        if "hbm_gbs" in d:
+            out["hbm_gbs"], out["source"] = float(d["hbm_gbs"]), "measured"
+        for key in ("bf16_tflops", "bf16_tflops_sustained"):
             if key in d:
-                hbm, src = float(d[key]), "measured"
-                break
-        for key in ("bf16_tflops", "bf16_TFLOPs"):
-            if key in d:
-                bf16 = float(d[key])
-                break
+                out[key] = float(d[key])
     except Exception:
         pass
-    return hbm, bf16, src
+    return out
 
 
 # ------------------------------------------------------------------------------------------
@@ -219,14 +227,17 @@ def oracle_step(cfg, inp_np, tokens, n_threads=0):
     """One oracle layer pass over `tokens` (route + expert FFN + combine)."""
     import oracle
     x = inp_np["x"][tokens]
+    hash_kw = {}
+    if cfg.scoring in (synth.SCORE_HASH, synth.SCORE_HASH_SQRTSOFTPLUS):
+        hash_kw = dict(tid2eid=inp_np["tid2eid"], token_ids=inp_np["token_ids"][tokens],
+                       vocab=cfg.vocab)
     if cfg.scoring == synth.SCORE_HASH:
         r = oracle.route(T=len(tokens), E=cfg.E, k=cfg.k, scoring=2, scaling=cfg.scaling,
-                         tid2eid=inp_np["tid2eid"], token_ids=inp_np["token_ids"][tokens],
-                         vocab=cfg.vocab, nthreads=n_threads)
+                         nthreads=n_threads, **hash_kw)
     else:
         r = oracle.route(T=len(tokens), E=cfg.E, k=cfg.k, scoring=cfg.scoring, renorm=cfg.renorm,
                          scaling=cfg.scaling, x_bf16=x, w_router_bf16=inp_np["w_router"],
-                         bias=inp_np.get("bias"), nthreads=n_threads)
+                         bias=inp_np.get("bias"), nthreads=n_threads, **hash_kw)
     return oracle.moe_ffn(T=len(tokens), E=cfg.E, H=cfg.H, I=cfg.I, k=cfg.k, gate=inp_np["gate"],
                           up=inp_np["up"], down=inp_np["down"], x_bf16=x, ids=r["ids"], w=r["w"],
                           sh_I=cfg.I_shared, sh_gate=inp_np.get("sh_gate"), sh_up=inp_np.get("sh_up"),
@@ -275,12 +286,14 @@ def run_reference(args, cfg):
     oracle.build()
     _, inp_np = host_inputs(cfg, seed=0)
     tokens_all = np.arange(cfg.T)
-    # size each step's sample so that warmup + steps fit in about two minutes
+    # size each step's sample so that warmup + steps fit in about two minutes: the oracle
+    # threads over tokens, so a step of n * threads tokens takes about n one-token times
     t0 = time.perf_counter()
     oracle_step(cfg, inp_np, tokens_all[:1])
     t_tok = time.perf_counter() - t0
     per_step_budget = 120.0 / max(1, args.steps + args.warmup)
-    n_tok = int(max(1, min(cfg.T, per_step_budget // max(t_tok, 1e-6))))
+    per_thread = int(per_step_budget // max(t_tok, 1e-6))
+    n_tok = int(max(1, min(cfg.T, max(1, per_thread) * (oracle.hardware_threads() if per_thread else 1))))
     sample = tokens_all[:n_tok]
     for _ in range(args.warmup):
         oracle_step(cfg, inp_np, sample)
@@ -303,26 +316,45 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+
+
 # ------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------
-def run_ours(args, cfg):
-    from block_quantized_moe_router_gb300 import build, capi
+def launches_per_step(cfg):
+    """Kernels one step launches.  A few tokens: one persistent kernel.  Otherwise router
+    GEMM + top-K (or the hash lookup), then the FFN: tcgen05 path -- histogram, scan, scatter,
+    token quantizer, row gather, gate+up GEMM, down GEMM, combine; mma path -- prep, gate+up,
+    down, combine."""
+    if is_decode(cfg):
+        return 1
+    route = 1 if cfg.scoring == synth.SCORE_HASH else 2
+    return route + (8 if cfg.act == synth.ACT_NVFP4 else 4)
+
+
+def zipf_record(cfg, ids):
+    """The realized per-expert pair counts of a Zipf workload against its water-filled
+    targets (by Zipf rank)."""
+    counts = np.bincount(ids[ids >= 0].ravel(), minlength=cfg.E)
+    by_rank = np.empty(cfg.E, dtype=np.int64)
+    by_rank[synth.zipf_rank_of_expert(cfg, 0)] = counts
+    tgt = synth.zipf_targets(cfg.T, cfg.k, cfg.E, cfg.zipf_s)
+    srt = np.sort(counts)[::-1]
+    return {"targets_top5": [round(float(v), 1) for v in tgt[:5]],
+            "realized_top5_by_rank": by_rank[:5].tolist(),
+            "sorted_counts_top10": srt[:10].tolist(), "median": float(np.median(counts)),
+            "min": int(srt[-1]), "experts_touched": int((counts > 0).sum()),
+            "total_variation_vs_targets": round(float(np.abs(by_rank - tgt).sum() / (2.0 * cfg.T * cfg.k)), 4)}
+
+
+def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True):
+    """One workload: build its replicas, capture the step graphs, warm up, run the timed
+    regions, then the end-to-end leg.  Returns the line's fields (rank 0) or None."""
+    from block_quantized_moe_router_gb300 import capi
     from block_quantized_moe_router_gb300.layer import MoeLayer
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    build.build()
-    capi.load_library()
     props = torch.cuda.get_device_properties(local)
     l2 = getattr(props, "L2_cache_size", 0) or 128 * 2 ** 20
-
     inp = synth.make_inputs(cfg, seed=rank, device="cuda")
     base = MoeLayer.from_inputs(inp)
     x = inp["x"].cuda()
@@ -330,7 +362,9 @@ def run_ours(args, cfg):
     T = cfg.T
     ids0, _, _ = base.route(x, token_ids=tok)
     torch.cuda.synchronize()
-    touched = int(torch.unique(ids0[ids0 >= 0]).numel())
+    ids0_h = ids0.cpu().numpy()
+    real = ids0_h[(ids0_h >= 0) & (ids0_h < cfg.E)]
+    touched = int(np.unique(real).size)
     nbytes = step_bytes(cfg, touched)
     replicas = max(1, math.ceil(4 * l2 / nbytes["total"]))
     if args.replicas:
@@ -349,19 +383,20 @@ def run_ours(args, cfg):
                          w=torch.empty((T, cfg.k), dtype=torch.float32, device="cuda"),
                          logits=torch.empty((T, cfg.E), dtype=torch.float32, device="cuda"),
                          out=torch.empty((T, cfg.H), dtype=torch.bfloat16, device="cuda")))
-    # time the dominant kernel live in one replica only: its event nodes break the programmatic
-    # launch chain of that replica's steps, the other replicas run undisturbed
-    capi.moe_profile_enable(layers[0].handle, 1 << capi.PHASE_GATE_UP)
+    dec = is_decode(cfg)
+    if not dec:
+        # the gate+up GEMM timed by events around it in every replica's step; read back after
+        # each timed region (the last execution of every replica, all inside that region)
+        for layer in layers:
+            capi.moe_profile_enable(layer.handle, 1 << capi.PHASE_GATE_UP)
 
     stream = torch.cuda.Stream()
     graphs = []
+
     def step(layer, b):  # one layer step through the public API: route + FFN in one call
         layer.forward(x, token_ids=tok, out=b["out"], topk_ids=b["ids"], topk_w=b["w"],
-                      logits_out=None if tok is not None else b["logits"])
+                      logits_out=None if cfg.scoring == synth.SCORE_HASH else b["logits"])
 
-    # One graph holds one step of every weight replica in turn (as a serving engine captures
-    # all layers of a decode step in one graph); single-replica graphs make up the remainder
-    # so that exactly `steps` layer steps run in the timed region.
     with torch.cuda.stream(stream):
         for layer, b in zip(layers, bufs):   # one eager pass per replica before capture
             step(layer, b)
@@ -400,56 +435,73 @@ def run_ours(args, cfg):
         w0.record(stream)
         run_steps(0, args.warmup)
         w1.record(stream)
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        if args.steps is None:  # about one second of timed work, the same on every rank
+        step_s = w0.elapsed_time(w1) * 1e-3 / args.warmup
+        if steps is None:  # about one second of timed work, the same on every rank
             try:
-                steps = auto_steps(w0.elapsed_time(w1) * 1e-3 / args.warmup, replicas)
+                steps = auto_steps(step_s, replicas)
             except Exception:  # no usable warm-up timing: the fixed default
                 steps = 2000
-            args.steps = int(max_over_ranks([steps], dist, device="cuda")[0])
+            steps = int(max_over_ranks([steps], dist, device="cuda")[0])
+        # regions of exactly `steps` steps, repeated until about args.min_timed_s of timed work
+        est = max(step_s * steps, 1e-6)
+        regions = int(min(args.max_regions, max(1, math.ceil(args.min_timed_s / est))))
+        regions = int(max_over_ranks([regions], dist, device="cuda")[0])
+        region_ms, dom_ms = [], []
+        first = args.warmup
         barrier()
         torch.cuda.synchronize()
         clocks.mark()
-        ev0.record(stream)
-        run_steps(args.warmup, args.steps)
-        ev1.record(stream)
+        for _ in range(regions):
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            barrier()
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            run_steps(first, steps)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            first += steps
+            region_ms.append(ev0.elapsed_time(ev1) / steps)
+            if not dec:
+                per = [float(capi.moe_profile_read(layer.handle)[capi.PHASE_GATE_UP]) for layer in layers]
+                dom_ms.append(sum(per) / len(per))
     torch.cuda.synchronize()
     clocks.mark()
-    barrier()
-    torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    # dominant kernel: the last execution of replica 0's gate+up GEMM (inside the timed region
-    # when steps >= replicas)
-    dom_ms = float(capi.moe_profile_read(layers[0].handle)[capi.PHASE_GATE_UP])
-    ms, dom_ms = max_over_ranks([ms, dom_ms], dist, device="cuda")
+    ms = statistics.median(region_ms)
+    # a few tokens: the step is one launch, so the kernel's time per launch is the step time
+    # (inter-launch gaps included); otherwise the gate+up GEMM's event time
+    launch_ms = ms if dec else statistics.median(dom_ms)
+    ms, launch_ms = max_over_ranks([ms, launch_ms], dist, device="cuda")
+    assert launch_ms <= ms * 1.0001 or not dec
     ok = all(torch.equal(bufs[0]["out"], b["out"]) for b in bufs[1:])
+    if not dec:
+        for layer in layers:
+            capi.moe_profile_enable(layer.handle, 0)
 
-    # end to end through the public API with host buffers: H2D of x, route + FFN, D2H of out
-    e2e_s = float("nan")
+    # end to end through the public API with host buffers: H2D of x (and the token ids),
+    # route + FFN, D2H of the output, the host waiting for every step's result
+    e2e_s, e2e_mode = float("nan"), None
     x_host = inp["x"].pin_memory()
     out_host = torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory()
     tok_host = inp["token_ids"].pin_memory() if tok is not None else None
     x_dev = torch.empty_like(x)
     tok_dev = torch.empty_like(tok) if tok is not None else None
-    e2e_steps = max(3, min(args.steps, 200)) if args.e2e else 0
-    e2e_mode = None
 
-    def e2e_step(layer, b):  # H2D of the step's inputs, route + FFN, D2H of its output
+    def e2e_step(layer, b):
         x_dev.copy_(x_host, non_blocking=True)
         if tok_dev is not None:
             tok_dev.copy_(tok_host, non_blocking=True)
         layer.forward(x_dev, token_ids=tok_dev, out=b["out"], topk_ids=b["ids"], topk_w=b["w"],
-                      logits_out=None if tok is not None else b["logits"])
+                      logits_out=None if cfg.scoring == synth.SCORE_HASH else b["logits"])
         out_host.copy_(b["out"], non_blocking=True)
 
-    if args.e2e:
-        # as a serving loop runs it: each step (copies included) captured once as a CUDA graph
-        # from the public-API calls and replayed, the host waiting for every step's result
+    if want_e2e:
+        e2e_steps = max(3, min(steps, 200, int(math.ceil(0.5 / max(step_s, 1e-6)))))
         e2e_graphs = []
-        try:
+        try:  # as a serving loop runs it: each step, copies included, one captured graph
             with torch.cuda.stream(stream):
                 for layer, b in zip(layers, bufs):
                     e2e_step(layer, b)
@@ -480,97 +532,132 @@ def run_ours(args, cfg):
     h2d = T * cfg.H * 2 + (T * 4 if tok is not None else 0)
     d2h = T * cfg.H * 2
 
+    result = None
     if rank == 0:
-        peak, bf16_peak, peak_kind = measured_peaks()
-        dec = is_decode(cfg)
-        # dominant kernel: the whole-layer persistent kernel for a few tokens, else gate+up
+        pk = measured_peaks()
+        hbm = pk["hbm_gbs"]
+        fp4_peak = pk["bf16_tflops_sustained"] * FP4_OVER_BF16
         dom_bytes = nbytes["total"] if dec else nbytes["gate_up"]
         dom_flops = nbytes["flops"] if dec else nbytes["gate_up_flops"]
-        dom_name = ("dec_fused_kernel (route + FFN)" if dec else "gate+up GEMM (" +
-                    ("tc_gemm_kernel" if cfg.act == synth.ACT_NVFP4 else "expert_mma_kernel") + ")")
-        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-        fp4_peak = bf16_peak * FP4_OVER_BF16
-        tflops = dom_flops / (dom_ms * 1e-3) / 1e12
-        layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
-        src = kernel_source_hash(KERNEL_SOURCES["decode" if dec else
-                                                "tc" if cfg.act == synth.ACT_NVFP4 else "mma"])
+        a4 = cfg.act == synth.ACT_NVFP4
+        dom_name = ("dec_fused_kernel (route + FFN, one launch per step)" if dec else
+                    "gate+up GEMM (" + ("tc_gemm_kernel" if a4 else "expert_mma_kernel") + ")")
+        gbs = dom_bytes / (launch_ms * 1e-3) / 1e9
+        tflops = dom_flops / (launch_ms * 1e-3) / 1e12
+        mma_peak = fp4_peak if a4 else pk["bf16_tflops_sustained"]
+        # the bound: whichever roof is lower for this launch's bytes and FLOPs
+        tensor_bound = a4 and dom_flops / (mma_peak * 1e12) > dom_bytes / (hbm * 1e9)
+        src = kernel_source_hash(KERNEL_SOURCES["decode" if dec else "tc" if a4 else "mma"])
         tr = TRAFFIC.get(cfg.name)
         traffic = tr[0] if tr and tr[1] == src else None
-        line = {
-            "metric": METRIC, "value": job_tokens_per_s(T, world, ms * 1e-3), "unit": "tokens/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "nvfp4 weights, f16 mma / f32 accumulate" if cfg.act == synth.ACT_BF16
-            else "nvfp4 weights and activations, f32 accumulate",
-            "data": "synthetic",
+        if tensor_bound:
+            roof = {"bound": "tensor", "achieved": tflops, "peak": mma_peak, "unit": "TFLOP/s",
+                    "frac": tflops / mma_peak, "traffic": traffic,
+                    "peak_source": f"{pk['source']} sustained bf16 x nominal fp4/bf16 ratio"}
+        else:
+            roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                    "frac": gbs / hbm, "traffic": traffic, "peak_source": pk["source"] + " copy"}
+        roof.update({"kernel": dom_name, "bytes_per_launch": dom_bytes,
+                     "flops_per_launch": dom_flops, "launch_ms": launch_ms,
+                     "launch_timing": "step time (one launch per step)" if dec else
+                     "CUDA events around the launch in every replica, median of regions"})
+        layer_gbs = nbytes["total"] / (ms * 1e-3) / 1e9
+        result = {
+            "value": job_tokens_per_s(T, world, ms * 1e-3), "ms_per_step": ms,
+            "steps": steps, "regions": regions,
             "config": {"workload": cfg.name, "T": T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
                        "top_k": cfg.k, "I_shared": cfg.I_shared, "replicas": replicas,
                        "l2_policy": f"inputs larger than L2: {replicas} weight replicas cycled, "
                                     f"{replicas * nbytes['total'] / 1e6:.0f} MB touched per cycle",
                        "launch": f"CUDA graph of {replicas} layer steps (one per replica), replayed",
+                       "timed_regions": f"{regions} regions of {steps} steps, median reported",
                        "touched_experts": touched},
-            "gpu_launches": args.steps * launches_per_step(cfg),
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic, "kernel": dom_name,
-                         "bytes_per_launch": dom_bytes, "launch_ms": dom_ms,
-                         "peak_source": peak_kind},
-            "tensor_view": {"achieved_tflops": tflops,
-                            "peak_tflops": fp4_peak if cfg.act == synth.ACT_NVFP4 else bf16_peak,
-                            "frac": tflops / (fp4_peak if cfg.act == synth.ACT_NVFP4 else bf16_peak),
-                            "dtype": "nvfp4 x nvfp4" if cfg.act == synth.ACT_NVFP4 else "f16 mma",
-                            "flops_per_launch": dom_flops,
-                            "peak_source": peak_kind + " bf16 x nominal fp4/bf16 ratio"
-                            if cfg.act == synth.ACT_NVFP4 else peak_kind},
-            "layer_roofline": {"achieved": layer_gbs, "peak": peak, "unit": "GB/s",
-                               "frac": layer_gbs / peak, "bytes_per_step": nbytes["total"]},
+            "gpu_launches": steps * launches_per_step(cfg),
+            "roofline": roof,
+            "tensor_view": {"achieved_tflops": tflops, "peak_tflops": mma_peak,
+                            "frac": tflops / mma_peak,
+                            "dtype": "nvfp4 x nvfp4" if a4 else "f16 mma",
+                            "peak_source": f"{pk['source']} sustained bf16" +
+                                           (" x nominal fp4/bf16 ratio" if a4 else "")},
+            "layer_roofline": {"achieved": layer_gbs, "peak": hbm, "unit": "GB/s",
+                               "frac": layer_gbs / hbm, "bytes_per_step": nbytes["total"],
+                               "flops_per_step": nbytes["flops"]},
             "clocks": clk,
-            "e2e": {"value": job_tokens_per_s(T, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "mode": e2e_mode, "ms_per_step": e2e_s * 1e3},
+            "e2e": {"value": job_tokens_per_s(T, world, e2e_s), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "mode": e2e_mode,
+                    "ms_per_step": e2e_s * 1e3},
             "replica_outputs_equal": ok,
             "kernel_source": src,
         }
-        if args.cpu_baseline:
-            _, inp_np = host_inputs_from(inp)
-            line["cpu_baseline"] = cpu_baseline(cfg, inp_np, budget_s=args.cpu_budget)
-        print(json.dumps(line), flush=True)
+        if cfg.zipf_s > 0:
+            result["config"]["zipf_counts"] = zipf_record(cfg, ids0_h)
     for layer in layers:
         layer.close()
+    del layers, bufs, graphs, cycle, inp, base, x
+    torch.cuda.empty_cache()
+    return result
+
+
+def run_ours(args, cfg):
+    from block_quantized_moe_router_gb300 import build, capi
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    capi.load_library()
+
+    head = measure(cfg, args, args.steps, dist, world, rank, local, want_e2e=args.e2e)
+    others = {}
+    if args.per_workload:
+        for name in PER_WORKLOAD:
+            if name == cfg.name:
+                continue
+            res = measure(synth.CONFIGS[name], args, args.steps, dist, world, rank, local,
+                          want_e2e=args.e2e)
+            if res is not None:
+                others[name] = res
+    if rank == 0:
+        line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": head["steps"], "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "nvfp4 weights and activations, f32 accumulate"
+                if cfg.act == synth.ACT_NVFP4 else "nvfp4 weights, f16 mma / f32 accumulate",
+                "data": "synthetic (seeded; shapes and distributions of the named workload)"}
+        for key in ("config", "gpu_launches", "roofline", "tensor_view", "layer_roofline", "clocks",
+                    "e2e", "replica_outputs_equal", "kernel_source", "regions"):
+            line[key] = head[key]
+        line["gpu_launches_scope"] = "one timed region of `steps` steps"
+        if others:
+            line["per_workload"] = others
+        if args.cpu_baseline:
+            _, inp_np = host_inputs(cfg, seed=rank)
+            line["cpu_baseline"] = cpu_baseline(cfg, inp_np, budget_s=args.cpu_budget)
+        print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
-
-
-def host_inputs_from(inp):
-    d = {"x": synth.bf16_bits(inp["x"])}
-    if "w_router" in inp:
-        d["w_router"] = synth.bf16_bits(inp["w_router"])
-    for key in ("bias", "tid2eid", "token_ids"):
-        if key in inp:
-            d[key] = inp[key].cpu().numpy()
-    for key in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
-        if key in inp:
-            d[key] = synth.to_numpy_proj(inp[key])
-    return inp, d
-
-
-def launches_per_step(cfg):
-    """Kernels one step launches.  A few tokens: one persistent kernel.  Otherwise router
-    GEMM + top-K (or the hash lookup), then the FFN: tcgen05 path -- histogram, scan, scatter,
-    token quantizer, row gather, gate+up GEMM, down GEMM, combine; mma path -- prep, gate+up,
-    down, combine."""
-    if is_decode(cfg):
-        return 1
-    route = 1 if cfg.scoring == synth.SCORE_HASH else 2
-    return route + (8 if cfg.act == synth.ACT_NVFP4 else 4)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: about one second of device time, at least 2000)")
+                    help="steps per timed region (default: about one second of device time)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(synth.CONFIGS))
+    ap.add_argument("--per-workload", dest="per_workload", action="store_true", default=None,
+                    help="also measure dec1, dec8, hash64 and pre32768 (default: with the "
+                         "default workload only)")
+    ap.add_argument("--no-per-workload", dest="per_workload", action="store_false")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="repeat the timed region until about this much timed work")
+    ap.add_argument("--max-regions", type=int, default=5000)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--replicas", type=int, default=0,
@@ -578,6 +665,8 @@ def main():
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.per_workload is None:
+        args.per_workload = args.config == DEFAULT_CONFIG
     cfg = synth.CONFIGS[args.config]
     if args.impl == "reference":
         if args.steps is None:

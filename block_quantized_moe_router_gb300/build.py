@@ -3,10 +3,17 @@
 Each translation unit is compiled in parallel with
 ``-gencode arch=compute_103a,code=sm_103a -O3 -lineinfo`` and linked with the static CUDA
 runtime, so the shared object loads without a GPU (the driver is resolved on first use).
+
+A stamp file beside the library holds a hash of every source, the header, this script, the
+compiler flags, the nvcc version and the machine; the library is rebuilt whenever the stamp
+does not match (a copied-in library built elsewhere is never reused), and each call says on
+stderr whether it compiled or reused the library.
 """
 from __future__ import annotations
 
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -27,19 +34,42 @@ def nvcc() -> str:
     return cand
 
 
-def _stamp_inputs():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "moe.h"))
-    files.append(os.path.abspath(__file__))
-    return max(os.path.getmtime(f) for f in files)
+STAMP = LIB + ".stamp"
+FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I",
+                CSRC, "--expt-relaxed-constexpr"]
+
+
+def _nvcc_version() -> str:
+    try:
+        return subprocess.run([nvcc(), "--version"], capture_output=True, text=True).stdout
+    except OSError:
+        return "no nvcc"
+
+
+def source_stamp() -> str:
+    """Hash of everything the library is built from, and of where it is built."""
+    h = hashlib.sha256()
+    files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
+    files += [os.path.join(INCLUDE, "moe.h"), os.path.abspath(__file__)]
+    for f in files:
+        h.update(f.encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(FLAGS).encode())
+    h.update(_nvcc_version().encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _stamp_inputs():
-        return LIB
-    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-                    "-I", CSRC, "--expt-relaxed-constexpr"]
+    stamp = source_stamp()
+    if not force and os.path.exists(LIB) and os.path.exists(STAMP):
+        with open(STAMP) as fh:
+            if fh.read().strip() == stamp:
+                sys.stderr.write(f"libmoe_gb300: reused {LIB} (stamp {stamp[:16]})\n")
+                return LIB
+    flags = list(FLAGS)
     if verbose:
         flags += ["-Xptxas", "-v"]
 
@@ -61,6 +91,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as fh:
+        fh.write(stamp + "\n")
+    sys.stderr.write(f"libmoe_gb300: compiled {LIB} (stamp {stamp[:16]})\n")
     return LIB
 
 

@@ -19,14 +19,15 @@ LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = range(5)
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_TOKEN_ID, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT = 1, 2, 4, 8
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID, MOE_SCORE_HASH, MOE_SCORE_SQRTSOFTPLUS = 0, 1, 2, 3
-MOE_SCORE_SOFTMAX_BIAS = 4
+MOE_SCORE_SOFTMAX_BIAS, MOE_SCORE_HASH_SQRTSOFTPLUS = 4, 5
 MOE_FMT_NVFP4, MOE_FMT_MXFP4 = 0, 1
 MOE_ACT_BF16, MOE_ACT_NVFP4 = 0, 1
 
 # Every symbol include/moe.h declares.
 EXPORTED = ["moe_route", "moe_workspace_size", "moe_prepare_weights", "moe_release_weights",
             "moe_ffn_forward", "moe_forward", "moe_ffn_forward_noalloc", "moe_quantize_act_nvfp4",
-            "moe_profile_enable", "moe_profile_read", "moe_status_string"]
+            "moe_set_wait_limit", "moe_skew_barrier", "moe_profile_enable", "moe_profile_read",
+            "moe_status_string"]
 
 
 class MoeError(RuntimeError):
@@ -88,6 +89,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_ffn_forward_noalloc.restype = ctypes.c_int
     lib.moe_quantize_act_nvfp4.argtypes = [vp, i64, i64, f32, vp, vp, vp]
     lib.moe_quantize_act_nvfp4.restype = ctypes.c_int
+    lib.moe_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+    lib.moe_set_wait_limit.restype = ctypes.c_int
+    lib.moe_skew_barrier.argtypes = [vp, vp]
+    lib.moe_skew_barrier.restype = ctypes.c_int
     lib.moe_profile_enable.argtypes = [vp, ctypes.c_uint32]
     lib.moe_profile_enable.restype = ctypes.c_int
     lib.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float)]
@@ -223,6 +228,16 @@ def moe_quantize_act_nvfp4(x, g: float, packed, scales, stream=None):
         _dptr(x, torch.bfloat16, "x"), int(rows), int(K), float(g),
         _dptr(packed, torch.uint8, "packed"), _dptr(scales, torch.uint8, "scales"), _stream(stream))
     _check(st, "moe_quantize_act_nvfp4")
+
+
+def moe_set_wait_limit(handle: int, cycles: int):
+    _check(load_library().moe_set_wait_limit(ctypes.c_void_p(handle), int(cycles)),
+           "moe_set_wait_limit")
+
+
+def moe_skew_barrier(handle: int, stream=None):
+    _check(load_library().moe_skew_barrier(ctypes.c_void_p(handle), _stream(stream)),
+           "moe_skew_barrier")
 
 
 PHASE_DISPATCH, PHASE_GATE_UP, PHASE_DOWN, PHASE_COMBINE = 0, 1, 2, 3

@@ -19,6 +19,8 @@ bool pow2_positive(float g) {
     return std::frexp(g, &ex) == 0.5f;
 }
 
+bool is_hash(int scoring) { return scoring == MOE_SCORE_HASH || scoring == MOE_SCORE_HASH_SQRTSOFTPLUS; }
+
 bool valid_fmt(int f) { return f == MOE_FMT_NVFP4 || f == MOE_FMT_MXFP4; }
 
 bool valid_qtensor(const moe_qtensor& t) {
@@ -43,6 +45,7 @@ struct Handle {
     TcWeights tc{};        // owned; the tcgen05 path's scale tiles and tensor maps
     int sms = 0;           // SM count of the device the weights live on
     unsigned long long* bar = nullptr;  // owned; grid-barrier tickets of the few-token kernel
+    unsigned long long wait_cycles = 0;  // device-wide barrier wait limit (0 = the default)
 };
 
 bool desc_tc_shape(const moe_ffn_desc& d) {
@@ -114,9 +117,9 @@ moe_status_t validate_route(const moe_route_desc* d, const float* logits_in) {
     if (!std::isfinite(d->routed_scaling)) return MOE_ERR_INVALID_ARG;
     if (d->scoring != MOE_SCORE_SOFTMAX && d->scoring != MOE_SCORE_SIGMOID &&
         d->scoring != MOE_SCORE_HASH && d->scoring != MOE_SCORE_SQRTSOFTPLUS &&
-        d->scoring != MOE_SCORE_SOFTMAX_BIAS)
+        d->scoring != MOE_SCORE_SOFTMAX_BIAS && d->scoring != MOE_SCORE_HASH_SQRTSOFTPLUS)
         return MOE_ERR_INVALID_ARG;
-    if (d->scoring == MOE_SCORE_HASH && d->vocab < 1) return MOE_ERR_INVALID_ARG;
+    if (is_hash(d->scoring) && d->vocab < 1) return MOE_ERR_INVALID_ARG;
     if (d->scoring != MOE_SCORE_HASH && !logits_in && (d->H < 32 || d->H % 32))
         return MOE_ERR_INVALID_ARG;
     return MOE_OK;
@@ -131,6 +134,7 @@ FfnLaunch make_launch(const Handle* h, int T, int act, float g1, float g2, int p
     L.T = T; L.E = d.E; L.H = d.H; L.I = d.I; L.k = d.top_k; L.I_shared = d.I_shared;
     L.Z = d.zero_experts;
     L.act = act; L.path = path; L.g1 = g1; L.g2 = g2;
+    L.wait_cycles = h->wait_cycles;
     L.x = x; L.ids = ids; L.w = w; L.out = out; L.status = status;
     L.gate = h->gate.view; L.up = h->up.view; L.down = h->down.view;
     L.sh_gate = h->sh_gate.view; L.sh_up = h->sh_up.view; L.sh_down = h->sh_down.view;
@@ -186,9 +190,12 @@ moe_status_t moe_route(const moe_route_desc* d, const void* x_bf16, const float*
     if (d->scoring == MOE_SCORE_HASH) {
         if (!d->tid2eid || !d->token_ids) return MOE_ERR_INVALID_ARG;
         return launch_hash_route(d->tid2eid, d->token_ids, d->vocab, d->T, Er, d->top_k,
-                                 d->routed_scaling, topk_ids, topk_w, dev_status, st) == cudaSuccess
+                                 d->routed_scaling, nullptr, 0, topk_ids, topk_w, dev_status,
+                                 st) == cudaSuccess
                    ? MOE_OK : MOE_ERR_CUDA;
     }
+    if (d->scoring == MOE_SCORE_HASH_SQRTSOFTPLUS && (!d->tid2eid || !d->token_ids))
+        return MOE_ERR_INVALID_ARG;
     const float* logits = logits_in;
     if (!logits) {
         if (!d->w_router || !x_bf16 || !logits_out) return MOE_ERR_INVALID_ARG;
@@ -199,6 +206,11 @@ moe_status_t moe_route(const moe_route_desc* d, const void* x_bf16, const float*
         if (err != cudaSuccess) return MOE_ERR_CUDA;
         logits = logits_out;
     }
+    if (d->scoring == MOE_SCORE_HASH_SQRTSOFTPLUS)  // table ids, router-score weights
+        return launch_hash_route(d->tid2eid, d->token_ids, d->vocab, d->T, Er, d->top_k,
+                                 d->routed_scaling, logits, d->renormalize ? 1 : 0, topk_ids,
+                                 topk_w, dev_status, st) == cudaSuccess
+                   ? MOE_OK : MOE_ERR_CUDA;
     const float* bias = d->scoring != MOE_SCORE_SOFTMAX ? d->correction_bias : nullptr;
     return launch_topk(logits, bias, d->T, Er, d->top_k, d->scoring, d->renormalize ? 1 : 0,
                        d->routed_scaling, topk_ids, topk_w, dev_status, st) == cudaSuccess
@@ -338,8 +350,8 @@ moe_status_t moe_forward(const void* handle, const moe_route_desc* rd, int32_t a
     const int T = rd->T;
     if (T == 0) return MOE_OK;
     if (!x_bf16 || !topk_ids || !topk_w || !out_bf16 || !workspace) return MOE_ERR_INVALID_ARG;
-    const bool hash = rd->scoring == MOE_SCORE_HASH;
-    if (hash && (!rd->tid2eid || !rd->token_ids)) return MOE_ERR_INVALID_ARG;
+    const bool hash = rd->scoring == MOE_SCORE_HASH;  // no router at all
+    if (is_hash(rd->scoring) && (!rd->tid2eid || !rd->token_ids)) return MOE_ERR_INVALID_ARG;
     if (!hash && !logits_in && (!rd->w_router || !logits_out)) return MOE_ERR_INVALID_ARG;
     const int path = select_path(T, d.H, d.top_k, act, h->tc_shape);
     if (path != PATH_DECODE) {
@@ -356,10 +368,11 @@ moe_status_t moe_forward(const void* handle, const moe_route_desc* rd, int32_t a
                                     out_bf16, dev_status);
     DecRoute R{};
     R.mode = hash ? DEC_ROUTE_HASH : (logits_in ? DEC_ROUTE_LOGITS : DEC_ROUTE_ROUTER);
+    R.hash_ids = is_hash(rd->scoring) ? 1 : 0;  // ids from the table (weights as R.scoring says)
     R.w_router = rd->w_router;
     R.logits_in = logits_in;
     R.logits_out = logits_out;
-    R.bias = rd->scoring != MOE_SCORE_SOFTMAX ? rd->correction_bias : nullptr;
+    R.bias = (rd->scoring != MOE_SCORE_SOFTMAX && !is_hash(rd->scoring)) ? rd->correction_bias : nullptr;
     R.scoring = rd->scoring;
     R.renorm = rd->renormalize ? 1 : 0;
     R.scaling = rd->routed_scaling;
@@ -369,6 +382,20 @@ moe_status_t moe_forward(const void* handle, const moe_route_desc* rd, int32_t a
     R.ids_out = topk_ids;
     R.w_out = topk_w;
     return run_decode(h, L, R, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_set_wait_limit(void* handle, uint64_t cycles) {
+    Handle* h = static_cast<Handle*>(handle);
+    if (!h || h->magic != 0x4D4F4531u) return MOE_ERR_INVALID_ARG;
+    h->wait_cycles = cycles;
+    return MOE_OK;
+}
+
+moe_status_t moe_skew_barrier(void* handle, void* stream) {
+    Handle* h = static_cast<Handle*>(handle);
+    if (!h || h->magic != 0x4D4F4531u) return MOE_ERR_INVALID_ARG;
+    return launch_barrier_skew(h->bar, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status_t moe_profile_enable(void* handle, uint32_t mask) {

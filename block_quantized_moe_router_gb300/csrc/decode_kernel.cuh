@@ -75,7 +75,7 @@ constexpr int kDecRedDTile = kDecWarps * 128 * 4;
 constexpr int kDecMaxTilesPerCta = 4;
 // router phase: experts handled together per CTA, 8-element chunks per thread and expert
 constexpr int kDecRouterBatch = 4, kDecRouterChunks = 4;  // H <= 8 * 256 * 4 = 8192
-constexpr long long kBarrierCycles = 4000000000ll;  // ~2 s at 2 GHz
+constexpr long long kBarrierCycles = 4000000000ll;  // default wait limit: ~2 s at 2 GHz
 
 // Dispatch of T <= 8 tokens, derived by every CTA from the routing ids / weights.
 struct DecDispatch {
@@ -126,8 +126,10 @@ __device__ __forceinline__ int nth_bit(uint32_t mask, int g) {
 }
 
 // Grid-wide barrier of a cooperative launch: 64-bit arrival tickets, never reset; barrier
-// instance n completes when the counter reaches (n + 1) * G.  The wait is bounded.
-__device__ __forceinline__ void grid_barrier(unsigned long long* bar, int32_t* status) {
+// instance n completes when the counter reaches (n + 1) * G.  The wait is bounded: after
+// `limit` SM cycles it sets MOE_DEV_TIMEOUT and returns.
+__device__ __forceinline__ void grid_barrier(unsigned long long* bar, int32_t* status,
+                                             long long limit) {
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -140,7 +142,7 @@ __device__ __forceinline__ void grid_barrier(unsigned long long* bar, int32_t* s
         while (!done) {
             if (++spins > 64) __nanosleep(64);
             done = ld_acquire_u64(bar) >= target;
-            if (!done && clock64() - t0 > kBarrierCycles) break;
+            if (!done && clock64() - t0 > limit) break;
         }
         if (!done) status_or(status, MOE_DEV_TIMEOUT);
         __threadfence();
@@ -409,11 +411,61 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         }
     }
     cp_async_wait<0>();           // the post-scale tables are in
-    grid_barrier(bar, L.status);  // x16 and the logits are written
+    const long long wait_limit = L.wait_cycles ? (long long)L.wait_cycles : kBarrierCycles;
+    grid_barrier(bar, L.status, wait_limit);  // x16 and the logits are written
 
     // ---- phase 1: routing and dispatch ---------------------------------------------------------
     const int P = T * k;
-    if (R.mode == DEC_ROUTE_ROUTER || R.mode == DEC_ROUTE_LOGITS) {
+    if (R.hash_ids) {
+        // ids from the table; weights scaling / k, or from the sqrt(softplus) router scores of
+        // the table's experts (logits from phase 0 or given), renormalised per token
+        float wv = 0.f;
+        if (tid < P) {
+            const int t = tid / k, j = tid - t * k;
+            const int64_t tok = R.token_ids[t];
+            int32_t e = -1;
+            if (tok < 0 || tok >= R.vocab) {
+                if (cta == 0) status_or(L.status, MOE_DEV_BAD_TOKEN_ID);
+            } else {
+                const int64_t te = R.tid2eid[tok * k + j];
+                if (te < 0 || te >= Er) {
+                    if (cta == 0) status_or(L.status, MOE_DEV_BAD_EXPERT_ID);
+                } else {
+                    e = (int32_t)te;
+                    wv = 1.f;
+                    if (R.mode != DEC_ROUTE_HASH) {
+                        const float l = R.mode == DEC_ROUTE_ROUTER
+                                            ? ld_cg_f32(R.logits_out + (size_t)t * Er + e)
+                                            : R.logits_in[(size_t)t * Er + e];
+                        if (isfinite(l)) {
+                            wv = gate_score(MOE_SCORE_SQRTSOFTPLUS, l);
+                        } else {
+                            wv = 0.f;
+                            if (cta == 0) status_or(L.status, MOE_DEV_NONFINITE);
+                        }
+                    }
+                }
+            }
+            S.ids[tid] = e;
+            S.w[tid] = wv;
+        }
+        __syncthreads();
+        if (tid < P) {
+            if (R.mode == DEC_ROUTE_HASH) {
+                wv *= R.scaling / (float)k;
+            } else {
+                float den = 1.f;
+                if (R.renorm) {
+                    const int t0 = (tid / k) * k;
+                    den = 0.f;
+                    for (int j = 0; j < k; ++j) den += S.w[t0 + j];
+                }
+                wv = den > 0.f ? wv / den * R.scaling : 0.f;
+            }
+        }
+        __syncthreads();
+        if (tid < P) S.w[tid] = wv;
+    } else if (R.mode == DEC_ROUTE_ROUTER || R.mode == DEC_ROUTE_LOGITS) {
         if (warp < T) {
             const bool in_launch = R.mode == DEC_ROUTE_ROUTER;
             const float* row = (in_launch ? R.logits_out : R.logits_in) + (size_t)warp * Er;
@@ -435,28 +487,12 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
                 S.w[warp * k + lane] = my_w;
             }
         }
-    } else if (R.mode == DEC_ROUTE_HASH) {
-        if (tid < P) {
-            const int t = tid / k, j = tid - t * k;
-            const int64_t tok = R.token_ids[t];
-            int32_t e = -1;
-            float w = 0.f;
-            if (tok < 0 || tok >= R.vocab) {
-                if (cta == 0) status_or(L.status, MOE_DEV_BAD_TOKEN_ID);
-            } else {
-                const int64_t te = R.tid2eid[tok * k + j];
-                if (te < 0 || te >= Er) {
-                    if (cta == 0) status_or(L.status, MOE_DEV_BAD_EXPERT_ID);
-                } else {
-                    e = (int32_t)te;
-                    w = R.scaling / (float)k;
-                }
-            }
-            S.ids[tid] = e;
-            S.w[tid] = w;
-        }
     } else if (tid < P) {
-        S.ids[tid] = L.ids[tid];
+        // given ids: anything but -1, a real expert or a zero-computation expert is dropped
+        // (the dispatch ignores it) and flagged, as on the many-token paths
+        const int32_t e = L.ids[tid];
+        if (e != -1 && (e < 0 || e >= Er) && cta == 0) status_or(L.status, MOE_DEV_BAD_EXPERT_ID);
+        S.ids[tid] = e;
         S.w[tid] = L.w[tid];
     }
     __syncthreads();
@@ -692,7 +728,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             }
         }
     }
-    grid_barrier(bar, L.status);  // every h is written (and red_g is no longer read)
+    grid_barrier(bar, L.status, wait_limit);  // every h is written (and red_g is no longer read)
 
     // ---- phase 3: down + weighted sum + shared expert ----------------------------------------------
     // the h chunks of the down stages already in the ring, then every later stage copies its own

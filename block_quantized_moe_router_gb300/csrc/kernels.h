@@ -18,9 +18,12 @@ cudaError_t launch_router_tc(const void* x, const void* wr, float* logits, int T
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int scoring,
                         int renorm, float scaling, int32_t* ids, float* w, int32_t* status,
                         cudaStream_t st);
+// ids = tid2eid[token] (table order).  Weights: scaling / k, or -- with router logits given --
+// sqrt(softplus(logit at the id)), renormalised over the token's kept pairs when `renorm`,
+// times scaling.
 cudaError_t launch_hash_route(const int64_t* tid2eid, const int32_t* token_ids, int64_t vocab,
-                              int T, int E, int k, float scaling, int32_t* ids, float* w,
-                              int32_t* status, cudaStream_t st);
+                              int T, int E, int k, float scaling, const float* logits, int renorm,
+                              int32_t* ids, float* w, int32_t* status, cudaStream_t st);
 
 // ---- expert FFN (ffn.cu) --------------------------------------------------------------------
 // One projection as the kernels see it: packed codes, block scales, and a per-expert fp32
@@ -38,6 +41,7 @@ struct FfnLaunch {
     int T, E, H, I, k, I_shared, act, path;
     int Z;                  // zero-computation experts: ids E .. E + Z - 1 add w * x
     float g1, g2;
+    unsigned long long wait_cycles;  // device-wide barrier wait limit in SM cycles (0: default)
     const void* x;          // bf16 [T][H]
     const int32_t* ids;     // [T][k]
     const float* w;         // [T][k]
@@ -148,6 +152,8 @@ enum DecRouteMode {
 };
 struct DecRoute {
     int mode;
+    int hash_ids;             // ids from tid2eid[token_ids] (with mode ROUTER / LOGITS the
+                              // weights come from the sqrt(softplus) scores of the logits)
     const void* w_router;     // bf16 [E][H]
     const float* logits_in;   // [T][E]
     float* logits_out;        // [T][E]
@@ -164,6 +170,9 @@ struct DecRoute {
 // only by launches of `sms` CTAs.
 cudaError_t launch_decode_fused(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
                                 int sms, cudaStream_t st);
+// Adds one to the barrier ticket counter (test aid: the next fused launch's last barrier wait
+// then runs out its limit).
+cudaError_t launch_barrier_skew(unsigned long long* bar, cudaStream_t st);
 
 cudaError_t launch_quantize_act(const void* x, int64_t rows, int64_t K, float g, uint8_t* packed,
                                 uint8_t* scales, __half* deq16, cudaStream_t st);

@@ -5,7 +5,10 @@
 //   sigmoid + correction bias (selection on sigmoid+bias, weights from the unbiased sigmoid,
 //     renormalised and scaled) -- moe/mod.rs, `correction_bias_dev` field doc;
 //   sqrt(softplus) scores in the same scheme -- moe/mod.rs, `moe_topk_sqrtsoftplus` handles;
-//   static hash routing through tid2eid [vocab, top_k] -- moe/init.rs, `new_with_hash` doc.
+//   static hash routing through tid2eid [vocab, top_k] -- moe/init.rs, `new_with_hash` doc;
+//     its weights either equal or, for the family that ships both the hash and the
+//     sqrt(softplus) routing handles (moe/init.rs lookups), the sqrt(softplus) router scores
+//     of the table's experts.
 // The router keeps fp32 logits (moe/mod.rs, `dense_gemm_f32out` field doc: an fp32-output
 // router GEMM feeding an fp32-input top-K).  Ids and weights stay on the device.
 #include "common.cuh"
@@ -221,31 +224,60 @@ topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, in
 }
 
 // ------------------------------------------------------------------------------------------
-// Hash routing: ids = tid2eid[token_ids[t]] (table order), weight = scaling / k.
+// Hash routing: ids = tid2eid[token_ids[t]] (table order).  One warp per token, lane j < k
+// holds pair j.  Weights: scaling / k; or, with router logits (the hash layers of the family
+// that also routes by sqrt(softplus) scores), s_j = sqrt(softplus(logit[t][id_j])),
+// renormalised over the token's kept pairs when asked, times scaling.  A bad table entry or
+// token id drops the pair (id -1, weight 0); a non-finite logit gives weight 0.
 // ------------------------------------------------------------------------------------------
-__global__ void hash_route_kernel(const int64_t* __restrict__ tid2eid,
-                                  const int32_t* __restrict__ token_ids, int64_t vocab, int T,
-                                  int E, int k, float scaling, int32_t* __restrict__ ids,
-                                  float* __restrict__ wout, int32_t* __restrict__ status) {
-    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= T * k) return;
-    const int t = idx / k, j = idx - t * k;
+__global__ void __launch_bounds__(256)
+hash_route_kernel(const int64_t* __restrict__ tid2eid, const int32_t* __restrict__ token_ids,
+                  int64_t vocab, int T, int E, int k, float scaling,
+                  const float* __restrict__ logits, int renorm, int32_t* __restrict__ ids,
+                  float* __restrict__ wout, int32_t* __restrict__ status) {
+    pdl_wait();  // token ids (and the logits) may come from the preceding kernel
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
     const int64_t tok = token_ids[t];
+    const bool tok_ok = tok >= 0 && tok < vocab;
+    if (!tok_ok && lane == 0) status_or(status, MOE_DEV_BAD_TOKEN_ID);
     int32_t e = -1;
     float w = 0.f;
-    if (tok < 0 || tok >= vocab) {
-        status_or(status, MOE_DEV_BAD_TOKEN_ID);
-    } else {
-        const int64_t te = tid2eid[tok * k + j];
+    if (lane < k && tok_ok) {
+        const int64_t te = tid2eid[tok * k + lane];
         if (te < 0 || te >= E) {
             status_or(status, MOE_DEV_BAD_EXPERT_ID);
         } else {
             e = (int32_t)te;
-            w = scaling / (float)k;
+            w = 1.f;
+            if (logits) {
+                const float l = logits[(size_t)t * E + e];
+                if (isfinite(l)) {
+                    w = gate_score(MOE_SCORE_SQRTSOFTPLUS, l);
+                } else {
+                    w = 0.f;
+                    status_or(status, MOE_DEV_NONFINITE);
+                }
+            }
         }
     }
-    ids[idx] = e;
-    wout[idx] = w;
+    if (logits) {
+        float den = 1.f;
+        if (renorm) {
+            den = w;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        }
+        w = den > 0.f ? w / den * scaling : 0.f;
+    } else {
+        w *= scaling / (float)k;
+    }
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = e;
+        wout[(size_t)t * k + lane] = w;
+    }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -297,12 +329,11 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
 }
 
 cudaError_t launch_hash_route(const int64_t* tid2eid, const int32_t* token_ids, int64_t vocab,
-                              int T, int E, int k, float scaling, int32_t* ids, float* w,
-                              int32_t* status, cudaStream_t st) {
-    const int n = T * k;
-    hash_route_kernel<<<(n + 255) / 256, 256, 0, st>>>(tid2eid, token_ids, vocab, T, E, k,
-                                                        scaling, ids, w, status);
-    return cudaGetLastError();
+                              int T, int E, int k, float scaling, const float* logits, int renorm,
+                              int32_t* ids, float* w, int32_t* status, cudaStream_t st) {
+    const int warps = T < 8 ? T : 8;
+    return launch_pdl(hash_route_kernel, dim3((T + warps - 1) / warps), dim3(32 * warps), st,
+                      tid2eid, token_ids, vocab, T, E, k, scaling, logits, renorm, ids, w, status);
 }
 
 }  // namespace moe

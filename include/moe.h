@@ -59,7 +59,8 @@ typedef enum {
     MOE_SCORE_SIGMOID = 1,
     MOE_SCORE_HASH = 2,
     MOE_SCORE_SQRTSOFTPLUS = 3,
-    MOE_SCORE_SOFTMAX_BIAS = 4
+    MOE_SCORE_SOFTMAX_BIAS = 4,
+    MOE_SCORE_HASH_SQRTSOFTPLUS = 5  /* hash ids, weights from sqrt(softplus) router scores */
 } moe_scoring_t;
 typedef enum { MOE_FMT_NVFP4 = 0, MOE_FMT_MXFP4 = 1 } moe_fmt_t;
 /* Activation precision of the expert GEMMs.  BF16: W4A16 (bf16 tokens, dequantized
@@ -93,7 +94,7 @@ typedef struct {
  * E .. E + zero_experts - 1; see moe_ffn_desc).  The router has E + zero_experts outputs:
  * w_router [E + Z][H], correction_bias [E + Z], logits [T][E + Z].  Constraints (checked):
  * 1 <= E, E + Z <= 512, 1 <= top_k <= min(E + Z, 32); learned routers: H a multiple of 32 when
- * the router GEMM runs; hash: tid2eid and token_ids non-NULL, vocab >= 1. */
+ * the router GEMM runs; both hash kinds: tid2eid and token_ids non-NULL, vocab >= 1. */
 typedef struct {
     int32_t T, E, H, top_k;
     int32_t scoring;           /* moe_scoring_t                                            */
@@ -101,9 +102,9 @@ typedef struct {
     float routed_scaling;      /* multiplies every routing weight (1.0 for plain top-K)    */
     const void* w_router;      /* [device] bf16 [E][H], or NULL when logits are supplied   */
     const float* correction_bias; /* [device] float [E] (sigmoid/sqrt-softplus selection) or NULL */
-    const int64_t* tid2eid;    /* [device] int64 [vocab][top_k] (hash only)               */
+    const int64_t* tid2eid;    /* [device] int64 [vocab][top_k] (hash kinds only)         */
     int64_t vocab;
-    const int32_t* token_ids;  /* [device] int32 [T] (hash only)                          */
+    const int32_t* token_ids;  /* [device] int32 [T] (hash kinds only)                    */
     int32_t zero_experts;      /* Z >= 0 zero-computation experts after the E real ones    */
 } moe_route_desc;
 
@@ -120,6 +121,15 @@ typedef struct {
  *     `moe_topk_sqrtsoftplus` routing handles).
  *   Hash: ids = tid2eid[token_ids[t]] in table order; weight = routed_scaling / top_k.
  *     (moe/init.rs, `new_with_hash` doc.)
+ *   Hash + sqrt(softplus) weights: ids as for Hash; the router GEMM still runs (or logits_in
+ *     is read) and pair j gets s_j = sqrt(log(1 + exp(logits[t][id_j]))); weight = s_j /
+ *     sum over the token's kept pairs of s when renormalize, else s_j; times routed_scaling.
+ *     No correction bias (nothing is selected).  This is how this library reads the hash
+ *     layers of the model family that ships both the `moe_hash_route` and the
+ *     `moe_topk_sqrtsoftplus` routing handles (moe/init.rs handle lookups; moe/mod.rs,
+ *     `tid2eid_dev` field doc): the table fixes the experts, the learned router their weights.
+ *     A pair with a bad table entry is dropped (weight 0) and left out of the sum; a
+ *     non-finite logit at a chosen id gives that pair weight 0 and sets MOE_DEV_NONFINITE.
  * Ids are written in descending selection-score order, ties to the lower expert index.
  * x_bf16      [device] bf16 [T][H]; used when w_router != NULL.
  * logits_in   [device] float [T][E] or NULL: precomputed router logits (then w_router and
@@ -133,19 +143,40 @@ moe_status_t moe_route(const moe_route_desc* desc, const void* x_bf16, const flo
                        float* logits_out, int32_t* topk_ids, float* topk_w, int32_t* dev_status,
                        void* stream);
 
-/* Bytes of device workspace moe_ffn_forward needs for T tokens in activation mode act. */
+/* Bytes of device workspace moe_ffn_forward needs for T tokens in activation mode act.
+ * Source: the spark_model MoE pages, moe/mod.rs, `zero_accum_dev` field doc (the layer's
+ * scratch is a fixed-size allocation made once, so that the forward pass stays graph-safe):
+ * here the caller makes that one allocation, sized by this call, and passes it to every
+ * moe_ffn_forward / moe_forward with at most T tokens.  The size depends only on the
+ * descriptor, T and act.  Host-only: launches nothing.  Errors: MOE_ERR_INVALID_ARG for a
+ * NULL `bytes`, an invalid descriptor (the checks of moe_ffn_desc), T < 0 or an unknown act. */
 moe_status_t moe_workspace_size(const moe_ffn_desc* desc, int32_t T, int32_t act, size_t* bytes);
 
-/* One-time weight preparation: validates the descriptor, derives per-tensor post-scales
- * (the NVFP4 globals; for MXFP4 a power-of-two exponent offset) and the scale-factor tiles
- * of the FP4 tensor-core path (3 * (E * I + I_shared) * H / 16 bytes: the weights' scales in
- * the order the tensor-core kernel copies them to TMEM).  The weight buffers must stay alive
- * and unchanged until moe_release_weights.  Allocates device memory and synchronises
- * `stream` before returning. */
+/* One-time weight preparation.  Source: the spark_model MoE pages, moe/mod.rs, the
+ * `cutlass_grouped_host` (`MoeCutlassHostTables`) and `_cutlass_sfb_owned` field docs: the
+ * per-expert scale-factor (SFB) layout the grouped FP4 GEMM consumes is built ONCE at load
+ * from the weights' scales and owned by the layer, dying with it.  Here: validates the
+ * descriptor (the construction-time checks of moe/init.rs, `MoeLayer::new_with_hash`),
+ * derives per-tensor post-scales (the NVFP4 globals; for MXFP4 a power-of-two exponent
+ * offset) and the scale-factor tiles of the FP4 tensor-core path (3 * (E * I + I_shared) *
+ * H / 16 bytes: the weights' scales in the order the tensor-core kernel copies them to TMEM).
+ * desc        [host] read during the call only; the device buffers it points to must stay
+ *             alive and unchanged until moe_release_weights.
+ * handle_out  [host] receives the handle (NULL on error).
+ * Allocates device memory and synchronises `stream` before returning.  Errors:
+ * MOE_ERR_INVALID_ARG (descriptor checks), MOE_ERR_UNSUPPORTED (gate/up/down of mixed formats),
+ * MOE_ERR_CUDA (allocation or launch failure; nothing is leaked). */
 moe_status_t moe_prepare_weights(const moe_ffn_desc* desc, void** handle_out, void* stream);
+/* Frees everything moe_prepare_weights allocated (moe/mod.rs, `_cutlass_sfb_owned` field doc:
+ * the owned scale buffers live exactly as long as the layer).  The caller must make sure no
+ * launch using the handle is still running.
+ * Errors: MOE_ERR_INVALID_ARG for NULL or a pointer that is not a live handle. */
 moe_status_t moe_release_weights(void* handle);
 
-/* Expert FFN + weighted combine:
+/* Expert FFN + weighted combine.  Source: the spark_model MoE pages, moe/mod.rs module doc
+ * (the top-K experts of a batch run in two fused expert launches -- gate+up, then SiLU+down --
+ * with ids and weights kept on the device) and moe/init.rs (`moe_weighted_sum_blend`: the
+ * weighted sum plus the shared expert):
  *   out[t] = sum_j topk_w[t][j] * FFN_{topk_ids[t][j]}(x[t]) + FFN_shared(x[t]),
  *   FFN_e(a) = W_down,e (SiLU(W_gate,e a) * (W_up,e a)) for a real expert e < E,
  *   FFN_e(a) = x[t] for a zero-computation expert E <= e < E + zero_experts;
@@ -209,7 +240,22 @@ moe_status_t moe_ffn_forward_noalloc(const void* handle, int32_t T, int32_t act,
                                      const float* topk_w, void* out_bf16, int32_t* dev_status,
                                      void* stream);
 
-/* Kernel timing for benchmarks.  moe_profile_enable(handle, mask) makes the handle record
+/* Diagnostics for the bounded device waits (no counterpart on the pages, which give no
+ * device-side wait at all; the few-token kernel's device-wide barriers are this library's).
+ * moe_set_wait_limit(handle, cycles): every device-wide barrier wait of the few-token kernel
+ * launched on `handle` afterwards gives up after `cycles` SM clock cycles (0 = the default,
+ * 4e9 cycles, about 2 s) and then sets MOE_DEV_TIMEOUT and carries on.  Host-only.
+ * moe_skew_barrier(handle, stream): adds one to the handle's barrier ticket counter on
+ * `stream`.  In the next few-token launch one thread block then waits for an arrival that
+ * never comes: its wait runs out after the limit, MOE_DEV_TIMEOUT is set, the launch returns
+ * normally and its outputs are invalid.  Used by the tests of the timeout path; after it (or
+ * after any MOE_DEV_TIMEOUT) release the handle and prepare the weights again.
+ * Errors: MOE_ERR_INVALID_ARG for a bad handle, MOE_ERR_CUDA if the launch fails. */
+moe_status_t moe_set_wait_limit(void* handle, uint64_t cycles);
+moe_status_t moe_skew_barrier(void* handle, void* stream);
+
+/* Kernel timing for benchmarks (no counterpart on the pages; a measurement aid).
+ * moe_profile_enable(handle, mask) makes the handle record
  * a pair of CUDA timing events around each kernel phase selected by `mask` in every later
  * moe_ffn_forward on that handle (as external event nodes when the stream is being captured
  * into a CUDA graph); mask 0 stops it.  Phases: bit 0 dispatch + activation conversion,
@@ -219,6 +265,10 @@ moe_status_t moe_ffn_forward_noalloc(const void* handle, int32_t T, int32_t act,
 moe_status_t moe_profile_enable(void* handle, uint32_t mask);
 moe_status_t moe_profile_read(void* handle, float* ms_out);
 
+/* A static, NUL-terminated description of a status code ("unknown moe_status_t" for values
+ * outside the enum); never NULL, nothing to free.  Source: the loud construction-time errors
+ * of the spark_model MoE layer (moe/init.rs, `MoeLayer::new_with_hash`: a top_k above the
+ * expert count is refused at load with a message instead of routing out of bounds). */
 const char* moe_status_string(moe_status_t status);
 
 #ifdef __cplusplus

@@ -84,7 +84,9 @@ def test_route_rejects_before_launch(lib):
     assert call(top_k=9) == capi.MOE_ERR_INVALID_ARG
     assert call(E=0) == capi.MOE_ERR_INVALID_ARG
     assert call(T=-1) == capi.MOE_ERR_INVALID_ARG
-    assert call(scoring=5, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG
+    assert call(scoring=6, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG
+    assert call(scoring=5, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG  # no table, vocab 0
+    assert call(scoring=5, w_router=0x1000, vocab=10) == capi.MOE_ERR_INVALID_ARG  # no table
     assert call(zero_experts=-1, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG
     assert call(E=500, zero_experts=13, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG  # E + Z > 512
     assert call(top_k=9, zero_experts=1, w_router=0x1000) == capi.MOE_ERR_INVALID_ARG  # k > E + Z
@@ -102,3 +104,23 @@ def test_ffn_forward_rejects_bad_handle(lib):
     d = _fake_desc(E=0)
     assert lib.moe_prepare_weights(ctypes.byref(d), ctypes.byref(h), None) == capi.MOE_ERR_INVALID_ARG
     assert lib.moe_quantize_act_nvfp4(fake, 4, 24, 1.0, fake, fake, None) == capi.MOE_ERR_INVALID_ARG
+
+
+def test_every_declaration_cites_its_passage():
+    """Each entry point's comment names the passage of the pages that defines it (a page of
+    the spark_model MoE source: moe/mod.rs, moe/init.rs, qwen3_attention/init.rs) or says that
+    the pages have no counterpart."""
+    src = open(HEADER).read()
+    decls = list(re.finditer(r"\n(moe_status_t|const char\*)\s+(moe_[a-z_0-9]+)\s*\(", src))
+    assert {m.group(2) for m in decls} == set(capi.EXPORTED)
+    for m in decls:
+        before = src[:m.start() + 1]
+        # the comment block that ends right before this declaration (or before the previous
+        # declaration of a pair that shares one comment)
+        end = before.rfind("*/")
+        start = before.rfind("/*", 0, end)
+        comment = before[start:end]
+        between = before[end + 2:]
+        assert re.fullmatch(r"\s*(moe_status_t [^;]*;\s*)?", between, flags=re.S), m.group(2)
+        assert ("moe/mod.rs" in comment or "moe/init.rs" in comment or
+                "qwen3_attention/init.rs" in comment or "no counterpart" in comment), m.group(2)

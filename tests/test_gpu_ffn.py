@@ -74,6 +74,20 @@ SMALL = {
     "tc_many_mx": S.MoeConfig("tc_many_mx", T=1040, H=768, I=512, E=4, k=2,
                              scoring=S.SCORE_SOFTMAX, I_shared=256, fmt=S.FMT_MXFP4,
                              shared_fmt=S.FMT_NVFP4, act=S.ACT_NVFP4),
+    # the prefill recipe at reduced size, every row compared: Zipf-skewed counts (the head
+    # experts capped at every token, 16 padded 128-row blocks; the tail a partial block each)
+    "tc_zipf_all_rows": S.MoeConfig("tc_zipf_all_rows", T=2048, H=768, I=512, E=24, k=8,
+                                    scoring=S.SCORE_SIGMOID, scaling=2.5, I_shared=256,
+                                    act=S.ACT_NVFP4, zipf_s=1.1),
+    # hash-table ids weighted by the router's sqrt(softplus) scores, on the bf16 many-token
+    # path and on the tensor-core path
+    "hash_sqrt": S.MoeConfig("hash_sqrt", T=20, H=256, I=128, E=16, k=3,
+                             scoring=S.SCORE_HASH_SQRTSOFTPLUS, scaling=1.5, I_shared=128,
+                             fmt=S.FMT_MXFP4, vocab=100),
+    "hash_sqrt_tc": S.MoeConfig("hash_sqrt_tc", T=64, H=512, I=512, E=16, k=6,
+                                scoring=S.SCORE_HASH_SQRTSOFTPLUS, I_shared=512,
+                                fmt=S.FMT_MXFP4, shared_fmt=S.FMT_NVFP4, vocab=500,
+                                act=S.ACT_NVFP4),
 }
 
 
@@ -103,28 +117,112 @@ def test_small_configs(cuda_lib, name):
     parity.assert_close(out, ref, name)
 
 
+def covering_tokens(ids, E, per_expert=2, extra=(0, 1)):
+    """Tokens such that every routed expert is compared: each expert's first and last token
+    (in token order) and, for experts with many rows, per_expert more spread over its tokens;
+    plus the `extra` tokens.  Sorted, unique."""
+    pick = set(int(t) for t in extra)
+    for e in range(E):
+        toks = np.nonzero((ids == e).any(1))[0]
+        if len(toks) == 0:
+            continue
+        pick.update([int(toks[0]), int(toks[-1])])
+        if len(toks) > 256:
+            pick.update(int(t) for t in toks[np.linspace(0, len(toks) - 1, per_expert + 2)[1:-1].astype(int)])
+    return sorted(pick)
+
+
 FULL = {
-    "dec1": (S.CONFIGS["dec1"], None),
-    "dec8": (S.CONFIGS["dec8"], None),
-    "hash64": (S.CONFIGS["hash64"], [0, 1, 17, 38, 62, 63]),
-    "pre4096": (S.CONFIGS["pre4096"], [0, 1, 2047, 4095]),
+    "dec1": S.CONFIGS["dec1"],
+    "dec8": S.CONFIGS["dec8"],
+    "hash64": S.CONFIGS["hash64"],
+    "pre4096": S.CONFIGS["pre4096"],
 }
 
 
 @pytest.mark.parametrize("name", list(FULL))
 def test_full_size_configs(cuda_lib, name):
-    cfg, sample = FULL[name]
+    """Full-size workloads: every token for the decode and hash workloads; for the prefill
+    workload the first and last token of every routed expert (a few hundred tokens) plus
+    tokens spread over the Zipf head's rows; all rows finite and nonzero."""
+    cfg = FULL[name]
     inp, _ = parity.make_case(cfg, seed=0, device="cuda")
     ref_r = parity.oracle_route(cfg, inp)
     ids, w, out, status, logits = _run(cfg, inp, with_logits=True)
     assert status == 0
     parity.assert_routing(cfg, ref_r, ids, w, gpu_logits=logits, inp=inp)
+    sample = None
+    if cfg.T > 64:
+        sample = covering_tokens(ref_r["ids"], cfg.E, per_expert=6, extra=(0, 1, cfg.T - 1))
+        assert len(sample) >= cfg.E  # (a few hundred tokens at 4096)
     ref = parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"], tokens=sample)
     got = out if sample is None else out[sample]
     parity.assert_close(got, ref, name)
     # every output row is finite and the unsampled rows are not left untouched
     assert torch.isfinite(out.float()).all()
     assert (out.float().abs().amax(1) > 0).all()
+
+
+def test_mxfp4_blocks_far_below_the_largest_scale(cuda_lib):
+    """MXFP4 blocks far below their tensor's largest scale: the tensor-core path re-expresses
+    E8M0 scales as E4M3 powers of two and flushes blocks more than 2^17 below the largest to
+    zero; the few-token path's f16 scale flushes blocks more than 2^27 below.  Rows whose
+    every block sits 18, 20 or 28 binades below the largest must still match the oracle (an
+    element of a flushed block is below 6 * 2^-17 of the largest block's scale)."""
+    cases = [SMALL["tc_mx_routed"],
+             S.MoeConfig("mx_flush_dec", T=5, H=512, I=256, E=12, k=4, scoring=S.SCORE_SIGMOID,
+                         scaling=2.5, I_shared=128, fmt=S.FMT_MXFP4, shared_fmt=S.FMT_NVFP4),
+             S.MoeConfig("mx_flush_generic", T=24, H=256, I=256, E=12, k=4,
+                         scoring=S.SCORE_SOFTMAX, fmt=S.FMT_MXFP4)]
+    for cfg in cases:
+        inp, _ = parity.make_case(cfg, seed=8, device="cpu")
+        ref_r = parity.oracle_route(cfg, inp)
+        e = int(ref_r["ids"][0, 0])  # an expert that is routed
+        for key, drops in (("gate", (18, 20, 28)), ("up", (20, 28, 18)), ("down", (28, 18, 20))):
+            sc = inp[key]["scales"].clone()
+            bmax = int(sc[e].max())
+            n = sc.shape[1]
+            for i, d in enumerate(drops):
+                rows = slice(i * n // 8, i * n // 8 + n // 16)
+                sc[e, rows] = bmax - d
+            inp[key] = dict(inp[key], scales=sc)
+        ids, w, out, status = _run(cfg, inp)
+        assert status == 0
+        parity.assert_routing(cfg, ref_r, ids, w)
+        parity.assert_close(out, parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"]), cfg.name)
+
+
+GIVEN = {
+    "decode": S.MoeConfig("given_dec", T=6, H=256, I=128, E=16, k=3, scoring=S.SCORE_SOFTMAX,
+                          I_shared=128, zero_experts=2),
+    "generic": S.MoeConfig("given_generic", T=20, H=256, I=128, E=16, k=3,
+                           scoring=S.SCORE_SOFTMAX, I_shared=128, zero_experts=2),
+    "tc": S.MoeConfig("given_tc", T=40, H=512, I=256, E=16, k=3, scoring=S.SCORE_SOFTMAX,
+                      I_shared=256, act=S.ACT_NVFP4, zero_experts=2),
+}
+
+
+@pytest.mark.parametrize("name", list(GIVEN))
+def test_given_ids_out_of_range(cuda_lib, name):
+    """moe_ffn_forward with caller ids: ids outside [-1] + [0, E + Z) are dropped and flagged
+    with MOE_DEV_BAD_EXPERT_ID on every path (few-token, bf16 many-token, tensor cores); -1 is
+    a silent drop; zero-computation ids add w * x."""
+    cfg = GIVEN[name]
+    inp, _ = parity.make_case(cfg, seed=7, device="cpu")
+    ref_r = parity.oracle_route(cfg, inp)
+    ids = ref_r["ids"].copy()
+    w = ref_r["w"].astype(np.float32)
+    ids[1, 0] = 99          # beyond E + Z
+    ids[2, 1] = -5          # negative, not -1
+    ids[3, 2] = -1          # the drop marker
+    ids[4, 0] = cfg.E + 1   # a zero-computation expert
+    layer = MoeLayer.from_inputs(inp)
+    x = inp["x"].cuda()
+    out = layer.ffn(x, torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda())
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == capi.MOE_DEV_BAD_EXPERT_ID
+    layer.close()
+    parity.assert_close(out, parity.oracle_ffn(cfg, inp, ids, w.astype(np.float64)), name)
 
 
 DROP = {

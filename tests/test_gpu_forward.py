@@ -9,6 +9,7 @@ checked against the oracle's top-K of the GPU's own fp32 logits; outputs within
 max|gpu - ref| <= 1e-2 * max|ref| + 1e-3.
 """
 import dataclasses
+import time
 
 import numpy as np
 import pytest
@@ -55,6 +56,16 @@ CASES = {
                                             scoring=S.SCORE_SOFTMAX_BIAS, zero_experts=6),
     "zero_hash": S.MoeConfig("fw_zero_hash", T=6, H=256, I=256, E=16, k=4, scoring=S.SCORE_HASH,
                              I_shared=128, fmt=S.FMT_MXFP4, vocab=50, zero_experts=3),
+    # hash-table ids weighted by the router's sqrt(softplus) scores: the router GEMV still runs
+    # in the single launch, the table replaces the top-K
+    "hash_sqrt": S.MoeConfig("fw_hash_sqrt", T=6, H=512, I=256, E=16, k=4,
+                             scoring=S.SCORE_HASH_SQRTSOFTPLUS, scaling=1.5, I_shared=128,
+                             fmt=S.FMT_MXFP4, vocab=50),
+    "t1_hash_sqrt": S.MoeConfig("fw_t1_hash_sqrt", T=1, H=256, I=384, E=12, k=6,
+                                scoring=S.SCORE_HASH_SQRTSOFTPLUS, renorm=False, vocab=40),
+    "fallback_hash_sqrt_tc": S.MoeConfig("fw_hash_sqrt_tc", T=40, H=512, I=256, E=16, k=4,
+                                         scoring=S.SCORE_HASH_SQRTSOFTPLUS, scaling=2.0,
+                                         I_shared=256, act=S.ACT_NVFP4, vocab=64),
     # more tokens: moe_route + moe_ffn_forward behind the same call
     "fallback_generic": S.MoeConfig("fw_generic", T=20, H=256, I=128, E=16, k=3,
                                     scoring=S.SCORE_SIGMOID, scaling=2.5, I_shared=128),
@@ -200,4 +211,35 @@ def test_forward_zero_tokens_and_arg_checks(cuda_lib):
                          layer.workspace(cfg.T),
                          logits_out=torch.empty((cfg.T, cfg.E + 1), device="cuda"))
     assert ei.value.status == capi.MOE_ERR_INVALID_ARG
+    layer.close()
+
+
+def test_barrier_wait_runs_out(cuda_lib):
+    """The few-token kernel's device-wide barrier waits are bounded.  With a 10 ms limit and
+    the handle's ticket counter advanced by one (moe_skew_barrier), one thread block waits for
+    an arrival that never comes: the launch must return (well inside a second), set
+    MOE_DEV_TIMEOUT, and leave the device usable -- a fresh handle then gives correct results."""
+    cfg = CASES["ragged"]
+    inp, _ = parity.make_case(cfg, seed=6, device="cpu")
+    layer = MoeLayer.from_inputs(inp)
+    x = inp["x"].cuda()
+    layer.forward(x)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    capi.moe_set_wait_limit(layer.handle, 20_000_000)  # SM cycles: about 10 ms
+    layer.forward(x)                                    # a short limit alone changes nothing
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    capi.moe_skew_barrier(layer.handle)
+    t0 = time.perf_counter()
+    layer.forward(x)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(layer.status.item()) & capi.MOE_DEV_TIMEOUT
+    assert dt < 1.0, f"the timed-out launch took {dt:.3f} s"
+    layer.close()
+    ref_r = parity.oracle_route(cfg, inp)
+    layer = MoeLayer.from_inputs(inp)
+    out, ids, w, logits = _forward(layer, inp)
+    _check(cfg, inp, ref_r, out, ids, w, logits, int(layer.status.item()))
     layer.close()

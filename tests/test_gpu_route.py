@@ -48,6 +48,13 @@ CASES = {
     "tc_router": synth.MoeConfig("tr", T=300, H=384, I=128, E=128, k=6, scoring=synth.SCORE_SOFTMAX),
     "tc_router_sig": synth.MoeConfig("trs", T=129, H=1152, I=128, E=256, k=8,
                                      scoring=synth.SCORE_SIGMOID, scaling=2.5),
+    # hash-table ids, sqrt(softplus) router-score weights (router on the tensor cores, then the
+    # hash kernel reads the logits)
+    "hash_sqrt": synth.MoeConfig("hs", T=200, H=1024, I=128, E=128, k=6,
+                                 scoring=synth.SCORE_HASH_SQRTSOFTPLUS, scaling=2.5, vocab=1000),
+    "hash_sqrt_norenorm": synth.MoeConfig("hsn", T=7, H=256, I=128, E=64, k=6,
+                                          scoring=synth.SCORE_HASH_SQRTSOFTPLUS, renorm=False,
+                                          vocab=30),
 }
 
 
