@@ -767,7 +767,9 @@ void tc_release(TcWeights* tw) {
 
 // ------------------------------------------------------------------------------------------
 // Router logits of many tokens on the tensor cores: logits[t][e] = x[t] . W_r[e] (bf16 in,
-// fp32 out), one 128-token x 128-expert tile per CTA over the whole K = H.  Warp 0 issues the
+// fp32 out), one 128-token x 128-expert tile and one half of K = H per CTA: the two halves are
+// added into the zeroed logits with fp32 atomics (exactly two addends onto zero, so the result
+// does not depend on their order), which doubles the CTAs a few tiles give.  Warp 0 issues the
 // TMA loads into a 4-stage ring (64 elements of K per stage, 128-byte swizzled rows), one lane
 // of warp 1 issues tcgen05.mma.kind::f16 (M 128, N 128, K 16; four per stage) into a 128-column
 // TMEM accumulator, warps 2-5 (one per lane quarter) read it back and write fp32 rows.  Every
@@ -794,7 +796,8 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, float* __restrict__ logits
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t0 = blockIdx.x * 128, e0 = blockIdx.y * 128, nk = H / 64;
+    const int t0 = blockIdx.x * 128, e0 = blockIdx.y * 128;
+    const int nk = H / 128, k0 = blockIdx.z * nk;  // this CTA's half of the 64-element K steps
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRtStages; ++s) {
             mbar_init(&full[s], 1);
@@ -820,14 +823,15 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, float* __restrict__ logits
         for (int ks = 0; ks < nk && !*abort_flag; ++ks) {
             const int s = ks % kRtStages;
             const uint32_t ph = (ks / kRtStages) & 1u;
+            const int kx = (k0 + ks) * 128;  // bytes along the bf16 row
             if (!mbar_wait_bounded(&empty[s], ph ^ 1u, kTcWaitLimit)) {
                 give_up();
                 break;
             }
             uint8_t* base = smem + s * kRtStageBytes;
             mbar_arrive_expect_tx(&full[s], kRtStageBytes);
-            tma_load_2d(base, &maps.x, ks * 128, t0, &full[s]);
-            tma_load_2d(base + 128 * 128, &maps.w, ks * 128, e0, &full[s]);
+            tma_load_2d(base, &maps.x, kx, t0, &full[s]);
+            tma_load_2d(base + 128 * 128, &maps.w, kx, e0, &full[s]);
             ++issued;
         }
         if (*abort_flag)  // wait (bounded) for the copies still in flight
@@ -875,10 +879,9 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, float* __restrict__ logits
                 if (t < T) {
                     float* dst = logits + (size_t)t * E + e0 + c;
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        const uint32_t (&w8)[8] = *reinterpret_cast<const uint32_t(*)[8]>(v + i);
-                        st_global_v8(dst + i, w8);
-                    }
+                    for (int i = 0; i < 32; i += 4)
+                        red_add_v4(dst + i, __uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                   __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
                 }
             }
         } else if (!ok) {
@@ -896,7 +899,7 @@ router_tc_kernel(const __grid_constant__ RtMaps maps, float* __restrict__ logits
 cudaError_t launch_router_tc(const void* x, const void* wr, float* logits, int T, int E, int H,
                              int32_t* status, cudaStream_t st) {
     if (T < 128 || E % 128 != 0 || H % 128 != 0 || encode_fn() == nullptr) return cudaErrorNotSupported;
-    // TMA sources 16-byte aligned, 32-byte row stores
+    // TMA sources 16-byte aligned, 16-byte vector reductions
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(wr)) % 16 != 0 ||
         reinterpret_cast<uintptr_t>(logits) % 32 != 0)
         return cudaErrorNotSupported;
@@ -911,7 +914,9 @@ cudaError_t launch_router_tc(const void* x, const void* wr, float* logits, int T
         if (err != cudaSuccess) return err;
         attr_set = true;
     }
-    router_tc_kernel<<<dim3((T + 127) / 128, E / 128), kRtThreads, kRtSmemBytes, st>>>(m, logits, T, E, H, status);
+    cudaError_t err = cudaMemsetAsync(logits, 0, sizeof(float) * (size_t)T * E, st);
+    if (err != cudaSuccess) return err;
+    router_tc_kernel<<<dim3((T + 127) / 128, E / 128, 2), kRtThreads, kRtSmemBytes, st>>>(m, logits, T, E, H, status);
     return cudaGetLastError();
 }
 

@@ -61,6 +61,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
         "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+// Four fp32 atomic adds to 16 consecutive bytes (address 16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
 // Contiguous bulk copy global -> shared (addresses 16-byte aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
