@@ -22,7 +22,7 @@
 // tiles sharing the activation chunk of the step); a down stage is two K-steps of 16 rows.
 // A stage also holds the block scales and the activations (x in f16 for gate+up, h for
 // down).  The activations take 256 B per token column and K-step, so a one-token launch
-// has stages of 3 KiB instead of 6.5 KiB and rings of 7 stages instead of 3.  The down weights depend only on the routing, so they are already in flight while
+// has stages of 3 KiB instead of 6.5 KiB.  The down weights depend only on the routing, so they are already in flight while
 // the CTA waits at barrier 2; the h chunks of the down stages issued before that barrier are
 // copied right after it.
 //
@@ -59,17 +59,19 @@ constexpr int kDecRingBudget = 232448 - kDecRedG - 6144;
 //   down:    [0, kDnCodes) activation chunks of the two K-steps, kAct each
 //            [kDnCodes, kDnSc) codes, 512 B each of (step u, rows +8 r) at (2u + r)
 //            [kDnSc, +512) scales, 256 B per step
-// As many stages as the budget holds (fewer tokens -> smaller stages -> a deeper ring).
+// Three stages per warp.  A one-token stage is 3 KiB, so seven would fit, but priming six of
+// them per warp on every SM asks for most of a layer's weights in one burst and delays each
+// warp's first stage: one token took 24.3 us per layer step with 7-stage rings, 23.5 with 5,
+// 22.6 with 4 and 22.0 with 3.
 template <int TPS, int NTOK>
 struct DecGeom {
     static constexpr int kAct = NTOK * 256;
     static constexpr int kGuAct = TPS * 2048, kGuSc = kGuAct + kAct, kGuBytes = kGuSc + TPS * 256;
     static constexpr int kDnCodes = 2 * kAct, kDnSc = kDnCodes + 2048, kDnBytes = kDnSc + 512;
     static constexpr int kStageBytes = ((kGuBytes > kDnBytes ? kGuBytes : kDnBytes) + 127) / 128 * 128;
-    static constexpr int kFit = kDecRingBudget / (kDecWarps * kStageBytes);
-    static constexpr int kStages = kFit < 8 ? kFit : 8;
+    static constexpr int kStages = 3;
     static constexpr int kRingBytes = kDecWarps * kStages * kStageBytes;
-    static_assert(kStages >= 3, "ring too shallow");
+    static_assert(kRingBytes <= kDecRingBudget, "ring does not fit");
 };
 constexpr int kDecRedDTile = kDecWarps * 128 * 4;
 constexpr int kDecMaxTilesPerCta = 4;
@@ -867,7 +869,7 @@ static cudaError_t launch_decode_fused_ntok(const FfnLaunch& L, const DecRoute& 
     return launch_fused_fmt<1, 1, NTOK>(L, R, bar, sms, st);
 }
 
-// one token (compact activation chunks, deeper rings): compiled in its own translation unit
+// one token (compact activation chunks): compiled in its own translation unit
 cudaError_t launch_decode_fused_t1(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
                                    int sms, cudaStream_t st);
 

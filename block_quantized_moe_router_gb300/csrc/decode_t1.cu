@@ -1,5 +1,5 @@
 // decode_t1.cu -- the fused few-token MoE block instantiated for one token: activation chunks
-// of 256 B per K-step instead of 2 KiB, so the stages are smaller and the rings deeper.
+// of 256 B per K-step instead of 2 KiB, so its stages are 3 KiB instead of 6.5 KiB.
 #include "decode_kernel.cuh"
 
 namespace moe {
