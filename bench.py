@@ -15,7 +15,8 @@ one line per other workload (dec1, dec8, hash64, pre32768) under "per_workload".
 carries MoE-layer tokens/s (whole job), the roofline of the dominant kernel (algorithmic bytes
 or FLOPs / its CUDA-event duration inside the timed regions), the clocks seen during the timed
 regions, an end-to-end figure through the public API with host buffers, and (headline only) the
-CPU oracle's throughput on a bounded sample.
+CPU oracle's throughput on a bounded sample.  The per-workload lines time whole cycles over their
+weight replicas (a given step count is rounded up to a multiple of the replica count).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config pre4096] [--impl reference]
 """
@@ -347,9 +348,12 @@ def zipf_record(cfg, ids):
             "total_variation_vs_targets": round(float(np.abs(by_rank - tgt).sum() / (2.0 * cfg.T * cfg.k)), 4)}
 
 
-def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True):
+def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True, whole_cycles=False):
     """One workload: build its replicas, capture the step graphs, warm up, run the timed
-    regions, then the end-to-end leg.  Returns the line's fields (rank 0) or None."""
+    regions, then the end-to-end leg.  Returns the line's fields (rank 0) or None.
+    whole_cycles: round a given step count up to whole cycles over the weight replicas, so
+    that every region replays the graph of one step per replica (fewer steps would replay
+    one-step graphs, each its own graph launch)."""
     from block_quantized_moe_router_gb300 import capi
     from block_quantized_moe_router_gb300.layer import MoeLayer
 
@@ -369,6 +373,8 @@ def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True):
     replicas = max(1, math.ceil(4 * l2 / nbytes["total"]))
     if args.replicas:
         replicas = args.replicas
+    if whole_cycles and steps is not None:
+        steps = -(-steps // replicas) * replicas
 
     layers = [base]
     for _ in range(replicas - 1):
@@ -619,7 +625,7 @@ def run_ours(args, cfg):
             if name == cfg.name:
                 continue
             res = measure(synth.CONFIGS[name], args, args.steps, dist, world, rank, local,
-                          want_e2e=args.e2e)
+                          want_e2e=args.e2e, whole_cycles=True)
             if res is not None:
                 others[name] = res
     if rank == 0:
