@@ -9,9 +9,10 @@
 // Data flow (every step on the device, no host synchronisation):
 //   tc_hist_kernel / tc_scan_kernel / tc_scatter_kernel  histogram of the routed pairs,
 //                    expert rows padded to 128 (one MMA M tile), padded-row -> pair map,
-//                    per-128-row block -> expert map, and the two tile lists (expert-major,
-//                    then N block, then M block, so that concurrently running CTAs share one
-//                    expert's weight tile through L2);
+//                    per-128-row block -> expert map, and the two tile lists (expert-major;
+//                    gate+up then M block, then N block, so that concurrently running CTAs
+//                    share one block of token rows and the expert's weight tiles stay in L2 for
+//                    its next block; down then N block, then M block);
 //   tc_quant_tokens_kernel / tc_gather_rows_kernel  NVFP4 quantization of every token once,
 //                    then a copy of each pair's token row into its padded row with the scales
 //                    rearranged into the 128 x 4 scale-factor tile layout of the MMA;
@@ -210,9 +211,15 @@ __global__ void __launch_bounds__(1024) tc_scatter_kernel(TcPrepArgs a) {
                 if (tb[mid] <= t) lo = mid; else hi = mid;
             }
             while (lo < E && tb[lo + 1] <= t) ++lo;  // skip experts with no tiles
+            // gate+up: M block outer, N block inner -- the 16 tiles of one block of token rows
+            // run at the same time (its rows are read once from HBM) and the expert's weight
+            // tiles are reused from L2 by its next row block (at 32768 tokens this halves the
+            // launch's DRAM reads); down: N block outer, M block inner (measured faster there)
             const int nmb = mbase[lo + 1] - mbase[lo];
+            const int nnb = (lo < E ? a.I : a.I_shared) / 128;
             const int r = t - tb[lo];
-            const int nb = r / nmb, mb = r - nb * nmb;
+            const int mb = pass == 0 ? r / nnb : r % nmb;
+            const int nb = pass == 0 ? r % nnb : r / nmb;
             const int K = pass == 0 ? a.H : (lo < E ? a.I : a.I_shared);
             out[t] = make_int4(mbase[lo] + mb, nb, lo, K / 256);
         }
