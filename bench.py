@@ -15,8 +15,9 @@ one line per other workload (dec1, dec8, hash64, pre32768) under "per_workload".
 carries MoE-layer tokens/s (whole job), the roofline of the dominant kernel (algorithmic bytes
 or FLOPs / its CUDA-event duration inside the timed regions), the clocks seen during the timed
 regions, an end-to-end figure through the public API with host buffers, and (headline only) the
-CPU oracle's throughput on a bounded sample.  The per-workload lines time whole cycles over their
-weight replicas (a given step count is rounded up to a multiple of the replica count).
+CPU oracle's throughput on a bounded sample.  The per-workload lines time regions of whole cycles
+over their weight replicas and of at least --min-region-ms of work (a given step count is rounded
+up accordingly); the headline times exactly the given K.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config pre4096] [--impl reference]
 """
@@ -357,9 +358,9 @@ def zipf_record(cfg, ids):
 def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True, whole_cycles=False):
     """One workload: build its replicas, capture the step graphs, warm up, run the timed
     regions, then the end-to-end leg.  Returns the line's fields (rank 0) or None.
-    whole_cycles: round a given step count up to whole cycles over the weight replicas, so
-    that every region replays the graph of one step per replica (fewer steps would replay
-    one-step graphs, each its own graph launch)."""
+    whole_cycles: for the extra per-workload lines -- regions of whole cycles over the weight
+    replicas (fewer steps would replay one-step graphs, each its own graph launch) and of at
+    least min_region_ms of work (a region also times the launch of its first graph)."""
     from block_quantized_moe_router_gb300 import capi
     from block_quantized_moe_router_gb300.layer import MoeLayer
 
@@ -379,8 +380,6 @@ def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True, whole_cyc
     replicas = max(1, math.ceil(4 * l2 / nbytes["total"]))
     if args.replicas:
         replicas = args.replicas
-    if whole_cycles and steps is not None:
-        steps = -(-steps // replicas) * replicas
 
     layers = [base]
     for _ in range(replicas - 1):
@@ -449,6 +448,10 @@ def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True, whole_cyc
         w1.record(stream)
         torch.cuda.synchronize()
         step_s = w0.elapsed_time(w1) * 1e-3 / args.warmup
+        if whole_cycles and steps is not None:
+            per_cycle = max(step_s * replicas, 1e-9)
+            cycles = max(-(-steps // replicas), int(math.ceil(args.min_region_ms * 1e-3 / per_cycle)))
+            steps = int(max_over_ranks([cycles * replicas], dist, device="cuda")[0])
         if steps is None:  # about one second of timed work, the same on every rank
             try:
                 steps = auto_steps(step_s, replicas)
@@ -670,6 +673,8 @@ def main():
     ap.add_argument("--min-timed-s", type=float, default=1.0,
                     help="repeat the timed region until about this much timed work")
     ap.add_argument("--max-regions", type=int, default=5000)
+    ap.add_argument("--min-region-ms", type=float, default=5.0,
+                    help="per-workload lines: at least this much work per timed region")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--replicas", type=int, default=0,
