@@ -24,9 +24,10 @@
 //   tc_combine_kernel  out[t] = sum_j y[t, j] + y_shared[t].
 //
 // The GEMM kernel is persistent (one CTA per SM, tiles strided by the grid) and warp
-// specialised: warp 0 issues TMA / bulk copies into a 3-stage shared-memory ring, warp 1
-// allocates TMEM and one of its lanes issues tcgen05.cp (scale factors) and tcgen05.mma,
-// warps 2-9 drain the accumulator with tcgen05.ld.  Every mbarrier wait is bounded; a wait
+// specialised: warp 0 issues TMA / bulk copies into a 4-stage shared-memory ring, warp 1
+// allocates TMEM and one of its lanes issues tcgen05.mma, warps 2-9 drain the accumulator with
+// tcgen05.ld, warps 10-13 (one per TMEM lane quarter) write the stage's scale factors into
+// TMEM with tcgen05.st.  Every mbarrier wait is bounded; a wait
 // that gives up sets MOE_DEV_TIMEOUT, the CTA stops issuing work, waits (bounded) for its
 // copies and MMAs in flight, frees TMEM and returns.  The file also holds the many-token
 // router GEMM on the tensor cores (tcgen05.mma.kind::f16, bf16 in, fp32 logits).
@@ -48,21 +49,27 @@ constexpr int kTcABytes = 128 * 128;          // 128 rows x 128 B (256 E2M1 code
 constexpr int kTcBBytes = 256 * 128;          // 256 rows x 128 B
 constexpr int kTcSfaBytes = 4 * 512;          // 4 K blocks of 64 x one 128-row scale tile
 constexpr int kTcSfaOff = kTcABytes + kTcBBytes;
-constexpr uint32_t kTcTmemCols = 512;  // 256 accumulator + 3 stages x 48 scale columns, rounded
+constexpr uint32_t kTcTmemCols = 512;  // 256 accumulator + 4 stages x 48 scale columns, rounded
                                        // up to the power of two an allocation takes
-// B's scales reach TMEM as quarter tiles: a stage's scales (for a 256-row block of B and its 4
-// K blocks, the 16-byte lines of both 128-row scale tiles in the order the 32 TMEM lanes of
-// one lane quarter read them) are prepared once as one 4 KB tile, bulk-copied into each of
-// the four lane quarters' shared-memory slices (the three repeats hit L2), then moved by one
-// 128-lane copy per K block.  A copy that replicates 32 lanes to the four quarters
-// (`32x128b.warpx4`, used for A's scales) costs the tensor pipe several times more.  3 stages
-// of 66 KiB.
-constexpr int kTcStages = 3;
-constexpr int kTcSfbBytes = 4 * 4096;
+// Scale factors: the MMA reads the same 32 lanes x 8 columns per K block of B's scales, and the
+// same 32 lanes x 4 columns of A's, from each of the four TMEM lane quarters.  A stage's B
+// scales (for a 256-row block of B and its 4 K blocks, the 16-byte lines of both 128-row scale
+// tiles in the order the 32 lanes of one quarter read them) are prepared once as one 4 KB tile,
+// A's as 4 tiles of 512 B; both are bulk-copied into the stage once, and four scale warps, one
+// per lane quarter, load them from shared memory and write them into their quarter with
+// tcgen05.st.  That keeps the scale copies off the tensor pipe (a 128-lane tcgen05.cp needs a
+// tile four times in shared memory, a copy that replicates 32 lanes to the four quarters costs
+// the pipe several times more) and leaves room for a fourth stage: 4 stages of 54 KiB.
+constexpr int kTcStages = 4;
+constexpr int kTcSfbBytes = 4096;
 constexpr int kTcSfbOff = kTcSfaOff + kTcSfaBytes;
-constexpr int kTcStageBytes = kTcSfbOff + kTcSfbBytes;  // 67584 (66 KiB, 1 KiB multiple)
+constexpr int kTcStageBytes = kTcSfbOff + kTcSfbBytes;  // 55296 (54 KiB, 1 KiB multiple)
 constexpr int kTcSmemBytes = kTcStages * kTcStageBytes + 1024 + 256;
-constexpr int kTcThreads = 320;    // producer warp, MMA warp, 8 epilogue warps
+constexpr int kTcThreads = 448;    // producer warp, MMA warp, 8 epilogue warps, 4 scale warps
+constexpr int kTcScaleWarp0 = 10;
+// Registers: each of the SM's four sub-partitions holds 16384, and 14 warps put four warps on
+// two of them, so a thread may use at most 128 (the epilogue's 128-column slice spills a little).
+constexpr int kTcMaxRegs = 128;
 constexpr int kTcEpiThreads = 256;
 constexpr uint64_t kTcWaitLimit = 1ull << 26;  // polls before a wait is declared stuck
 
@@ -312,7 +319,7 @@ __device__ __forceinline__ void tc_abort(TcGemmParams const& p, volatile int* fl
     status_or(p.status, MOE_DEV_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __maxnreg__(kTcMaxRegs)
 tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -322,7 +329,8 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
     uint64_t* acc_full = empty + kTcStages;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* drain = acc_empty + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sfr = drain + 1;  // per stage: B's scales are in TMEM (one arrival per scale warp)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfr + kTcStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -330,6 +338,7 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sfr[s], 4);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kTcEpiThreads);
@@ -382,16 +391,14 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                                     &full[stage]);
                         const size_t tix = ((size_t)es * (N / 128) + nb) * (p.H / 64) + 4 * ks;
                         const uint8_t* q4 = (sh ? p.ssfb0 : p.sfb0) + tix * 1024;  // quarter tile
-                        for (int qd = 0; qd < 4; ++qd)
-                            bulk_load(base + kTcSfbOff + qd * (kTcSfbBytes / 4), q4, kTcSfbBytes / 4, &full[stage]);
+                        bulk_load(base + kTcSfbOff, q4, kTcSfbBytes, &full[stage]);
                     } else {
                         const int K = sh ? p.I_shared : p.I;
                         const int row = es * p.H + nb * 256;
                         tma_load_2d(base + kTcABytes, sh ? &maps.sb0 : &maps.b0, xb, row, &full[stage]);
                         const uint8_t* q4 = (sh ? p.ssfb0 : p.sfb0) +
                                             (((size_t)es * (p.H / 256) + nb) * (K / 64) + 4 * ks) * 1024;
-                        for (int qd = 0; qd < 4; ++qd)
-                            bulk_load(base + kTcSfbOff + qd * (kTcSfbBytes / 4), q4, kTcSfbBytes / 4, &full[stage]);
+                        bulk_load(base + kTcSfbOff, q4, kTcSfbBytes, &full[stage]);
                     }
                     ++issued;
                     if (++stage == kTcStages) { stage = 0; phase ^= 1u; }
@@ -423,7 +430,8 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                 tc_fence_after();
                 bool ok = true;
                 for (int ks = 0; ks < kst; ++ks) {
-                    if (!mbar_wait_bounded(&full[stage], phase, kTcWaitLimit) || *abort_flag) {
+                    if (!mbar_wait_bounded(&full[stage], phase, kTcWaitLimit) ||
+                        !mbar_wait_bounded(&sfr[stage], phase, kTcWaitLimit) || *abort_flag) {
                         tc_abort(p, abort_flag);
                         ok = false;
                         break;
@@ -432,18 +440,13 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                     uint8_t* base = smem + stage * kTcStageBytes;
                     const uint32_t sbase = smem_u32(base);
                     const uint32_t sfcol = 256 + stage * 48;
-                    // scale columns of the stage, per K block j: B's 8 and A's 4
+                    // scale columns of the stage (written by the scale warps), per K block j:
+                    // B's 8 at +8 j, A's 4 at +32 + 4 j
                     uint32_t sfa_c[4], sfb_c[4];
-                    // B: one 128-lane copy per K block j of 128 rows x 32 B (row 32 Q + l =
-                    // line l of both tiles; core matrices of 8 rows x 16 B, 128 B between a
-                    // row's halves, 1 KB between 8-row groups, K block j at +256 j) into columns
-                    // +8 j; A: a replicating copy at +32 + 4 j
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         sfb_c[j] = tmem + sfcol + 8 * j;
                         sfa_c[j] = tmem + sfcol + 32 + 4 * j;
-                        tc_cp_128x256b(sfb_c[j], smem_desc(sbase + kTcSfbOff + 256 * j, 128, 1024, kLayoutNone));
-                        tc_cp_32x128b_warpx4(sfa_c[j], smem_desc(sbase + kTcSfaOff + 512 * j, 0, 128, kLayoutNone));
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -463,6 +466,55 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                 tc_commit(drain);
                 mbar_wait_bounded(drain, 0, kTcWaitLimit);
             }
+        }
+    } else if (warp >= kTcScaleWarp0) {
+        // ---------------- scales into TMEM (warps 10..13, lane quarter warp % 4) ----------
+        // Lane l of every quarter takes, per K block j, the 32 bytes of line l of the stage's
+        // B quarter tile (16 B at 1 KB (l / 8) + 256 j + 16 (l % 8) and 16 B at +128) into
+        // columns 8 j .. 8 j + 7 of the stage's scale columns, and line l of A's K-block tile j
+        // (16 B at 512 j + 16 l: rows l, l + 32, l + 64, l + 96) into columns 32 + 4 j .. +3.
+        const uint32_t qlane = (uint32_t)((warp & 3) * 32) << 16;
+        const int loff = 1024 * (lane >> 3) + 16 * (lane & 7);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+            const int kst = p.tiles[tile].w;
+            bool ok = true;
+            for (int ks = 0; ks < kst; ++ks) {
+                // the whole warp takes one decision (tcgen05.st below is warp-wide)
+                const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&full[stage], phase, kTcWaitLimit) &&
+                                                             !*abort_flag);
+                if (!got) {
+                    if (lane == 0) tc_abort(p, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t* src = smem + stage * kTcStageBytes + kTcSfbOff + loff;
+                uint32_t v[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 lo = *reinterpret_cast<const uint4*>(src + 256 * j);
+                    const uint4 hi = *reinterpret_cast<const uint4*>(src + 256 * j + 128);
+                    v[8 * j + 0] = lo.x; v[8 * j + 1] = lo.y; v[8 * j + 2] = lo.z; v[8 * j + 3] = lo.w;
+                    v[8 * j + 4] = hi.x; v[8 * j + 5] = hi.y; v[8 * j + 6] = hi.z; v[8 * j + 7] = hi.w;
+                }
+                const uint8_t* sa = smem + stage * kTcStageBytes + kTcSfaOff + 16 * lane;
+                uint32_t u[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(sa + 512 * j);
+                    u[4 * j + 0] = a.x; u[4 * j + 1] = a.y; u[4 * j + 2] = a.z; u[4 * j + 3] = a.w;
+                }
+                tmem_st_32(tmem + qlane + 256 + stage * 48, v);
+                tmem_st_16(tmem + qlane + 256 + stage * 48 + 32, u);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfr[stage]);
+                if (++stage == kTcStages) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
         }
     } else {
         // ---------------- epilogue (warps 2..9) ----------------
