@@ -44,7 +44,7 @@ struct Handle {
     bool tc_shape = false;
     TcWeights tc{};        // owned; the tcgen05 path's scale tiles and tensor maps
     int sms = 0;           // SM count of the device the weights live on
-    unsigned long long* bar = nullptr;  // owned; grid-barrier tickets of the few-token kernel
+    unsigned long long* bar = nullptr;  // owned; grid-barrier arrival counter and epoch (few-token kernel)
     unsigned long long wait_cycles = 0;  // device-wide barrier wait limit (0 = the default)
 };
 

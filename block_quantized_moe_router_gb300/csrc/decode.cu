@@ -11,10 +11,10 @@ cudaError_t launch_decode_fused(const FfnLaunch& L, const DecRoute& R, unsigned 
     return launch_decode_fused_ntok<kDecMaxT>(L, R, bar, sms, st);
 }
 
-// One arrival more on the ticket counter: the next fused launch's barriers then complete one
-// thread block early, and that block's last barrier wait runs out its limit (a test aid for the
-// bounded waits; nothing else launches it).
-__global__ void barrier_skew_kernel(unsigned long long* bar) { atomicAdd(bar, 1ull); }
+// The barrier epoch one ahead of the arrival counter: no barrier of the next fused launch can
+// complete, and every wait runs out its limit (a test aid for the bounded waits; nothing else
+// launches it).
+__global__ void barrier_skew_kernel(unsigned long long* bar) { atomicAdd(bar + 1, 1ull); }
 
 cudaError_t launch_barrier_skew(unsigned long long* bar, cudaStream_t st) {
     if (!bar) return cudaErrorInvalidValue;

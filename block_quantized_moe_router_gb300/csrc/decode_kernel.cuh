@@ -29,7 +29,8 @@
 // This is the "gate + top-K fused, expert FFN in two fused stages" structure of the
 // spark_model MoE module doc (moe/mod.rs) taken to a single launch, with the weighted sum
 // (init.rs `moe_weighted_sum_blend`) folded into the down stage.  Grid barriers are bounded
-// spins on a 64-bit ticket counter owned by the weights handle; a wait that runs out sets
+// spins on a 64-bit arrival counter owned by the weights handle, next to an epoch word (the
+// launches completed on the handle) that fixes each launch's targets; a wait that runs out sets
 // MOE_DEV_TIMEOUT and the kernel carries on (its results are then invalid) instead of hanging.
 #pragma once
 #include "common.cuh"
@@ -110,6 +111,9 @@ __device__ __forceinline__ float ld_cg_f32(const float* p) {
     asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
     return v;
 }
+__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -127,17 +131,17 @@ __device__ __forceinline__ int nth_bit(uint32_t mask, int g) {
     return mask ? __ffs(mask) - 1 : -1;
 }
 
-// Grid-wide barrier of a cooperative launch: 64-bit arrival tickets, never reset; barrier
-// instance n completes when the counter reaches (n + 1) * G.  The wait is bounded: after
-// `limit` SM cycles it sets MOE_DEV_TIMEOUT and returns.
-__device__ __forceinline__ void grid_barrier(unsigned long long* bar, int32_t* status,
-                                             long long limit) {
+// Grid-wide barrier of a cooperative launch.  bar[0] counts arrivals and is never reset;
+// bar[1] counts the launches completed on it, so a launch starts with bar[0] = 2 G bar[1] and
+// its two barriers complete at 2 G bar[1] + G and + 2 G (`target`, known to thread 0 of every
+// block from the start).  Thread 0 arrives with a release add that needs no reply and polls
+// with acquire loads.  The wait is bounded: after `limit` SM cycles it sets MOE_DEV_TIMEOUT and
+// returns.
+__device__ __forceinline__ void grid_barrier(unsigned long long* bar, unsigned long long target,
+                                             int32_t* status, long long limit) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned long long G = gridDim.x;
-        const unsigned long long ticket = atomicAdd(bar, 1ull);
-        const unsigned long long target = (ticket / G + 1ull) * G;
+        red_release_add_u64(bar, 1ull);
         const long long t0 = clock64();
         bool done = ld_acquire_u64(bar) >= target;
         int spins = 0;
@@ -147,7 +151,6 @@ __device__ __forceinline__ void grid_barrier(unsigned long long* bar, int32_t* s
             if (!done && clock64() - t0 > limit) break;
         }
         if (!done) status_or(status, MOE_DEV_TIMEOUT);
-        __threadfence();
     }
     __syncthreads();
 }
@@ -308,6 +311,12 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
     const int cnt_d = cta < tiles_out ? (tiles_out - cta + G - 1) / G : 0;
     float* red_g = reinterpret_cast<float*>(dsm + Geo::kRingBytes);
     float* red_d = red_g;  // reused for the down partial sums after barrier 2
+    // this launch's barrier targets (thread 0 of each block runs the barriers)
+    unsigned long long epoch = 0, bar_base = 0;
+    if (tid == 0) {
+        epoch = ld_acquire_u64(bar + 1);
+        bar_base = 2ull * (unsigned long long)G * epoch;
+    }
 
     // ---- phase 0 ----------------------------------------------------------------------------
     // The post-scales (and MXFP4 exponent offsets) of the routed projections for ALL experts
@@ -414,10 +423,12 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
     }
     cp_async_wait<0>();           // the post-scale tables are in
     const long long wait_limit = L.wait_cycles ? (long long)L.wait_cycles : kBarrierCycles;
-    grid_barrier(bar, L.status, wait_limit);  // x16 and the logits are written
+    grid_barrier(bar, bar_base + G, L.status, wait_limit);  // x16 and the logits are written
 
     // ---- phase 1: routing and dispatch ---------------------------------------------------------
     const int P = T * k;
+    // one routed token: its warp builds the dispatch itself (the picks of a top-K are distinct)
+    const bool fast1 = NTOK == 1 && !R.hash_ids && (R.mode == DEC_ROUTE_ROUTER || R.mode == DEC_ROUTE_LOGITS);
     if (R.hash_ids) {
         // ids from the table; weights scaling / k, or from the sqrt(softplus) router scores of
         // the table's experts (logits from phase 0 or given), renormalised per token
@@ -484,7 +495,51 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             else
                 nonfinite = warp_topk<16>(load, R.bias, Er, k, R.scoring, R.renorm, R.scaling, lane, my_e, my_w);
             if (nonfinite && lane == 0 && cta == 0) status_or(L.status, MOE_DEV_NONFINITE);
-            if (lane < k) {
+            if (fast1) {
+                // the real experts among the picks become the slots, in ascending id order; the
+                // zero-computation ones fold into one weight
+                const bool real = lane < k && my_e < E;
+                int rank = 0;
+                for (int j = 0; j < k; ++j) {
+                    const int ej = __shfl_sync(0xffffffffu, my_e, j);
+                    rank += (ej < E && ej < my_e) ? 1 : 0;
+                }
+                const int n_act = __popc(__ballot_sync(0xffffffffu, real));
+                float z = (lane < k && !real) ? my_w : 0.f;
+#pragma unroll
+                for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+                for (int i = lane; i < (k + 1) * (kDecMaxT - 1); i += 32)
+                    D.w[i / (kDecMaxT - 1)][1 + i % (kDecMaxT - 1)] = 0.f;
+                if (real) {
+                    D.expert[rank] = my_e;
+                    D.tokmask[rank] = 1u;
+                    D.w[rank][0] = my_w;
+#pragma unroll
+                    for (int pj = 0; pj < 3; ++pj) {
+                        const bool mx = (pj == 0 ? L.gate.fmt : pj == 1 ? L.up.fmt : L.down.fmt) == MOE_FMT_MXFP4;
+                        D.post[rank][pj] = tab_post[pj * kMaxExperts + my_e];
+                        D.mxb[rank][pj] = mx ? 112 + tab_mx[pj * kMaxExperts + my_e] : 0;
+                    }
+                }
+                if (lane == 0) {
+                    D.n_active = n_act;
+                    S.zw[0] = z;
+                    if (L.I_shared > 0) {
+                        D.expert[n_act] = 0;
+                        D.tokmask[n_act] = 1u;
+                        D.w[n_act][0] = 1.f;
+#pragma unroll
+                        for (int pj = 0; pj < 3; ++pj) {
+                            D.post[n_act][pj] = S.sh_post[pj];
+                            D.mxb[n_act][pj] = S.sh_mxb[pj];
+                        }
+                    }
+                }
+                if (cta == 0 && lane < k) {
+                    R.ids_out[lane] = my_e;
+                    R.w_out[lane] = my_w;
+                }
+            } else if (lane < k) {
                 S.ids[warp * k + lane] = my_e;
                 S.w[warp * k + lane] = my_w;
             }
@@ -498,6 +553,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         S.w[tid] = L.w[tid];
     }
     __syncthreads();
+    if (!fast1) {
     if (R.mode != DEC_ROUTE_GIVEN && cta == 0 && tid < P) {
         R.ids_out[tid] = S.ids[tid];
         R.w_out[tid] = S.w[tid];
@@ -526,6 +582,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             }
         }
         __syncthreads();
+    }
     }
 
     // ---- the work of this CTA and of this warp ----------------------------------------------------
@@ -730,7 +787,8 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
             }
         }
     }
-    grid_barrier(bar, L.status, wait_limit);  // every h is written (and red_g is no longer read)
+    grid_barrier(bar, bar_base + 2ull * G, L.status, wait_limit);  // every h is written (and red_g is no longer read)
+    if (cta == 0 && tid == 0) bar[1] = epoch + 1ull;  // every block has passed barrier 1
 
     // ---- phase 3: down + weighted sum + shared expert ----------------------------------------------
     // the h chunks of the down stages already in the ring, then every later stage copies its own

@@ -170,8 +170,8 @@ struct DecRoute {
 // only by launches of `sms` CTAs.
 cudaError_t launch_decode_fused(const FfnLaunch& L, const DecRoute& R, unsigned long long* bar,
                                 int sms, cudaStream_t st);
-// Adds one to the barrier ticket counter (test aid: the next fused launch's last barrier wait
-// then runs out its limit).
+// Moves the barrier epoch one launch ahead of the arrival counter (test aid: every barrier
+// wait of the next fused launch then runs out its limit).
 cudaError_t launch_barrier_skew(unsigned long long* bar, cudaStream_t st);
 
 cudaError_t launch_quantize_act(const void* x, int64_t rows, int64_t K, float g, uint8_t* packed,

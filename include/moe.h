@@ -245,11 +245,12 @@ moe_status_t moe_ffn_forward_noalloc(const void* handle, int32_t T, int32_t act,
  * moe_set_wait_limit(handle, cycles): every device-wide barrier wait of the few-token kernel
  * launched on `handle` afterwards gives up after `cycles` SM clock cycles (0 = the default,
  * 4e9 cycles, about 2 s) and then sets MOE_DEV_TIMEOUT and carries on.  Host-only.
- * moe_skew_barrier(handle, stream): adds one to the handle's barrier ticket counter on
- * `stream`.  In the next few-token launch one thread block then waits for an arrival that
- * never comes: its wait runs out after the limit, MOE_DEV_TIMEOUT is set, the launch returns
- * normally and its outputs are invalid.  Used by the tests of the timeout path; after it (or
- * after any MOE_DEV_TIMEOUT) release the handle and prepare the weights again.
+ * moe_skew_barrier(handle, stream): moves the handle's barrier epoch (the count of few-token
+ * launches completed on it) one ahead of its arrival counter, on `stream`.  In the next
+ * few-token launch no device-wide barrier can complete: every wait runs out after the limit,
+ * MOE_DEV_TIMEOUT is set, the launch returns normally (after about twice the limit) and its
+ * outputs are invalid.  Used by the tests of the timeout path; after it (or after any
+ * MOE_DEV_TIMEOUT) release the handle and prepare the weights again.
  * Errors: MOE_ERR_INVALID_ARG for a bad handle, MOE_ERR_CUDA if the launch fails. */
 moe_status_t moe_set_wait_limit(void* handle, uint64_t cycles);
 moe_status_t moe_skew_barrier(void* handle, void* stream);

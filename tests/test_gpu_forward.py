@@ -216,8 +216,8 @@ def test_forward_zero_tokens_and_arg_checks(cuda_lib):
 
 def test_barrier_wait_runs_out(cuda_lib):
     """The few-token kernel's device-wide barrier waits are bounded.  With a 10 ms limit and
-    the handle's ticket counter advanced by one (moe_skew_barrier), one thread block waits for
-    an arrival that never comes: the launch must return (well inside a second), set
+    the handle's barrier epoch moved one launch ahead (moe_skew_barrier), no barrier of the
+    next launch can complete: the launch must return (well inside a second), set
     MOE_DEV_TIMEOUT, and leave the device usable -- a fresh handle then gives correct results."""
     cfg = CASES["ragged"]
     inp, _ = parity.make_case(cfg, seed=6, device="cpu")
