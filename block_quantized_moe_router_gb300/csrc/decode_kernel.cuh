@@ -311,12 +311,7 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
     const int cnt_d = cta < tiles_out ? (tiles_out - cta + G - 1) / G : 0;
     float* red_g = reinterpret_cast<float*>(dsm + Geo::kRingBytes);
     float* red_d = red_g;  // reused for the down partial sums after barrier 2
-    // this launch's barrier targets (thread 0 of each block runs the barriers)
-    unsigned long long epoch = 0, bar_base = 0;
-    if (tid == 0) {
-        epoch = ld_acquire_u64(bar + 1);
-        bar_base = 2ull * (unsigned long long)G * epoch;
-    }
+    unsigned long long epoch = 0, bar_base = 0;  // this launch's barrier targets (thread 0)
 
     // ---- phase 0 ----------------------------------------------------------------------------
     // The post-scales (and MXFP4 exponent offsets) of the routed projections for ALL experts
@@ -335,6 +330,15 @@ dec_fused_kernel(FfnLaunch L, DecRoute R, unsigned long long* bar) {
         const ProjView& PV = tid == 0 ? L.sh_gate : tid == 1 ? L.sh_up : L.sh_down;
         S.sh_post[tid] = PV.post[0];
         S.sh_mxb[tid] = PV.fmt == MOE_FMT_MXFP4 ? 112 + PV.mx_off[0] : 0;
+    }
+    // Everything above reads only tables of the prepared weights.  The inputs, the barrier words
+    // and the workspace may belong to the preceding kernel on the stream (a programmatic
+    // launch: this grid may be scheduled before that kernel has finished).
+    pdl_wait();
+    pdl_trigger();
+    if (tid == 0) {  // thread 0 of each block runs the barriers
+        epoch = ld_acquire_u64(bar + 1);
+        bar_base = 2ull * (unsigned long long)G * epoch;
     }
     {   // x -> f16 (this CTA's slice of the flat array)
         const int n8 = T * H / 8;
@@ -896,11 +900,13 @@ static cudaError_t launch_fused_tps(const FfnLaunch& L, const DecRoute& R, unsig
     cfg.blockDim = dim3(kDecThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait in the kernel
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, L, R, bar);
 }
 
