@@ -59,8 +59,8 @@ KERNEL_SOURCES = {
 TRAFFIC = {  # one-pass captures at full size (the commands are in the profile summaries)
     "pre4096": (4733255424, "2c9a5ba3d8804c26"),
     "pre32768": (5961782528, "2c9a5ba3d8804c26"),
-    "dec1": (21883904, "2b0cf46ccd91cad4"),
-    "dec8": (1270616832, "2b0cf46ccd91cad4"),
+    "dec1": (21881344, "047b93c02bb9da69"),
+    "dec8": (1270784256, "047b93c02bb9da69"),
     "hash64": (584604672, "43b546cd6aeb1483"),
 }
 
