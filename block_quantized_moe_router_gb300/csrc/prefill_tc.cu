@@ -319,6 +319,9 @@ __device__ __forceinline__ void tc_abort(TcGemmParams const& p, volatile int* fl
     status_or(p.status, MOE_DEV_TIMEOUT);
 }
 
+// MODE 0: gate+up (epilogue h = SiLU(g) * u, requantized); MODE 1: down (epilogue bf16 pair
+// rows).  p.mode must match.
+template <int MODE>
 __global__ void __maxnreg__(kTcMaxRegs)
 tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -383,7 +386,7 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                     tma_load_2d(base, &maps.a, xb, b * 128, &full[stage]);
                     bulk_load(base + kTcSfaOff, p.sfa + ((size_t)b * p.sfa_kblocks + 4 * ks) * 512,
                               kTcSfaBytes, &full[stage]);
-                    if (p.mode == 0) {
+                    if (MODE == 0) {
                         const int N = sh ? p.I_shared : p.I;
                         const int row = es * N + nb * 128;
                         tma_load_2d(base + kTcABytes, sh ? &maps.sb0 : &maps.b0, xb, row, &full[stage]);
@@ -526,6 +529,21 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
         const int r = quad * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t acc_phase = 0;
+        // down: this row's pair, N block and output scale, read one tile ahead (the scale is a
+        // dependent load, so it is not waited for between a tile's MMAs and the release of
+        // its accumulator)
+        int pair_n = -1, nb_n = 0;
+        float sc_n = 0.f;
+        auto row_scale = [&](int tile) {
+            if (tile >= ntiles) return;
+            const int4 tl = p.tiles[tile];
+            const bool sh = tl.z == p.E;
+            pair_n = p.padrow_pair[tl.x * 128 + r];
+            nb_n = tl.y;
+            const float pd = (sh ? p.spost0 : p.post0)[sh ? 0 : tl.z];
+            sc_n = pair_n < 0 ? 0.f : pd * (pair_n < p.P ? p.topk_w[pair_n] : 1.f);
+        };
+        if (MODE == 1) row_scale(blockIdx.x);
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
             if (!mbar_wait_bounded(acc_full, acc_phase, kTcWaitLimit)) {
                 tc_abort(p, abort_flag);
@@ -533,17 +551,47 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
             }
             if (*abort_flag) break;
             tc_fence_after();
+            if constexpr (MODE == 1) {
+                // output columns [128 half, +128) in two halves, packed to bf16 as they arrive,
+                // so a thread holds 64 packed words instead of 128 accumulators
+                const int pair = pair_n, nb = nb_n;
+                const float sc = sc_n;
+                uint32_t P[64];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t W[64];
+#pragma unroll
+                    for (int c = 0; c < 64; c += 16)
+                        tmem_ld_16(trow + 128 * half + 64 * hh + c, *reinterpret_cast<uint32_t(*)[16]>(W + c));
+                    tmem_ld_wait();
+                    if (hh == 1) {
+                        tc_fence_before();
+                        mbar_arrive(acc_empty);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(W[2 * i]) * sc,
+                                                                 __uint_as_float(W[2 * i + 1]) * sc);
+                        P[32 * hh + i] = *reinterpret_cast<uint32_t*>(&v);
+                    }
+                }
+                acc_phase ^= 1u;
+                row_scale(tile + gridDim.x);
+                if (pair < 0) continue;
+                // 32-byte stores (the row segment is 256 B, 32-byte aligned): half as many
+                // scattered store transactions as 16-byte ones
+                __nv_bfloat16* dst = p.y + (size_t)pair * p.H + nb * 256 + 128 * half;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_global_v8(dst + 16 * c, *reinterpret_cast<const uint32_t(*)[8]>(P + 8 * c));
+            } else {
             uint32_t V[128];
-            if (p.mode == 0) {  // gate columns [64 half, +64) and up columns [128 + 64 half, +64)
+            {  // gate columns [64 half, +64) and up columns [128 + 64 half, +64)
 #pragma unroll
                 for (int c = 0; c < 64; c += 16) {
                     tmem_ld_16(trow + 64 * half + c, *reinterpret_cast<uint32_t(*)[16]>(V + c));
                     tmem_ld_16(trow + 128 + 64 * half + c, *reinterpret_cast<uint32_t(*)[16]>(V + 64 + c));
                 }
-            } else {            // output columns [128 half, +128)
-#pragma unroll
-                for (int c = 0; c < 128; c += 16)
-                    tmem_ld_16(trow + 128 * half + c, *reinterpret_cast<uint32_t(*)[16]>(V + c));
             }
             tmem_ld_wait();
             tc_fence_before();
@@ -557,7 +605,7 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
             const int prow = b * 128 + r;
             const int pair = p.padrow_pair[prow];
             if (pair < 0) continue;
-            if (p.mode == 0) {
+            {
                 const float pg = (sh ? p.spost0 : p.post0)[es];
                 const float pu = (sh ? p.spost1 : p.post1)[es];
 #pragma unroll
@@ -574,23 +622,7 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                                   sf_tile_offset(r, (i >> 4) & 3);
                     quant16_rcp(h, p.g2, p.hq + (size_t)prow * p.hq_row_bytes + i / 2, sf);
                 }
-            } else {
-                const float pd = (sh ? p.spost0 : p.post0)[es];
-                const float sc = pd * (pair < p.P ? p.topk_w[pair] : 1.f);
-                // 32-byte stores (the row segment is 256 B, 32-byte aligned): half as many
-                // scattered store transactions as 16-byte ones
-                __nv_bfloat16* dst = p.y + (size_t)pair * p.H + nb * 256 + 128 * half;
-#pragma unroll
-                for (int c = 0; c < 128; c += 16) {
-                    uint32_t ow[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(V[c + 2 * i]) * sc,
-                                                                 __uint_as_float(V[c + 2 * i + 1]) * sc);
-                        ow[i] = *reinterpret_cast<uint32_t*>(&v);
-                    }
-                    st_global_v8(dst + c, ow);
-                }
+            }
             }
         }
     }
@@ -807,9 +839,10 @@ cudaError_t tc_prepare(const FfnLaunch& L, TcWeights* tw, cudaStream_t st) {
         if (*b) cudaFree(*b);
         *b = nullptr;
     }
-    err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kTcSmemBytes);
-    if (err != cudaSuccess) return err;
+    for (auto kern : {tc_gemm_kernel<0>, tc_gemm_kernel<1>}) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+        if (err != cudaSuccess) return err;
+    }
     tw->ready = true;
     return cudaSuccess;
 }
@@ -1032,7 +1065,7 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
     g1.sfa = B.xsf; g1.sfa_kblocks = L.H / 64;
     g1.sfb0 = tw.sfp_gu; g1.ssfb0 = tw.sfp_sh_gu;  // quarter tiles of gate | up
     g1.post0 = tw.post_gate; g1.post1 = tw.post_up; g1.spost0 = tw.post_sh_gate; g1.spost1 = tw.post_sh_up;
-    TC_PHASE(1, (tc_gemm_kernel<<<sms, kTcThreads, kTcSmemBytes, st>>>(m1, g1)))
+    TC_PHASE(1, (tc_gemm_kernel<0><<<sms, kTcThreads, kTcSmemBytes, st>>>(m1, g1)))
 
     TcGemmParams g2 = g;
     g2.mode = 1;
@@ -1040,7 +1073,7 @@ cudaError_t launch_ffn_tc(const FfnLaunch& L, const TcWeights& tw, const TcBuffe
     g2.sfa = B.hsf; g2.sfa_kblocks = Imax / 64;
     g2.sfb0 = tw.sfp_dn; g2.ssfb0 = tw.sfp_sh_dn;  // quarter tiles of down
     g2.post0 = tw.post_down; g2.post1 = tw.post_down; g2.spost0 = tw.post_sh_down; g2.spost1 = tw.post_sh_down;
-    TC_PHASE(2, (tc_gemm_kernel<<<sms, kTcThreads, kTcSmemBytes, st>>>(m2, g2)))
+    TC_PHASE(2, (tc_gemm_kernel<1><<<sms, kTcThreads, kTcSmemBytes, st>>>(m2, g2)))
 
     TcCombineArgs ca{};
     ca.y = B.y; ca.ids = L.ids; ca.out = L.out; ca.T = L.T; ca.H = L.H; ca.k = L.k; ca.E = L.E;
