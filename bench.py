@@ -4,8 +4,9 @@ One step = one MoE layer forward (moe_forward: route + FFN) over one batch of T 
 tokens.  Steps cycle through L replicas of the layer's weights (distinct device copies, as the
 layers of a model would be) with L * touched-bytes >= 4 * L2, so every step streams its expert
 weights from HBM.  One CUDA graph holds one step of each replica in turn (as a serving engine
-captures the layers of a step in one graph) and is replayed; single-step graphs make up any
-remainder, so a timed region is exactly K steps, between a barrier + device synchronisation on
+captures the layers of a step in one graph), repeated to at least 4 steps, and is replayed;
+single-step graphs make up any remainder, so a timed region is exactly K steps, between a
+barrier + device synchronisation on
 both sides, timed with CUDA events on the launching stream, max over ranks.  When K steps take
 less than about a second the region is repeated (each repetition again exactly K steps) and the
 median region is reported, so that the clock sampler sees the load.
@@ -57,8 +58,8 @@ KERNEL_SOURCES = {
     "mma": ("ffn.cu", "frag.cuh", "quant.cuh", "common.cuh"),
 }
 TRAFFIC = {  # one-pass captures at full size (the commands are in the profile summaries)
-    "pre4096": (4733255424, "2c9a5ba3d8804c26"),
-    "pre32768": (5961782528, "2c9a5ba3d8804c26"),
+    "pre4096": (4742197248, "92f5b574e4dfe58d"),
+    "pre32768": (5962880512, "92f5b574e4dfe58d"),
     "dec1": (21881344, "047b93c02bb9da69"),
     "dec8": (1270784256, "047b93c02bb9da69"),
     "hash64": (584604672, "43b546cd6aeb1483"),
@@ -417,19 +418,23 @@ def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True, whole_cyc
             with torch.cuda.graph(g, stream=stream):
                 step(layer, b)
             graphs.append(g)
+        # one graph of whole passes over the replicas, at least 4 steps (fewer graph launches
+        # between steps; the steps and their order are the same)
+        cyc_len = replicas * max(1, -(-4 // replicas))
         cycle = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cycle, stream=stream):
-            for layer, b in zip(layers, bufs):
-                step(layer, b)
+            for _ in range(cyc_len // replicas):
+                for layer, b in zip(layers, bufs):
+                    step(layer, b)
     torch.cuda.synchronize()
 
     def run_steps(first, n):
         """Layer steps first .. first + n - 1 (replica i % replicas), as graph replays."""
         i = first
         while i < first + n:
-            if i % replicas == 0 and first + n - i >= replicas:
+            if i % replicas == 0 and first + n - i >= cyc_len:
                 cycle.replay()
-                i += replicas
+                i += cyc_len
             else:
                 graphs[i % replicas].replay()
                 i += 1
