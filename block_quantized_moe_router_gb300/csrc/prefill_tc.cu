@@ -529,21 +529,24 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
         const int r = quad * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t acc_phase = 0;
-        // down: this row's pair, N block and output scale, read one tile ahead (the scale is a
-        // dependent load, so it is not waited for between a tile's MMAs and the release of
-        // its accumulator)
-        int pair_n = -1, nb_n = 0;
-        float sc_n = 0.f;
+        // this row's pair, row block, N block and scales, read one tile ahead (dependent loads,
+        // so they are not waited for between a tile's MMAs and the release of its accumulator):
+        // gate+up the two post-scales, down the output scale (post-scale x routing weight)
+        int pair_n = -1, b_n = 0, nb_n = 0;
+        float s0_n = 0.f, s1_n = 0.f;
         auto row_scale = [&](int tile) {
             if (tile >= ntiles) return;
             const int4 tl = p.tiles[tile];
             const bool sh = tl.z == p.E;
+            const int es = sh ? 0 : tl.z;
             pair_n = p.padrow_pair[tl.x * 128 + r];
+            b_n = tl.x;
             nb_n = tl.y;
-            const float pd = (sh ? p.spost0 : p.post0)[sh ? 0 : tl.z];
-            sc_n = pair_n < 0 ? 0.f : pd * (pair_n < p.P ? p.topk_w[pair_n] : 1.f);
+            s0_n = (sh ? p.spost0 : p.post0)[es];
+            if (MODE == 0) s1_n = (sh ? p.spost1 : p.post1)[es];
+            else s0_n = pair_n < 0 ? 0.f : s0_n * (pair_n < p.P ? p.topk_w[pair_n] : 1.f);
         };
-        if (MODE == 1) row_scale(blockIdx.x);
+        row_scale(blockIdx.x);
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
             if (!mbar_wait_bounded(acc_full, acc_phase, kTcWaitLimit)) {
                 tc_abort(p, abort_flag);
@@ -555,7 +558,7 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                 // output columns [128 half, +128) in two halves, packed to bf16 as they arrive,
                 // so a thread holds 64 packed words instead of 128 accumulators
                 const int pair = pair_n, nb = nb_n;
-                const float sc = sc_n;
+                const float sc = s0_n;
                 uint32_t P[64];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -585,44 +588,44 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
                 for (int c = 0; c < 8; ++c)
                     st_global_v8(dst + 16 * c, *reinterpret_cast<const uint32_t(*)[8]>(P + 8 * c));
             } else {
-            uint32_t V[128];
-            {  // gate columns [64 half, +64) and up columns [128 + 64 half, +64)
+                // gate columns [64 half, +64) and up columns [128 + 64 half, +64), in two halves
+                // of 32 + 32: the first half's h is computed and requantized before the second
+                // half is read, so a thread holds 64 accumulators instead of 128
+                const int pair = pair_n, b = b_n, nb = nb_n;
+                const float pg = s0_n, pu = s1_n;
+                const int prow = b * 128 + r;
 #pragma unroll
-                for (int c = 0; c < 64; c += 16) {
-                    tmem_ld_16(trow + 64 * half + c, *reinterpret_cast<uint32_t(*)[16]>(V + c));
-                    tmem_ld_16(trow + 128 + 64 * half + c, *reinterpret_cast<uint32_t(*)[16]>(V + 64 + c));
-                }
-            }
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(acc_empty);
-            acc_phase ^= 1u;
-
-            const int4 tl = p.tiles[tile];
-            const int b = tl.x, nb = tl.y, e = tl.z;
-            const bool sh = e == p.E;
-            const int es = sh ? 0 : e;
-            const int prow = b * 128 + r;
-            const int pair = p.padrow_pair[prow];
-            if (pair < 0) continue;
-            {
-                const float pg = (sh ? p.spost0 : p.post0)[es];
-                const float pu = (sh ? p.spost1 : p.post1)[es];
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t Gw[32], Uw[32];
 #pragma unroll
-                for (int blk = 0; blk < 4; ++blk) {
-                    float h[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float gv = __uint_as_float(V[16 * blk + i]) * pg;
-                        const float uv = __uint_as_float(V[64 + 16 * blk + i]) * pu;
-                        h[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                    for (int c = 0; c < 32; c += 16) {
+                        tmem_ld_16(trow + 64 * half + 32 * hh + c, *reinterpret_cast<uint32_t(*)[16]>(Gw + c));
+                        tmem_ld_16(trow + 128 + 64 * half + 32 * hh + c, *reinterpret_cast<uint32_t(*)[16]>(Uw + c));
                     }
-                    const int i = nb * 128 + 64 * half + 16 * blk;
-                    uint8_t* sf = p.hsf + ((size_t)b * p.hsf_kblocks + (i >> 6)) * 512 +
-                                  sf_tile_offset(r, (i >> 4) & 3);
-                    quant16_rcp(h, p.g2, p.hq + (size_t)prow * p.hq_row_bytes + i / 2, sf);
+                    tmem_ld_wait();
+                    if (hh == 1) {
+                        tc_fence_before();
+                        mbar_arrive(acc_empty);
+                    }
+                    if (pair >= 0) {
+#pragma unroll
+                        for (int blk = 0; blk < 2; ++blk) {
+                            float h[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float gv = __uint_as_float(Gw[16 * blk + i]) * pg;
+                                const float uv = __uint_as_float(Uw[16 * blk + i]) * pu;
+                                h[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                            }
+                            const int i = nb * 128 + 64 * half + 32 * hh + 16 * blk;
+                            uint8_t* sf = p.hsf + ((size_t)b * p.hsf_kblocks + (i >> 6)) * 512 +
+                                          sf_tile_offset(r, (i >> 4) & 3);
+                            quant16_rcp(h, p.g2, p.hq + (size_t)prow * p.hq_row_bytes + i / 2, sf);
+                        }
+                    }
                 }
-            }
+                acc_phase ^= 1u;
+                row_scale(tile + gridDim.x);
             }
         }
     }
