@@ -77,11 +77,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
-// 32-byte global store (address 32-byte aligned).
-__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&w)[8]) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
-                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
+// 32-byte global store (address 32-byte aligned) under an L2 cache policy, not allocated in L1.
+__device__ __forceinline__ void st_global_v8_hint(void* dst, const uint32_t (&w)[8], uint64_t pol) {
+    asm volatile(
+        "st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(dst),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "l"(pol)
+        : "memory");
+}
+// L2 policy: evict these lines first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 // ---- tcgen05 --------------------------------------------------------------------------------
