@@ -521,9 +521,9 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
         }
     } else {
         // ---------------- epilogue (warps 2..9) ----------------
-        // Two warps per TMEM lane quarter, each owning half of the tile's columns: a warp copies
-        // its whole slice (128 columns) into registers and releases the accumulator at once, so
-        // the next tile's MMAs run while it computes and stores.
+        // Two warps per TMEM lane quarter, each owning half of the tile's columns (128): a warp
+        // reads its slice in two halves and releases the accumulator once the second half is
+        // in registers, so the next tile's MMAs run while it finishes computing and storing.
         const int quad = warp & 3;
         const int half = (warp - 2) >> 2;
         const int r = quad * 32 + lane;
@@ -547,7 +547,7 @@ tc_gemm_kernel(const __grid_constant__ TcTensorMaps maps, const TcGemmParams p) 
             else s0_n = pair_n < 0 ? 0.f : s0_n * (pair_n < p.P ? p.topk_w[pair_n] : 1.f);
         };
         row_scale(blockIdx.x);
-        const uint64_t ypol = l2_policy_evict_first();  // down: the pair rows
+        const uint64_t ypol = MODE == 1 ? l2_policy_evict_first() : 0ull;  // down: the pair rows
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
             if (!mbar_wait_bounded(acc_full, acc_phase, kTcWaitLimit)) {
                 tc_abort(p, abort_flag);
