@@ -137,14 +137,33 @@ FULL = {
     "dec8": S.CONFIGS["dec8"],
     "hash64": S.CONFIGS["hash64"],
     "pre4096": S.CONFIGS["pre4096"],
+    "pre32768": S.CONFIGS["pre32768"],
 }
+
+
+def last_tokens(ids, E, head=16, extra=(0, 1)):
+    """For the largest prefill: the last token of every routed expert (its ragged last 128-row
+    block), the first token of the `head` experts with the most tokens, and the `extra` tokens.
+    Sorted, unique."""
+    pick = set(int(t) for t in extra)
+    counts = np.array([(ids == e).any(1).sum() for e in range(E)])
+    for e in range(E):
+        toks = np.nonzero((ids == e).any(1))[0]
+        if len(toks):
+            pick.add(int(toks[-1]))
+    for e in np.argsort(-counts)[:head]:
+        toks = np.nonzero((ids == e).any(1))[0]
+        if len(toks):
+            pick.add(int(toks[0]))
+    return sorted(pick)
 
 
 @pytest.mark.parametrize("name", list(FULL))
 def test_full_size_configs(cuda_lib, name):
-    """Full-size workloads: every token for the decode and hash workloads; for the prefill
-    workload the first and last token of every routed expert (a few hundred tokens) plus
-    tokens spread over the Zipf head's rows; all rows finite and nonzero."""
+    """Full-size workloads: every token for the decode and hash workloads; for the 4096-token
+    prefill the first and last token of every routed expert (a few hundred tokens) plus tokens
+    spread over the Zipf head's rows; for the 32768-token prefill the last token of every routed
+    expert and the first of the largest ones; all rows finite and nonzero."""
     cfg = FULL[name]
     inp, _ = parity.make_case(cfg, seed=0, device="cuda")
     ref_r = parity.oracle_route(cfg, inp)
@@ -152,7 +171,11 @@ def test_full_size_configs(cuda_lib, name):
     assert status == 0
     parity.assert_routing(cfg, ref_r, ids, w, gpu_logits=logits, inp=inp)
     sample = None
-    if cfg.T > 64:
+    if cfg.T > 8192:
+        sample = last_tokens(ref_r["ids"], cfg.E, extra=(0, 1, cfg.T - 1))
+        routed = set(int(e) for e in np.unique(ref_r["ids"]) if 0 <= e < cfg.E)
+        assert routed <= set(int(e) for e in np.unique(ref_r["ids"][sample]))  # every expert
+    elif cfg.T > 64:
         sample = covering_tokens(ref_r["ids"], cfg.E, per_expert=6, extra=(0, 1, cfg.T - 1))
         assert len(sample) >= cfg.E  # (a few hundred tokens at 4096)
     ref = parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"], tokens=sample)
