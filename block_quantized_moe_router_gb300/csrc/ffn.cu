@@ -137,31 +137,43 @@ constexpr int kErBOff = kErWarps * kErWarpBytes;
 constexpr int kErStageBytes = kErBOff + kErNT * 2048;
 constexpr int kErSmemBytes = kErStages * kErStageBytes;
 
-// Work item it = (slot, 64-row block): its expert, tokens and matrix shape, or invalid.
+// Work items: (routed slot, 64-row block) for the routed experts, slot-major; then, for the
+// shared expert, which takes every token, (64-row block, 8-token tile) with the tiles of one
+// row block adjacent.  Every item then carries at most 8 tokens of rows, so the items cost
+// about the same and the CTAs, which take items strided by the grid, finish together; the
+// shared expert's weight rows are read by the few CTAs running its adjacent items at the same
+// time (L2 hits after the first).  A shared expert taken as whole-row-block items with all its
+// tokens made those items several times heavier than the rest and left a tail.
 struct ErItem {
     bool valid, shared;
     int e, row0, cnt, N, K;
+    int xb, tb;  // 64-row block; first token of the item (shared expert)
 };
 template <int MODE>
 __device__ __forceinline__ ErItem er_item(const FfnLaunch& L, int max_routed_slots, int xblocks,
                                           int it) {
     ErItem w{};
-    const int slot = it / xblocks, xb = it - slot * xblocks;
-    w.shared = slot == max_routed_slots;
-    if (w.shared) {
-        w.e = 0;
-        w.row0 = 0;
-        w.cnt = L.T;
-    } else {
+    const int routed_items = max_routed_slots * xblocks;
+    if (it < routed_items) {
+        const int slot = it / xblocks;
+        w.xb = it - slot * xblocks;
         if (slot >= L.meta[0]) return w;
         w.e = L.active[slot];
         w.row0 = L.offsets[w.e];
         w.cnt = L.offsets[w.e + 1] - w.row0;
+    } else {
+        const int tiles = (L.T + 7) / 8, j = it - routed_items;
+        w.shared = true;
+        w.xb = j / tiles;
+        w.tb = (j - w.xb * tiles) * 8;
+        w.e = 0;
+        w.row0 = 0;
+        w.cnt = min(8, L.T - w.tb);
     }
     const int Iexp = w.shared ? L.I_shared : L.I;
     w.N = MODE == MODE_GATEUP ? Iexp : L.H;
     w.K = MODE == MODE_GATEUP ? L.H : Iexp;
-    w.valid = xb * kErWarps * 16 < w.N && w.cnt > 0;
+    w.valid = w.xb * kErWarps * 16 < w.N && w.cnt > 0;
     return w;
 }
 
@@ -180,10 +192,10 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
     auto b_src = [&](const ErItem& w, int col) -> const __half* {  // column col, K-step 0
         if (col >= w.cnt) return nullptr;
         if (MODE == MODE_GATEUP) {
-            const int tok = w.shared ? col : L.sorted_pair[w.row0 + col] / L.k;
+            const int tok = w.shared ? w.tb + col : L.sorted_pair[w.row0 + col] / L.k;
             return L.x16 + (size_t)tok * L.H + 32 * bq + 8 * bc;
         }
-        const int r = w.shared ? P + col : w.row0 + col;
+        const int r = w.shared ? P + w.tb + col : w.row0 + col;
         return L.h16 + (size_t)r * Imax + 32 * bq + 8 * bc;
     };
 
@@ -213,9 +225,10 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
         c_sfb = 128 / sv;
         c_steps = cw.K / 128;
         c_passes = (cw.cnt + 8 * NT - 1) / (8 * NT);
-        c_pol = c_passes > 1 ? pol_again : pol_once;
+        // the shared expert's rows are read by the items of all its token tiles
+        c_pol = (c_passes > 1 || cw.shared) ? pol_again : pol_once;
         c_rstride = (size_t)8 * (cw.K / 2);
-        const int xb = ci % xblocks;
+        const int xb = cw.xb;
         const int n0 = (xb * kErWarps + warp) * 16;
         const bool rows_ok = n0 < cw.N;
         const ProjView& PA = MODE == MODE_GATEUP ? (cw.shared ? L.sh_gate : L.gate)
@@ -275,8 +288,8 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
         const ErItem w = er_item<MODE>(L, max_routed_slots, xblocks, it);
         if (!w.valid) continue;  // CTA-uniform
         const bool shared = w.shared;
-        const int e = w.e, row0 = w.row0, cnt = w.cnt, N = w.N, K = w.K;
-        const int n0 = ((it % xblocks) * kErWarps + warp) * 16;
+        const int e = w.e, row0 = w.row0, cnt = w.cnt, N = w.N, K = w.K, tb = w.tb;
+        const int n0 = (w.xb * kErWarps + warp) * 16;
         const bool rows_ok = n0 < N;
         const int steps = K / 128;
         auto body = [&](auto fmt_c) {
@@ -352,7 +365,7 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
                     for (int j = 0; j < 2; ++j) {
                         const int col = c0 + nt * 8 + 2 * q + j;
                         const bool valid = col < cnt;
-                        const int r = shared ? P + col : row0 + col;
+                        const int r = shared ? P + tb + col : row0 + col;
                         if (MODE == MODE_GATEUP) {
                             const float h0 = silu_f32(accA[nt][j] * postA) * (accB[nt][j] * postB);
                             const float h1 = silu_f32(accA[nt][2 + j] * postA) * (accB[nt][2 + j] * postB);
@@ -496,7 +509,6 @@ cudaError_t record_phase_event(cudaEvent_t ev, cudaStream_t st) {
 
 template <int MODE, int FR, int FS>
 static cudaError_t launch_expert_gemm(const FfnLaunch& L, int slots_r, cudaStream_t st) {
-    const int slots = slots_r + (L.I_shared > 0 ? 1 : 0);
     const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
     const int N = MODE == MODE_GATEUP ? Imax : L.H;
     auto kern = expert_mma_kernel<MODE, FR, FS>;
@@ -507,10 +519,11 @@ static cudaError_t launch_expert_gemm(const FfnLaunch& L, int slots_r, cudaStrea
         return err;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-    // persistent CTAs: work items (slot, 64-row block) strided by the grid, slot-major so that
-    // concurrently running CTAs read neighbouring rows of one expert
+    // persistent CTAs: work items strided by the grid (er_item): routed (slot, 64-row block),
+    // slot-major so that concurrently running CTAs read neighbouring rows of one expert, then
+    // the shared expert's (64-row block, 8-token tile)
     const int xblocks = (N / 16 + kErWarps - 1) / kErWarps;
-    const int items = xblocks * slots;
+    const int items = xblocks * slots_r + (L.I_shared > 0 ? xblocks * ((L.T + 7) / 8) : 0);
     int grid = (per_sm > 0 ? per_sm : 1) * sms;
     if (grid > items) grid = items;
     kern<<<grid, kErWarps * 32, kErSmemBytes, st>>>(L, slots_r, xblocks, items);
