@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(512) prep_kernel(FfnLaunch L) {
 // Grouped expert GEMM on m16n8k16 f16 MMAs.
 //
 // A CTA of kErWarps warps owns 16 * kErWarps rows of one expert's projection (16 per warp)
-// over the whole K, and the expert's tokens in passes of up to NT MMA column tiles of 8.  The
+// over the whole K, and the expert's tokens in passes of up to NT = 2 MMA column tiles of 8;
+// each dequantized A fragment serves every column tile of the pass.  The
 // operands stream through a CTA ring of kErStages shared-memory stages filled by cp.async,
 // kErStages - 1 K-steps ahead of the MMAs (one flat sequence over all passes): every warp
 // copies its own weight rows, and the token chunks, the same for all warps, are copied once
@@ -131,19 +132,20 @@ __global__ void __launch_bounds__(512) prep_kernel(FfnLaunch L) {
 // ------------------------------------------------------------------------------------------
 constexpr int kErWarps = 4;
 constexpr int kErStages = 3;
-constexpr int kErNT = 4;
+constexpr int kErNT = 2;
 constexpr int kErWarpBytes = 2304;
 constexpr int kErBOff = kErWarps * kErWarpBytes;
 constexpr int kErStageBytes = kErBOff + kErNT * 2048;
 constexpr int kErSmemBytes = kErStages * kErStageBytes;
 
 // Work items: (routed slot, 64-row block) for the routed experts, slot-major; then, for the
-// shared expert, which takes every token, (64-row block, 8-token tile) with the tiles of one
-// row block adjacent.  Every item then carries at most 8 tokens of rows, so the items cost
-// about the same and the CTAs, which take items strided by the grid, finish together; the
-// shared expert's weight rows are read by the few CTAs running its adjacent items at the same
-// time (L2 hits after the first).  A shared expert taken as whole-row-block items with all its
-// tokens made those items several times heavier than the rest and left a tail.
+// shared expert, which takes every token, (64-row block, 16-token tile: one pass of the NT = 2
+// MMA column tiles) with the tiles of one row block adjacent.  The shared expert's items then
+// cost about as much as a routed item with its few tokens, so the CTAs, which take items
+// strided by the grid, finish together; its weight rows are read by the few CTAs running its
+// adjacent items at the same time (L2 hits after the first).  A shared expert taken as
+// whole-row-block items with all its tokens made those items several times heavier than the
+// rest and left a tail.
 struct ErItem {
     bool valid, shared;
     int e, row0, cnt, N, K;
@@ -162,13 +164,13 @@ __device__ __forceinline__ ErItem er_item(const FfnLaunch& L, int max_routed_slo
         w.row0 = L.offsets[w.e];
         w.cnt = L.offsets[w.e + 1] - w.row0;
     } else {
-        const int tiles = (L.T + 7) / 8, j = it - routed_items;
+        const int tiles = (L.T + 8 * kErNT - 1) / (8 * kErNT), j = it - routed_items;
         w.shared = true;
         w.xb = j / tiles;
-        w.tb = (j - w.xb * tiles) * 8;
+        w.tb = (j - w.xb * tiles) * 8 * kErNT;
         w.e = 0;
         w.row0 = 0;
-        w.cnt = min(8, L.T - w.tb);
+        w.cnt = min(8 * kErNT, L.T - w.tb);
     }
     const int Iexp = w.shared ? L.I_shared : L.I;
     w.N = MODE == MODE_GATEUP ? Iexp : L.H;
@@ -328,25 +330,31 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
                         scales_from_raw<FMT>(sc[g * 4 + 2], q, mxb, cb.s0lo, cb.s0hi);
                         scales_from_raw<FMT>(sc[g * 4 + 3], q, mxb, cb.s1lo, cb.s1hi);
                     }
+                    if (rows_ok) {
+                        // the column tiles of this pass that hold tokens (warp-uniform); each A
+                        // fragment is dequantized once and used for all of them
+                        const int ntv = min(NT, (cnt - c0 + 7) / 8);
+                        uint4 b[NT][4];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (!rows_ok || c0 + nt * 8 >= cnt) break;  // warp-uniform
-                        uint4 b[4];
+                        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            b[j] = bval[nt] ? *reinterpret_cast<const uint4*>(st + kErBOff + nt * 2048 + j * 512 + lane * 16)
-                                            : make_uint4(0, 0, 0, 0);
+                            for (int j = 0; j < 4; ++j)
+                                b[nt][j] = (nt < ntv && bval[nt])
+                                               ? *reinterpret_cast<const uint4*>(st + kErBOff + nt * 2048 + j * 512 + lane * 16)
+                                               : make_uint4(0, 0, 0, 0);
 #define MOE_STEP(I)                                                                   \
             {                                                                                 \
-                uint32_t fa[4];                                                               \
+                uint32_t fa[4], fb[4];                                                        \
                 frag_a<I>(ca, fa);                                                            \
-                const uint32_t b0 = word_of(b[I >> 1], (I & 1) * 2);                          \
-                const uint32_t b1 = word_of(b[I >> 1], (I & 1) * 2 + 1);                      \
-                mma_f16_16816(accA[nt], fa[0], fa[1], fa[2], fa[3], b0, b1);                  \
-                if (MODE == MODE_GATEUP) {                                                    \
-                    uint32_t fb[4];                                                           \
-                    frag_a<I>(cb, fb);                                                        \
-                    mma_f16_16816(accB[nt], fb[0], fb[1], fb[2], fb[3], b0, b1);              \
+                if (MODE == MODE_GATEUP) frag_a<I>(cb, fb);                                   \
+                _Pragma("unroll") for (int nt = 0; nt < NT; ++nt) {                           \
+                    if (nt < ntv) {                                                           \
+                        const uint32_t b0 = word_of(b[nt][I >> 1], (I & 1) * 2);              \
+                        const uint32_t b1 = word_of(b[nt][I >> 1], (I & 1) * 2 + 1);          \
+                        mma_f16_16816(accA[nt], fa[0], fa[1], fa[2], fa[3], b0, b1);          \
+                        if (MODE == MODE_GATEUP)                                              \
+                            mma_f16_16816(accB[nt], fb[0], fb[1], fb[2], fb[3], b0, b1);      \
+                    }                                                                         \
                 }                                                                             \
             }
                         MOE_STEP(0) MOE_STEP(1) MOE_STEP(2) MOE_STEP(3)
@@ -521,9 +529,9 @@ static cudaError_t launch_expert_gemm(const FfnLaunch& L, int slots_r, cudaStrea
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
     // persistent CTAs: work items strided by the grid (er_item): routed (slot, 64-row block),
     // slot-major so that concurrently running CTAs read neighbouring rows of one expert, then
-    // the shared expert's (64-row block, 8-token tile)
+    // the shared expert's (64-row block, 16-token tile)
     const int xblocks = (N / 16 + kErWarps - 1) / kErWarps;
-    const int items = xblocks * slots_r + (L.I_shared > 0 ? xblocks * ((L.T + 7) / 8) : 0);
+    const int items = xblocks * slots_r + (L.I_shared > 0 ? xblocks * ((L.T + 8 * kErNT - 1) / (8 * kErNT)) : 0);
     int grid = (per_sm > 0 ? per_sm : 1) * sms;
     if (grid > items) grid = items;
     kern<<<grid, kErWarps * 32, kErSmemBytes, st>>>(L, slots_r, xblocks, items);
