@@ -116,8 +116,9 @@ __global__ void __launch_bounds__(512) prep_kernel(FfnLaunch L) {
 // ------------------------------------------------------------------------------------------
 // Grouped expert GEMM on m16n8k16 f16 MMAs.
 //
-// A CTA of kErWarps warps owns 16 * kErWarps rows of one expert's projection (16 per warp)
-// over the whole K, and the expert's tokens in passes of up to NT = 2 MMA column tiles of 8;
+// A CTA of kErWarps warps owns rows of one expert's projection over the whole K -- gate+up:
+// 16 rows of gate and the same 16 of up per warp; down: two 16-row tiles per warp, as matrices
+// A and B -- and the expert's tokens in passes of up to NT = 2 MMA column tiles of 8;
 // each dequantized A fragment serves every column tile of the pass.  The
 // operands stream through a CTA ring of kErStages shared-memory stages filled by cp.async,
 // kErStages - 1 K-steps ahead of the MMAs (one flat sequence over all passes): every warp
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(512) prep_kernel(FfnLaunch L) {
 // by the whole CTA.  One CTA barrier per K-step both publishes a stage and frees the one the
 // next copies refill.  Stage layout (512 B = 32 lanes x 16 B; MMA row g = lane / 4):
 //   per warp w at w * kErWarpBytes: [0, 1024) codes of matrix A (rows g, g + 8),
-//     [1024, 2048) codes of matrix B (gate+up), [2048, 2304) block scales (lane (g, q) stages
+//     [1024, 2048) codes of matrix B (up, or down's second tile), [2048, 2304) block scales (lane (g, q) stages
 //     row g + 8 (q & 1) of matrix q >> 1);
 //   token chunks at kErBOff: tile t at t * 2048, 16 B per (8-element group c, column j, q) at
 //     c * 512 + (4 j + q) * 16.
@@ -175,7 +176,7 @@ __device__ __forceinline__ ErItem er_item(const FfnLaunch& L, int max_routed_slo
     const int Iexp = w.shared ? L.I_shared : L.I;
     w.N = MODE == MODE_GATEUP ? Iexp : L.H;
     w.K = MODE == MODE_GATEUP ? L.H : Iexp;
-    w.valid = w.xb * kErWarps * 16 < w.N && w.cnt > 0;
+    w.valid = w.xb * kErWarps * 16 * (MODE == MODE_GATEUP ? 1 : 2) < w.N && w.cnt > 0;
     return w;
 }
 
@@ -184,6 +185,8 @@ __global__ void __launch_bounds__(kErWarps * 32)
 expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
     extern __shared__ __align__(16) uint8_t er_smem[];
     constexpr int NT = kErNT;
+    // rows per warp: gate+up 16 of gate and 16 of up; down two 16-row tiles (matrices A and B)
+    constexpr int kErRowsW = MODE == MODE_GATEUP ? 16 : 32;
     uint8_t* ring = er_smem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
     const int Imax = L.I > L.I_shared ? L.I : L.I_shared;
@@ -231,17 +234,22 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
         c_pol = (c_passes > 1 || cw.shared) ? pol_again : pol_once;
         c_rstride = (size_t)8 * (cw.K / 2);
         const int xb = cw.xb;
-        const int n0 = (xb * kErWarps + warp) * 16;
+        const int n0 = (xb * kErWarps + warp) * kErRowsW;
         const bool rows_ok = n0 < cw.N;
         const ProjView& PA = MODE == MODE_GATEUP ? (cw.shared ? L.sh_gate : L.gate)
                                                  : (cw.shared ? L.sh_down : L.down);
         const ProjView& PB = cw.shared ? L.sh_up : L.up;
         const size_t rowA = (size_t)cw.e * cw.N + n0 + g;
         pa = rows_ok ? PA.packed + rowA * (cw.K / 2) + 16 * q : nullptr;
-        pb = (rows_ok && MODE == MODE_GATEUP) ? PB.packed + rowA * (cw.K / 2) + 16 * q : nullptr;
-        const ProjView& PS = (q >> 1) ? PB : PA;  // row g + 8 (q & 1) of matrix q >> 1
-        ps = (rows_ok && (MODE == MODE_GATEUP || q < 2))
-                 ? PS.scales + (rowA + 8 * (q & 1)) * (size_t)(cw.K / sv) : nullptr;
+        // matrix B: up (gate+up), or the warp's second 16-row tile of down
+        const bool rows2 = MODE == MODE_GATEUP ? rows_ok : n0 + 16 < cw.N;
+        const size_t rowB = MODE == MODE_GATEUP ? rowA : rowA + 16;
+        pb = rows2 ? (MODE == MODE_GATEUP ? PB : PA).packed + rowB * (cw.K / 2) + 16 * q : nullptr;
+        // lane (g, q) stages the scales of row g + 8 (q & 1) of matrix q >> 1
+        ps = ((q >> 1) ? rows2 : rows_ok)
+                 ? ((q >> 1) && MODE == MODE_GATEUP ? PB : PA).scales +
+                       ((q >> 1) ? rowB : rowA) * (size_t)(cw.K / sv) + 8 * (q & 1) * (size_t)(cw.K / sv)
+                 : nullptr;
         ip = 0;
         is = 0;
         enter_pass();
@@ -291,7 +299,7 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
         if (!w.valid) continue;  // CTA-uniform
         const bool shared = w.shared;
         const int e = w.e, row0 = w.row0, cnt = w.cnt, N = w.N, K = w.K, tb = w.tb;
-        const int n0 = (w.xb * kErWarps + warp) * 16;
+        const int n0 = (w.xb * kErWarps + warp) * kErRowsW;
         const bool rows_ok = n0 < N;
         const int steps = K / 128;
         auto body = [&](auto fmt_c) {
@@ -300,7 +308,7 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
                                                      : (shared ? L.sh_down : L.down);
             const ProjView& PB = shared ? L.sh_up : L.up;
             const int mxa = (FMT == MOE_FMT_MXFP4) ? 112 + PA.mx_off[e] : 0;
-            const int mxb = (FMT == MOE_FMT_MXFP4 && MODE == MODE_GATEUP) ? 112 + PB.mx_off[e] : 0;
+            const int mxb = FMT != MOE_FMT_MXFP4 ? 0 : MODE == MODE_GATEUP ? 112 + PB.mx_off[e] : mxa;
             const float postA = PA.post[e];
             const float postB = (MODE == MODE_GATEUP) ? PB.post[e] : 1.f;
             for (int c0 = 0; c0 < cnt; c0 += 8 * NT) {
@@ -324,7 +332,7 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
                     ca.r1 = *reinterpret_cast<const uint4*>(sw + 512 + lane * 16);
                     scales_from_raw<FMT>(sc[g * 4 + 0], q, mxa, ca.s0lo, ca.s0hi);
                     scales_from_raw<FMT>(sc[g * 4 + 1], q, mxa, ca.s1lo, ca.s1hi);
-                    if (MODE == MODE_GATEUP) {
+                    {   // matrix B: up, or down's second 16-row tile
                         cb.r0 = *reinterpret_cast<const uint4*>(sw + 1024 + lane * 16);
                         cb.r1 = *reinterpret_cast<const uint4*>(sw + 1536 + lane * 16);
                         scales_from_raw<FMT>(sc[g * 4 + 2], q, mxb, cb.s0lo, cb.s0hi);
@@ -346,14 +354,13 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
             {                                                                                 \
                 uint32_t fa[4], fb[4];                                                        \
                 frag_a<I>(ca, fa);                                                            \
-                if (MODE == MODE_GATEUP) frag_a<I>(cb, fb);                                   \
+                frag_a<I>(cb, fb);                                                            \
                 _Pragma("unroll") for (int nt = 0; nt < NT; ++nt) {                           \
                     if (nt < ntv) {                                                           \
                         const uint32_t b0 = word_of(b[nt][I >> 1], (I & 1) * 2);              \
                         const uint32_t b1 = word_of(b[nt][I >> 1], (I & 1) * 2 + 1);          \
                         mma_f16_16816(accA[nt], fa[0], fa[1], fa[2], fa[3], b0, b1);          \
-                        if (MODE == MODE_GATEUP)                                              \
-                            mma_f16_16816(accB[nt], fb[0], fb[1], fb[2], fb[3], b0, b1);      \
+                        mma_f16_16816(accB[nt], fb[0], fb[1], fb[2], fb[3], b0, b1);          \
                     }                                                                         \
                 }                                                                             \
             }
@@ -415,6 +422,10 @@ expert_mma_kernel(FfnLaunch L, int max_routed_slots, int xblocks, int items) {
                             float* yrow = L.y + (size_t)r * L.H + n0;
                             yrow[g] = accA[nt][j] * postA * wcol;
                             yrow[g + 8] = accA[nt][2 + j] * postA * wcol;
+                            if (n0 + 16 < N) {  // the second 16-row tile
+                                yrow[16 + g] = accB[nt][j] * postA * wcol;
+                                yrow[24 + g] = accB[nt][2 + j] * postA * wcol;
+                            }
                         }
                     }
                 }
@@ -530,7 +541,8 @@ static cudaError_t launch_expert_gemm(const FfnLaunch& L, int slots_r, cudaStrea
     // persistent CTAs: work items strided by the grid (er_item): routed (slot, 64-row block),
     // slot-major so that concurrently running CTAs read neighbouring rows of one expert, then
     // the shared expert's (64-row block, 16-token tile)
-    const int xblocks = (N / 16 + kErWarps - 1) / kErWarps;
+    const int rows_item = kErWarps * (MODE == MODE_GATEUP ? 16 : 32);  // down: two 16-row tiles a warp
+    const int xblocks = (N + rows_item - 1) / rows_item;
     const int items = xblocks * slots_r + (L.I_shared > 0 ? xblocks * ((L.T + 8 * kErNT - 1) / (8 * kErNT)) : 0);
     int grid = (per_sm > 0 ? per_sm : 1) * sms;
     if (grid > items) grid = items;
