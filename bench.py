@@ -62,7 +62,7 @@ TRAFFIC = {  # one-pass captures at full size (the commands are in the profile s
     "pre32768": (5843203328, "c7d739501b55265b"),
     "dec1": (21881344, "047b93c02bb9da69"),
     "dec8": (1270784256, "047b93c02bb9da69"),
-    "hash64": (585669376, "eb1df76d55722d8e"),
+    "hash64": (585473024, "072a5ab91b57aa02"),
 }
 
 
