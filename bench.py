@@ -503,14 +503,18 @@ def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True, whole_cyc
 
     # end to end through the public API with host buffers: every step copies its x (and token
     # ids) in from pinned host memory, runs route + FFN, and copies its output back to pinned
-    # host memory, and the host sees every step's output.  Two loops are timed and the faster
-    # one reported (both figures are in the line):
+    # host memory, and the host sees every step's output.  Three loops are timed and the
+    # fastest one reported (every figure is in the line):
     #   serial  -- one stream, each step one CUDA graph (copies + route + FFN), the host waiting
     #              for every step's output before the next;
     #   overlap -- the layer steps run one after another on one compute stream (each a CUDA
     #              graph of route + FFN), the copies on their own in / out streams with two
     #              buffer slots, so step i's copies overlap the compute of steps i - 1 and
-    #              i + 1; before issuing step i the host waits for step i - 2's output.
+    #              i + 1; before issuing step i the host waits for step i - 2's output;
+    #   host    -- the library's host-buffer entry point (moe_forward_host: copy in, route +
+    #              FFN, copy out, enqueued by the library on one stream) called once per step
+    #              with two pinned buffer slots in turn; the host waits for step i - 2's
+    #              output before reusing its slot.
     nsl = 2
     x_host = [inp["x"].pin_memory() for _ in range(nsl)]
     out_host = [torch.empty((T, cfg.H), dtype=torch.bfloat16).pin_memory() for _ in range(nsl)]
@@ -601,10 +605,29 @@ def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True, whole_cyc
         for ev in ev_out:
             ev.synchronize()
         e2e_runs["overlap"] = (time.perf_counter() - t0) / e2e_steps
+        # host: moe_forward_host per step, on `stream`
+        ev_h = [torch.cuda.Event() for _ in range(nsl)]
+        for i in range(e2e_steps + args.warmup):
+            s, r = i % nsl, i % replicas
+            if i == args.warmup:
+                barrier()
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            if i >= nsl:
+                ev_h[s].synchronize()         # step i - 2's output is in out_host[s]
+            layers[r].forward_host(x_host[s], out_host[s],
+                                   token_ids_host=None if tok_host is None else tok_host[s],
+                                   stream=stream)
+            ev_h[s].record(stream)
+        for ev in ev_h:
+            ev.synchronize()
+        e2e_runs["host"] = (time.perf_counter() - t0) / e2e_steps
+        last = e2e_steps + args.warmup - 1
+        host_ok = bool(torch.equal(out_host[last % nsl], bufs[0]["out"].cpu()))
         e2e_mode = min(e2e_runs, key=e2e_runs.get)
         e2e_s = e2e_runs[e2e_mode]
     else:
-        e2e_s, e2e_mode = float("nan"), None
+        e2e_s, e2e_mode, host_ok = float("nan"), None, None
     e2e_s = max_over_ranks([e2e_s], dist, device="cuda")[0]
     e2e_runs = {k: max_over_ranks([v], dist, device="cuda")[0] for k, v in e2e_runs.items()}
     h2d = T * cfg.H * 2 + (T * 4 if tok is not None else 0)
@@ -665,10 +688,13 @@ def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True, whole_cyc
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "mode": e2e_mode,
                     "ms_per_step": e2e_s * 1e3,
                     "loops_ms_per_step": {k: v * 1e3 for k, v in e2e_runs.items()},
+                    "host_entry_output_equal": host_ok,
                     "loops": "serial: one graph per step (copies + route + FFN), host waits "
                              "for each step; overlap: steps one after another on one compute "
                              "stream, copies on in/out streams with two buffer slots, host "
-                             "waits for step i - 2"},
+                             "waits for step i - 2; host: moe_forward_host (the library's "
+                             "host-buffer entry: copies and launches issued in C) per step, "
+                             "two pinned slots, host waits for step i - 2"},
             "replica_outputs_equal": ok,
             "kernel_source": src,
         }

@@ -25,7 +25,8 @@ MOE_ACT_BF16, MOE_ACT_NVFP4 = 0, 1
 
 # Every symbol include/moe.h declares.
 EXPORTED = ["moe_route", "moe_workspace_size", "moe_prepare_weights", "moe_release_weights",
-            "moe_ffn_forward", "moe_forward", "moe_ffn_forward_noalloc", "moe_quantize_act_nvfp4",
+            "moe_ffn_forward", "moe_forward", "moe_workspace_size_host", "moe_forward_host",
+            "moe_ffn_forward_noalloc", "moe_quantize_act_nvfp4",
             "moe_set_wait_limit", "moe_skew_barrier", "moe_profile_enable", "moe_profile_read",
             "moe_status_string"]
 
@@ -85,6 +86,11 @@ def load_library(path: str = LIB_PATH):
     lib.moe_forward.argtypes = [vp, ctypes.POINTER(moe_route_desc), i32, f32, f32, vp, vp, vp, vp,
                                 vp, vp, vp, sz, vp, vp]
     lib.moe_forward.restype = ctypes.c_int
+    lib.moe_workspace_size_host.argtypes = [ctypes.POINTER(moe_ffn_desc), i32, i32, ctypes.POINTER(sz)]
+    lib.moe_workspace_size_host.restype = ctypes.c_int
+    lib.moe_forward_host.argtypes = [vp, ctypes.POINTER(moe_route_desc), i32, f32, f32, vp, vp, vp,
+                                     vp, vp, vp, sz, vp, vp]
+    lib.moe_forward_host.restype = ctypes.c_int
     lib.moe_ffn_forward_noalloc.argtypes = [vp, i32, i32, f32, f32, vp, vp, vp, vp, vp, vp]
     lib.moe_ffn_forward_noalloc.restype = ctypes.c_int
     lib.moe_quantize_act_nvfp4.argtypes = [vp, i64, i64, f32, vp, vp, vp]
@@ -116,6 +122,18 @@ def _dptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _hptr(t: Optional[torch.Tensor], dtype, name="tensor"):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
         raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -209,6 +227,28 @@ def moe_forward(handle: int, route: moe_route_desc, act: int, g_act1: float, g_a
         _dptr(workspace, torch.uint8, "workspace"), workspace.numel(),
         _dptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check(st, "moe_forward")
+
+
+def moe_workspace_size_host(desc: moe_ffn_desc, T: int, act: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().moe_workspace_size_host(ctypes.byref(desc), int(T), int(act),
+                                                  ctypes.byref(n)), "moe_workspace_size_host")
+    return int(n.value)
+
+
+def moe_forward_host(handle: int, route: moe_route_desc, act: int, g_act1: float, g_act2: float,
+                     x_host, out_host, workspace, token_ids_host=None, topk_ids_host=None,
+                     topk_w_host=None, dev_status=None, stream=None):
+    """moe_forward on host buffers (CPU tensors, pinned for asynchronous copies): the copies in
+    and out are enqueued on the stream with the forward; synchronise before reading out_host."""
+    st = load_library().moe_forward_host(
+        ctypes.c_void_p(handle), ctypes.byref(route), int(act), float(g_act1), float(g_act2),
+        _hptr(x_host, torch.bfloat16, "x_host"), _hptr(token_ids_host, torch.int32, "token_ids_host"),
+        _hptr(out_host, torch.bfloat16, "out_host"), _hptr(topk_ids_host, torch.int32, "topk_ids_host"),
+        _hptr(topk_w_host, torch.float32, "topk_w_host"),
+        _dptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _dptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(st, "moe_forward_host")
 
 
 def moe_ffn_forward_noalloc(handle: int, T: int, act: int, g_act1: float, g_act2: float, x,

@@ -163,6 +163,29 @@ moe_status_t run_decode(const Handle* h, const FfnLaunch& L, const DecRoute& R, 
     return MOE_OK;
 }
 
+// Staging area of moe_forward_host, after the FFN workspace: the step's inputs and outputs.
+struct HostStage {
+    size_t x, out, ids, w, logits, tok, total;
+    static HostStage plan(const moe_ffn_desc& d, int T, int act) {
+        const int path = select_path(T, d.H, d.top_k, act, desc_tc_shape(d));
+        HostStage s{};
+        size_t off = align_up(Workspace::plan(d.E, d.H, d.I, d.I_shared, d.top_k, T, act, path).total, 256);
+        auto take = [&](size_t bytes) {
+            const size_t o = off;
+            off = align_up(off + bytes, 256);
+            return o;
+        };
+        s.x = take(sizeof(uint16_t) * (size_t)T * d.H);
+        s.out = take(sizeof(uint16_t) * (size_t)T * d.H);
+        s.ids = take(sizeof(int32_t) * (size_t)T * d.top_k);
+        s.w = take(sizeof(float) * (size_t)T * d.top_k);
+        s.logits = take(sizeof(float) * (size_t)T * (d.E + d.zero_experts));
+        s.tok = take(sizeof(int32_t) * (size_t)T);
+        s.total = off;
+        return s;
+    }
+};
+
 }  // namespace
 
 extern "C" {
@@ -382,6 +405,67 @@ moe_status_t moe_forward(const void* handle, const moe_route_desc* rd, int32_t a
     R.ids_out = topk_ids;
     R.w_out = topk_w;
     return run_decode(h, L, R, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_workspace_size_host(const moe_ffn_desc* d, int32_t T, int32_t act, size_t* bytes) {
+    const moe_status_t v = moe_workspace_size(d, T, act, bytes);
+    if (v != MOE_OK) return v;
+    *bytes = HostStage::plan(*d, T, act).total;
+    return MOE_OK;
+}
+
+moe_status_t moe_forward_host(const void* handle, const moe_route_desc* rd, int32_t act,
+                              float g_act1, float g_act2, const void* x_host,
+                              const int32_t* token_ids_host, void* out_host,
+                              int32_t* topk_ids_host, float* topk_w_host, void* workspace,
+                              size_t ws_bytes, int32_t* dev_status, void* stream) {
+    const Handle* h = static_cast<const Handle*>(handle);
+    if (!h || h->magic != 0x4D4F4531u) return MOE_ERR_INVALID_ARG;
+    const moe_status_t v = validate_route(rd, nullptr);
+    if (v != MOE_OK) return v;
+    const moe_ffn_desc& d = h->desc;
+    if (rd->E != d.E || rd->top_k != d.top_k || rd->H != d.H || rd->zero_experts != d.zero_experts)
+        return MOE_ERR_INVALID_ARG;
+    if (act != MOE_ACT_BF16 && act != MOE_ACT_NVFP4) return MOE_ERR_INVALID_ARG;
+    if (act == MOE_ACT_NVFP4 && (!pow2_positive(g_act1) || !pow2_positive(g_act2)))
+        return MOE_ERR_INVALID_ARG;
+    const int T = rd->T;
+    if (T == 0) return MOE_OK;
+    if (!x_host || !out_host || !workspace) return MOE_ERR_INVALID_ARG;
+    const bool hash_ids = is_hash(rd->scoring);
+    if (hash_ids && (!token_ids_host || !rd->tid2eid)) return MOE_ERR_INVALID_ARG;
+    if (rd->scoring != MOE_SCORE_HASH && !rd->w_router) return MOE_ERR_INVALID_ARG;
+    // every check moe_forward makes on the host, before the first copy is enqueued
+    if (select_path(T, d.H, d.top_k, act, h->tc_shape) == PATH_TC && !h->tc.ready)
+        return MOE_ERR_UNSUPPORTED;
+    const HostStage hs = HostStage::plan(d, T, act);
+    if (ws_bytes < hs.total) return MOE_ERR_WORKSPACE;
+    char* base = static_cast<char*>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t xbytes = sizeof(uint16_t) * (size_t)T * d.H;
+    const size_t pbytes = (size_t)T * d.top_k * 4;
+    moe_route_desc r = *rd;
+    r.token_ids = hash_ids ? reinterpret_cast<const int32_t*>(base + hs.tok) : nullptr;
+    if (cudaMemcpyAsync(base + hs.x, x_host, xbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (hash_ids && cudaMemcpyAsync(base + hs.tok, token_ids_host, sizeof(int32_t) * (size_t)T,
+                                    cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const moe_status_t f = moe_forward(
+        handle, &r, act, g_act1, g_act2, base + hs.x, nullptr,
+        rd->scoring == MOE_SCORE_HASH ? nullptr : reinterpret_cast<float*>(base + hs.logits),
+        reinterpret_cast<int32_t*>(base + hs.ids), reinterpret_cast<float*>(base + hs.w),
+        base + hs.out, workspace, ws_bytes, dev_status, stream);
+    if (f != MOE_OK) return f;
+    if (cudaMemcpyAsync(out_host, base + hs.out, xbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (topk_ids_host &&
+        cudaMemcpyAsync(topk_ids_host, base + hs.ids, pbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (topk_w_host &&
+        cudaMemcpyAsync(topk_w_host, base + hs.w, pbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 moe_status_t moe_set_wait_limit(void* handle, uint64_t cycles) {

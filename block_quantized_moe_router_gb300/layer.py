@@ -29,6 +29,8 @@ class MoeLayer:
                                   zero_experts)
         self.handle = capi.moe_prepare_weights(self.desc)
         self._ws = None
+        self._ws_host = None
+        self._host_route = {}
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     @classmethod
@@ -121,3 +123,27 @@ class MoeLayer:
                          out, self.workspace(T), logits_in=logits_in, logits_out=logits_out,
                          dev_status=self.status, stream=stream)
         return out, topk_ids, topk_w, logits_out
+
+    def forward_host(self, x_host, out_host, *, token_ids_host=None, topk_ids_host=None,
+                     topk_w_host=None, stream=None):
+        """Route + FFN on host buffers through moe_forward_host: x_host (and token_ids_host for
+        hash routing) are copied in, out_host (and the ids / weights when given) copied back, all
+        enqueued on the stream; the caller synchronises before reading the outputs."""
+        T = x_host.shape[0]
+        cached = self._host_route.get(T)
+        if cached is None:
+            d = capi.route_desc(T=T, E=self.E, H=self.H, top_k=self.top_k, scoring=self.scoring,
+                                renormalize=self.renormalize, routed_scaling=self.routed_scaling,
+                                w_router=self.w_router, correction_bias=self.correction_bias,
+                                tid2eid=self.tid2eid,
+                                vocab=0 if self.tid2eid is None else self.tid2eid.shape[0],
+                                zero_experts=self.zero_experts)
+            cached = self._host_route[T] = (d, capi.moe_workspace_size_host(self.desc, T, self.act))
+        d, need = cached
+        if self._ws_host is None or self._ws_host.numel() < need:
+            self._ws_host = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+        capi.moe_forward_host(self.handle, d, self.act, self.g_act1, self.g_act2, x_host, out_host,
+                              self._ws_host, token_ids_host=token_ids_host,
+                              topk_ids_host=topk_ids_host, topk_w_host=topk_w_host,
+                              dev_status=self.status, stream=stream)
+        return out_host

@@ -16,8 +16,9 @@
  *     The library owns only the prepared-weights handle and the buffers behind it.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *     Every call is asynchronous on that stream: no host synchronisation, no device-to-host
- *     copy and no memory allocation happen inside moe_route / moe_ffn_forward /
- *     moe_quantize_act_nvfp4.
+ *     copy and no memory allocation happen inside moe_route / moe_ffn_forward / moe_forward /
+ *     moe_quantize_act_nvfp4.  moe_forward_host alone copies, from and to the caller's host
+ *     buffers, and those copies are enqueued on the stream too.
  *   - Errors detectable on the host return a nonzero moe_status_t BEFORE anything is
  *     launched.  A failed launch returns MOE_ERR_CUDA.  Problems found in the data on the
  *     device are OR-ed into the caller's int32 device status word (MOE_DEV_* bits); the
@@ -212,6 +213,43 @@ moe_status_t moe_forward(const void* handle, const moe_route_desc* route, int32_
                          float g_act1, float g_act2, const void* x_bf16, const float* logits_in,
                          float* logits_out, int32_t* topk_ids, float* topk_w, void* out_bf16,
                          void* workspace, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* moe_forward for a caller whose tokens and results live in HOST memory.  It computes what
+ * moe_forward computes (the spark_model MoE pages, moe/mod.rs module doc: router, top-K and
+ * the expert FFN with the weighted sum); the pages' layer only ever sees device tensors, so
+ * the copies around it are this library's.  Enqueued on `stream`, in order: the copy of
+ * x_bf16_host (and, for both hash kinds, token_ids_host) into a staging area at the end of the
+ * workspace; moe_forward on the staged copies, with the router logits, ids and weights in that
+ * staging area; the copy of the output into out_bf16_host and, when those pointers are not
+ * NULL, of the ids and weights into topk_ids_host / topk_w_host.  The call returns once all
+ * of it is enqueued: the host buffers must stay valid, and the inputs unchanged, until the
+ * stream has passed the copies -- synchronise the stream (or an event recorded after the call)
+ * before reading the outputs.  Page-locked host memory (cudaHostAlloc / cudaHostRegister)
+ * makes the copies asynchronous and lets the call be captured into a CUDA graph; with pageable
+ * memory the runtime may block the host inside the copies.
+ * x_bf16_host    [host] bf16 [T][H].
+ * token_ids_host [host] int32 [T]; required for both hash kinds, ignored otherwise (the
+ *                route descriptor's token_ids field is ignored).
+ * out_bf16_host  [host] bf16 [T][H].
+ * topk_ids_host  [host] int32 [T][top_k] or NULL;  topk_w_host [host] float [T][top_k] or NULL.
+ * workspace      [device], ws_bytes >= moe_workspace_size_host for (desc, T, act).
+ * dev_status     [device] int32 [1] or NULL, as for moe_forward.
+ * The router must run in the call: route->w_router is required unless route->scoring is
+ * MOE_SCORE_HASH (precomputed logits are not taken from the host).  Errors: those of
+ * moe_forward; MOE_ERR_INVALID_ARG for a NULL x_bf16_host / out_bf16_host, a hash kind without
+ * token_ids_host, or a learned router without w_router; MOE_ERR_WORKSPACE when ws_bytes is
+ * below moe_workspace_size_host; MOE_ERR_CUDA when a copy cannot be enqueued.  T == 0 is a
+ * valid no-op.
+ * moe_workspace_size_host: moe_workspace_size plus the staging area (x and the output, T * H
+ * bf16 each; ids, weights, token ids and the E + zero_experts router logits per token), each
+ * part 256-byte aligned.  Host-only; errors as for moe_workspace_size. */
+moe_status_t moe_workspace_size_host(const moe_ffn_desc* desc, int32_t T, int32_t act,
+                                     size_t* bytes);
+moe_status_t moe_forward_host(const void* handle, const moe_route_desc* route, int32_t act,
+                              float g_act1, float g_act2, const void* x_bf16_host,
+                              const int32_t* token_ids_host, void* out_bf16_host,
+                              int32_t* topk_ids_host, float* topk_w_host, void* workspace,
+                              size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* The NVFP4 activation quantizer on its own (the `quantize_bf16_to_nvfp4` step of the
  * FP4 x FP4 recipe, qwen3_attention/init.rs handle list): per 16 consecutive elements of

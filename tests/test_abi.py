@@ -70,6 +70,22 @@ def test_workspace_size_and_validation(lib):
         capi.moe_workspace_size(d, 4, 0)
 
 
+def test_host_workspace_size(lib):
+    """The host-buffer entry's workspace is the FFN workspace plus its staging area."""
+    for T, act in ((1, 0), (8, 0), (64, 0), (300, 1)):
+        d = _fake_desc(H=512, I=256, Is=256, Z=2)
+        n = capi.moe_workspace_size(d, T, act)
+        nh = capi.moe_workspace_size_host(d, T, act)
+        stage = 2 * T * 512 * 2 + 2 * T * 2 * 4 + T * (8 + 2) * 4 + T * 4
+        assert n + stage <= nh <= n + stage + 7 * 256
+    with pytest.raises(capi.MoeError):
+        capi.moe_workspace_size_host(_fake_desc(E=0), 4, 0)
+    fake = ctypes.c_void_p(0x1000)
+    d = capi.moe_route_desc(4, 8, 256, 2, 0, 1, 1.0, 0x1000, None, None, 0, None, 0)
+    assert lib.moe_forward_host(None, ctypes.byref(d), 0, 1.0, 1.0, fake, None, fake, None, None,
+                                fake, 1 << 20, None, None) == capi.MOE_ERR_INVALID_ARG
+
+
 def test_route_rejects_before_launch(lib):
     fake = ctypes.c_void_p(0x1000)
 

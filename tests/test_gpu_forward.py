@@ -214,6 +214,79 @@ def test_forward_zero_tokens_and_arg_checks(cuda_lib):
     layer.close()
 
 
+HOST_CASES = ["t1_no_renorm", "t1_zero_hash", "max_pairs", "hash_sqrt", "fallback_generic",
+              "fallback_tc", "fallback_hash_sqrt_tc"]
+
+
+@pytest.mark.parametrize("name", HOST_CASES)
+def test_forward_host_buffers(cuda_lib, name):
+    """moe_forward_host (host buffers in and out, the copies enqueued with the forward) gives
+    the oracle's routing and output, and exactly what moe_forward gives on device buffers;
+    two slots of pinned buffers used in turn with inputs that differ stay separate."""
+    cfg = CASES[name]
+    inp, _ = parity.make_case(cfg, seed=7, device="cpu")
+    inp2, _ = parity.make_case(cfg, seed=8, device="cpu")
+    layer = MoeLayer.from_inputs(inp)
+    dev = []
+    for case in (inp, inp2):
+        out, ids, w, _ = _forward(layer, case)
+        dev.append((out.cpu(), ids.cpu(), w.cpu()))
+    hash_kind = cfg.scoring in (S.SCORE_HASH, S.SCORE_HASH_SQRTSOFTPLUS)
+    slots = []
+    for case in (inp, inp2):
+        slots.append(dict(
+            x=case["x"].to(torch.bfloat16).contiguous().pin_memory(),
+            tok=case["token_ids"].contiguous().pin_memory() if hash_kind else None,
+            out=torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory(),
+            ids=torch.empty((cfg.T, cfg.k), dtype=torch.int32).pin_memory(),
+            w=torch.empty((cfg.T, cfg.k), dtype=torch.float32).pin_memory()))
+    st = torch.cuda.Stream()
+    for _ in range(2):
+        for sl in slots:
+            layer.forward_host(sl["x"], sl["out"], token_ids_host=sl["tok"],
+                               topk_ids_host=sl["ids"], topk_w_host=sl["w"], stream=st)
+    st.synchronize()
+    assert int(layer.status.item()) == 0
+    for sl, (out, ids, w) in zip(slots, dev):
+        assert torch.equal(sl["out"], out) and torch.equal(sl["ids"], ids) and torch.equal(sl["w"], w)
+    ref_r = parity.oracle_route(cfg, inp)
+    parity.assert_routing(cfg, ref_r, slots[0]["ids"], slots[0]["w"], inp=inp)
+    parity.assert_close(slots[0]["out"], parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"]),
+                        cfg.name + " host")
+    # pageable host memory and no ids / weights requested: same output
+    out_p = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16)
+    layer.forward_host(inp["x"].to(torch.bfloat16).contiguous(), out_p,
+                       token_ids_host=inp["token_ids"].contiguous() if hash_kind else None)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p, dev[0][0])
+    layer.close()
+
+
+def test_forward_host_arg_checks(cuda_lib):
+    cfg = CASES["tiny"]
+    inp, _ = parity.make_case(cfg, seed=0, device="cpu")
+    layer = MoeLayer.from_inputs(inp)
+    x = inp["x"].to(torch.bfloat16).contiguous()
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16)
+    d = capi.route_desc(T=cfg.T, E=cfg.E, H=cfg.H, top_k=cfg.k, scoring=cfg.scoring,
+                        renormalize=True, routed_scaling=1.0, w_router=layer.w_router)
+    need = capi.moe_workspace_size_host(layer.desc, cfg.T, capi.MOE_ACT_BF16)
+    assert need >= capi.moe_workspace_size(layer.desc, cfg.T, capi.MOE_ACT_BF16) + 2 * cfg.T * cfg.H * 2
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(capi.MoeError) as ei:
+        capi.moe_forward_host(layer.handle, d, capi.MOE_ACT_BF16, 1.0, 1.0, x, out, ws)
+    assert ei.value.status == capi.MOE_ERR_WORKSPACE
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    nor = capi.route_desc(T=cfg.T, E=cfg.E, H=cfg.H, top_k=cfg.k, scoring=cfg.scoring,
+                          renormalize=True, routed_scaling=1.0)
+    with pytest.raises(capi.MoeError) as ei:  # the router must run inside the call
+        capi.moe_forward_host(layer.handle, nor, capi.MOE_ACT_BF16, 1.0, 1.0, x, out, ws)
+    assert ei.value.status == capi.MOE_ERR_INVALID_ARG
+    with pytest.raises(ValueError):  # device tensors are not host buffers
+        capi.moe_forward_host(layer.handle, d, capi.MOE_ACT_BF16, 1.0, 1.0, x.cuda(), out, ws)
+    layer.close()
+
+
 def test_barrier_wait_runs_out(cuda_lib):
     """The few-token kernel's device-wide barrier waits are bounded.  With a 10 ms limit and
     the handle's barrier epoch moved one launch ahead (moe_skew_barrier), no barrier of the
