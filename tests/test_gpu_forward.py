@@ -66,6 +66,18 @@ CASES = {
     "fallback_hash_sqrt_tc": S.MoeConfig("fw_hash_sqrt_tc", T=40, H=512, I=256, E=16, k=4,
                                          scoring=S.SCORE_HASH_SQRTSOFTPLUS, scaling=2.0,
                                          I_shared=256, act=S.ACT_NVFP4, vocab=64),
+    # the largest top_k (32): one token's 32 picks built by the top-K warp, 64 pairs of two
+    # tokens through the general dispatch, then the generic and tensor-core paths
+    "max_topk_t1": S.MoeConfig("fw_max_topk_t1", T=1, H=256, I=128, E=64, k=32,
+                               scoring=S.SCORE_SIGMOID, scaling=2.0, I_shared=128),
+    "max_topk_t2": S.MoeConfig("fw_max_topk_t2", T=2, H=256, I=256, E=48, k=32,
+                               scoring=S.SCORE_SOFTMAX),
+    # (softmax selection at H 1024: logits spread enough for every token's top 33 to stay
+    # 1e-3 apart, which sigmoid scores over 64 experts do not)
+    "max_topk_generic": S.MoeConfig("fw_max_topk_generic", T=12, H=1024, I=128, E=64, k=32,
+                                    scoring=S.SCORE_SOFTMAX, scaling=2.0, I_shared=128),
+    "max_topk_tc": S.MoeConfig("fw_max_topk_tc", T=40, H=1024, I=256, E=64, k=32,
+                               scoring=S.SCORE_SOFTMAX, I_shared=256, act=S.ACT_NVFP4),
     # more tokens: moe_route + moe_ffn_forward behind the same call
     "fallback_generic": S.MoeConfig("fw_generic", T=20, H=256, I=128, E=16, k=3,
                                     scoring=S.SCORE_SIGMOID, scaling=2.5, I_shared=128),
