@@ -249,64 +249,66 @@ __global__ void __launch_bounds__(256) tc_quant_tokens_kernel(TcQuantArgs a) {
     }
 }
 
-// Work items of (128-row block in use, chunk c of 32 K blocks), CTA-strided; with n chunks per
-// row an item copies the codes of rows [128 c / n, 128 (c + 1) / n) of its block and the
-// scales of its chunk.  Codes: one flat range of 16-byte words, each thread keeping 8 loads in
-// flight.  Scales: each row's 4-byte scale groups are read as one 128-byte run into shared
-// memory and written out as the tile lines (line l of K block kb holds the scales of rows l,
-// l + 32, l + 64, l + 96; 512 contiguous bytes per K block).  Rows without a pair keep
-// whatever codes they had and get zero scales, so they contribute nothing.
+// Warp items, strided over the grid's warps: first one per padded row in use -- the warp
+// copies the codes of the row's token (7 independent 16-byte loads per lane at H 7168) --,
+// then one per (128-row block, 16 K blocks) -- lane l builds line l of each K block's scale
+// tile (the scales of rows l, l + 32, l + 64, l + 96; 512 contiguous bytes per K block) from
+// 16-byte runs of its four tokens' scales.  Rows without a pair keep whatever codes they had
+// and get zero scales, so they contribute nothing.
 constexpr int kGatherThreads = 256;
 __global__ void __launch_bounds__(kGatherThreads) tc_gather_rows_kernel(TcQuantArgs a) {
-    __shared__ int tok[128];
-    __shared__ uint32_t sw[128][33];
-    const int nblk = a.meta[3];
-    const int KB = a.H / 64, wpr = a.H / 32;  // K blocks, 16-byte code words per row
-    const int nchunk = (KB + 31) / 32;
-    const uint32_t* toks32 = reinterpret_cast<const uint32_t*>(a.toks);
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * kGatherThreads + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * kGatherThreads) >> 5;
+    const int nblk = a.meta[3], rows = nblk * 128;
+    const int KB = a.H / 64, wpr = a.H / 32;  // K blocks (a multiple of 4), 16-byte code words per row
+    const int kch = (KB + 15) / 16;
     const uint4* src = reinterpret_cast<const uint4*>(a.tokq);
-    for (int item = blockIdx.x; item < nblk * nchunk; item += gridDim.x) {
-        const int mb = item / nchunk, c = item - mb * nchunk;
-        const int r0 = 128 * c / nchunk, r1 = 128 * (c + 1) / nchunk;
-        const int k0 = 32 * c, nk = min(32, KB - k0);
-        __syncthreads();  // the previous item's reads of tok[] and sw[] are done
-        if (threadIdx.x < 128) {
-            const int p = a.padrow_pair[mb * 128 + threadIdx.x];
-            tok[threadIdx.x] = p < 0 ? -1 : (p < a.P ? p / a.k : p - a.P);
-        }
-        __syncthreads();
-        const int total = (r1 - r0) * wpr;
-        uint4* dst = reinterpret_cast<uint4*>(a.xq + ((size_t)mb * 128 + r0) * (a.H / 2));
-        for (int j0 = threadIdx.x; j0 < total; j0 += 8 * kGatherThreads) {
-            uint4 v[8];
-            int dj[8];
+    uint4* dst = reinterpret_cast<uint4*>(a.xq);
+    auto token_of = [&](int row) {
+        const int p = a.padrow_pair[row];
+        return p < 0 ? -1 : (p < a.P ? p / a.k : p - a.P);
+    };
+    const int64_t items = (int64_t)rows + (int64_t)nblk * kch;
+    for (int64_t it = gw; it < items; it += nw) {
+        if (it < rows) {
+            const int row = (int)it;
+            const int t = token_of(row);
+            if (t < 0) continue;
+            const uint4* s = src + (size_t)t * wpr;
+            uint4* d = dst + (size_t)row * wpr;
+            for (int w0 = 0; w0 < wpr; w0 += 8 * 32) {
+                uint4 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = j0 + u * kGatherThreads;
-                dj[u] = -1;
-                if (j < total) {
-                    const int r = j / wpr;
-                    const int t = tok[r0 + r];
-                    if (t >= 0) {
-                        v[u] = src[(size_t)t * wpr + (j - r * wpr)];
-                        dj[u] = j;
-                    }
+                for (int u = 0; u < 8; ++u) {
+                    const int w = w0 + 32 * u + lane;
+                    if (w < wpr) v[u] = s[w];
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int w = w0 + 32 * u + lane;
+                    if (w < wpr) d[w] = v[u];
                 }
             }
+        } else {
+            const int64_t j = it - rows;
+            const int mb = (int)(j / kch), kb0 = 16 * (int)(j - (int64_t)mb * kch);
+            const int kb1 = min(KB, kb0 + 16);
+            int tk[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (dj[u] >= 0) dst[dj[u]] = v[u];
-        }
-        for (int i = threadIdx.x; i < 128 * 32; i += kGatherThreads) {
-            const int r = i >> 5, kk = i & 31;
-            const int t = tok[r];
-            sw[r][kk] = (t < 0 || kk >= nk) ? 0u : toks32[(size_t)t * KB + k0 + kk];
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < nk * 32; i += kGatherThreads) {
-            const int kk = i >> 5, l = i & 31;
-            *reinterpret_cast<uint4*>(a.xsf + ((size_t)mb * KB + k0 + kk) * 512 + l * 16) =
-                make_uint4(sw[l][kk], sw[32 + l][kk], sw[64 + l][kk], sw[96 + l][kk]);
+            for (int q = 0; q < 4; ++q) tk[q] = token_of(mb * 128 + 32 * q + lane);
+            for (int kb = kb0; kb < kb1; kb += 4) {
+                uint4 s4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    s4[q] = tk[q] < 0 ? make_uint4(0u, 0u, 0u, 0u)
+                                      : *reinterpret_cast<const uint4*>(a.toks + ((size_t)tk[q] * KB + kb) * 4);
+                uint8_t* line = a.xsf + ((size_t)mb * KB + kb) * 512 + 16 * lane;
+                *reinterpret_cast<uint4*>(line) = make_uint4(s4[0].x, s4[1].x, s4[2].x, s4[3].x);
+                *reinterpret_cast<uint4*>(line + 512) = make_uint4(s4[0].y, s4[1].y, s4[2].y, s4[3].y);
+                *reinterpret_cast<uint4*>(line + 1024) = make_uint4(s4[0].z, s4[1].z, s4[2].z, s4[3].z);
+                *reinterpret_cast<uint4*>(line + 1536) = make_uint4(s4[0].w, s4[1].w, s4[2].w, s4[3].w);
+            }
         }
     }
 }
