@@ -48,6 +48,9 @@ CASES = {
     "tc_router": synth.MoeConfig("tr", T=300, H=384, I=128, E=128, k=6, scoring=synth.SCORE_SOFTMAX),
     "tc_router_sig": synth.MoeConfig("trs", T=129, H=1152, I=128, E=256, k=8,
                                      scoring=synth.SCORE_SIGMOID, scaling=2.5),
+    # 16500 tokens: 129 token blocks of the tensor-core router, the last one ragged
+    "tc_router_many": synth.MoeConfig("trw", T=16500, H=256, I=128, E=256, k=8,
+                                      scoring=synth.SCORE_SOFTMAX),
     # hash-table ids, sqrt(softplus) router-score weights (router on the tensor cores, then the
     # hash kernel reads the logits)
     "hash_sqrt": synth.MoeConfig("hs", T=200, H=1024, I=128, E=128, k=6,
