@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,   /* a size, pointer or enum is out of its documented range  */
-    MOE_ERR_UNSUPPORTED = 2,   /* a valid combination this build does not implement       */
+    MOE_ERR_UNSUPPORTED = 2,   /* a valid combination this library does not implement     */
     MOE_ERR_CUDA = 3,          /* a CUDA runtime call or a kernel launch failed            */
     MOE_ERR_WORKSPACE = 4      /* the workspace passed is smaller than moe_workspace_size */
 } moe_status_t;
