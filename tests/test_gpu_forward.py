@@ -299,12 +299,15 @@ def test_forward_host_arg_checks(cuda_lib):
     layer.close()
 
 
-def test_barrier_wait_runs_out(cuda_lib):
+@pytest.mark.parametrize("name", ["ragged", "t1_no_renorm"])
+def test_barrier_wait_runs_out(cuda_lib, name):
     """The few-token kernel's device-wide barrier waits are bounded.  With a 10 ms limit and
     the handle's barrier epoch moved one launch ahead (moe_skew_barrier), no barrier of the
     next launch can complete: the launch must return (well inside a second), set
-    MOE_DEV_TIMEOUT, and leave the device usable -- a fresh handle then gives correct results."""
-    cfg = CASES["ragged"]
+    MOE_DEV_TIMEOUT, and leave the device usable -- a fresh handle then gives correct results.
+    One token (its own kernel instantiation, the top-K warp building the dispatch) and several
+    tokens."""
+    cfg = CASES[name]
     inp, _ = parity.make_case(cfg, seed=6, device="cpu")
     layer = MoeLayer.from_inputs(inp)
     x = inp["x"].cuda()
