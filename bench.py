@@ -66,6 +66,13 @@ TRAFFIC = {  # one-pass captures at full size (the commands are in the profile s
 }
 
 
+def captured_traffic(workload: str, src_hash: str):
+    """DRAM bytes per launch of the workload's dominant kernel from its ncu capture, or None when
+    there is none or the kernel's sources have changed since (their hash differs)."""
+    tr = TRAFFIC.get(workload)
+    return tr[0] if tr and tr[1] == src_hash else None
+
+
 def kernel_source_hash(files) -> str:
     h = hashlib.sha256()
     for f in files:
@@ -649,8 +656,7 @@ def measure(cfg, args, steps, dist, world, rank, local, want_e2e=True, whole_cyc
         # the bound: whichever roof is lower for this launch's bytes and FLOPs
         tensor_bound = a4 and dom_flops / (mma_peak * 1e12) > dom_bytes / (hbm * 1e9)
         src = kernel_source_hash(KERNEL_SOURCES["decode" if dec else "tc" if a4 else "mma"])
-        tr = TRAFFIC.get(cfg.name)
-        traffic = tr[0] if tr and tr[1] == src else None
+        traffic = captured_traffic(cfg.name, src)
         if tensor_bound:
             roof = {"bound": "tensor", "achieved": tflops, "peak": mma_peak, "unit": "TFLOP/s",
                     "frac": tflops / mma_peak, "traffic": traffic,

@@ -79,3 +79,19 @@ def test_clock_sampler_without_nvidia_smi(tmp_path):
     s.mark()
     s.mark()
     assert s.stop() is None
+
+
+def test_captured_traffic_follows_the_kernel_sources():
+    """The line reports a kernel's ncu DRAM traffic only while the hash of its sources matches
+    the one the capture was taken on; every workload's entry names a known kernel family."""
+    families = {"pre4096": "tc", "pre32768": "tc", "dec1": "decode", "dec8": "decode",
+                "hash64": "mma"}
+    assert set(bench.TRAFFIC) <= set(families)
+    for name, (nbytes, h) in bench.TRAFFIC.items():
+        assert nbytes > 0 and len(h) == 16
+        assert bench.captured_traffic(name, h) == nbytes
+        assert bench.captured_traffic(name, "0" * 16) is None
+    assert bench.captured_traffic("tiny", bench.kernel_source_hash(bench.KERNEL_SOURCES["tc"])) is None
+    for fam, files in bench.KERNEL_SOURCES.items():
+        assert len(bench.kernel_source_hash(files)) == 16
+
