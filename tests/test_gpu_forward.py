@@ -296,6 +296,13 @@ def test_forward_host_arg_checks(cuda_lib):
     assert ei.value.status == capi.MOE_ERR_INVALID_ARG
     with pytest.raises(ValueError):  # device tensors are not host buffers
         capi.moe_forward_host(layer.handle, d, capi.MOE_ACT_BF16, 1.0, 1.0, x.cuda(), out, ws)
+    # no tokens: a valid no-op
+    d0 = capi.route_desc(T=0, E=cfg.E, H=cfg.H, top_k=cfg.k, scoring=cfg.scoring,
+                         renormalize=True, routed_scaling=1.0, w_router=layer.w_router)
+    capi.moe_forward_host(layer.handle, d0, capi.MOE_ACT_BF16, 1.0, 1.0,
+                          torch.empty((0, cfg.H), dtype=torch.bfloat16),
+                          torch.empty((0, cfg.H), dtype=torch.bfloat16), ws)
+    torch.cuda.synchronize()
     layer.close()
 
 
