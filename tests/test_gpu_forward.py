@@ -78,6 +78,12 @@ CASES = {
                                     scoring=S.SCORE_SOFTMAX, scaling=2.0, I_shared=128),
     "max_topk_tc": S.MoeConfig("fw_max_topk_tc", T=40, H=1024, I=256, E=64, k=32,
                                scoring=S.SCORE_SOFTMAX, I_shared=256, act=S.ACT_NVFP4),
+    # the widest hidden size the single launch takes (H 8192: the router phase's chunk bound,
+    # four 16-row output tiles per CTA)
+    "max_h_t1": S.MoeConfig("fw_max_h_t1", T=1, H=8192, I=256, E=16, k=4,
+                            scoring=S.SCORE_SOFTMAX),
+    "max_h_t8": S.MoeConfig("fw_max_h_t8", T=8, H=8192, I=128, E=16, k=4,
+                            scoring=S.SCORE_SIGMOID, scaling=2.0, I_shared=128),
     # more tokens: moe_route + moe_ffn_forward behind the same call
     "fallback_generic": S.MoeConfig("fw_generic", T=20, H=256, I=128, E=16, k=3,
                                     scoring=S.SCORE_SIGMOID, scaling=2.5, I_shared=128),
