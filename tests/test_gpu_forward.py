@@ -84,6 +84,9 @@ CASES = {
                             scoring=S.SCORE_SOFTMAX),
     "max_h_t8": S.MoeConfig("fw_max_h_t8", T=8, H=8192, I=128, E=16, k=4,
                             scoring=S.SCORE_SIGMOID, scaling=2.0, I_shared=128),
+    # a hidden size above that bound: a few tokens take moe_route + the generic expert GEMM
+    "wide_h_generic": S.MoeConfig("fw_wide_h", T=3, H=8320, I=128, E=8, k=2,
+                                  scoring=S.SCORE_SOFTMAX, I_shared=128),
     # more tokens: moe_route + moe_ffn_forward behind the same call
     "fallback_generic": S.MoeConfig("fw_generic", T=20, H=256, I=128, E=16, k=3,
                                     scoring=S.SCORE_SIGMOID, scaling=2.5, I_shared=128),
