@@ -48,6 +48,10 @@ CASES = {
     "tc_router": synth.MoeConfig("tr", T=300, H=384, I=128, E=128, k=6, scoring=synth.SCORE_SOFTMAX),
     "tc_router_sig": synth.MoeConfig("trs", T=129, H=1152, I=128, E=256, k=8,
                                      scoring=synth.SCORE_SIGMOID, scaling=2.5),
+    # >= 128 tokens with experts not a multiple of 128: the shared-memory tiled router GEMM over
+    # three 128-token blocks, the last one ragged
+    "tiled_router_many": synth.MoeConfig("trm", T=300, H=512, I=128, E=96, k=6,
+                                         scoring=synth.SCORE_SOFTMAX),
     # 16500 tokens: 129 token blocks of the tensor-core router, the last one ragged
     "tc_router_many": synth.MoeConfig("trw", T=16500, H=256, I=128, E=256, k=8,
                                       scoring=synth.SCORE_SOFTMAX),
