@@ -315,6 +315,55 @@ def test_forward_host_arg_checks(cuda_lib):
     layer.close()
 
 
+GUARD = 4096
+
+
+def _guarded(nbytes):
+    """A device buffer of nbytes between two 4 KB guard regions filled with 0xA5."""
+    buf = torch.full((2 * GUARD + nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    return buf, buf[GUARD:GUARD + nbytes]
+
+
+@pytest.mark.parametrize("name", ["t1_zero_hash", "t1_wide", "max_pairs", "fallback_generic_zero",
+                                  "fallback_tc_zero", "fallback_hash_sqrt_tc"])
+def test_writes_stay_inside_their_buffers(cuda_lib, name):
+    """Every kernel of the call writes only inside the buffers it is given: the output, the ids,
+    the weights, the router logits and the workspace (sized exactly by moe_workspace_size) each
+    sit between guard regions that must come back untouched."""
+    cfg = CASES[name]
+    inp, _ = parity.make_case(cfg, seed=9, device="cpu")
+    layer = MoeLayer.from_inputs(inp)
+    T, Er = cfg.T, cfg.E + cfg.zero_experts
+    hash_only = cfg.scoring == S.SCORE_HASH
+    parts = {"out": (T * cfg.H * 2, torch.bfloat16, (T, cfg.H)),
+             "ids": (T * cfg.k * 4, torch.int32, (T, cfg.k)),
+             "w": (T * cfg.k * 4, torch.float32, (T, cfg.k)),
+             "ws": (capi.moe_workspace_size(layer.desc, T, cfg.act), torch.uint8, None)}
+    if not hash_only:
+        parts["logits"] = (T * Er * 4, torch.float32, (T, Er))
+    bufs, views = {}, {}
+    for key, (nbytes, dtype, shape) in parts.items():
+        bufs[key], raw = _guarded(nbytes)
+        views[key] = raw if shape is None else raw.view(dtype).view(shape)
+    tok = inp["token_ids"].cuda() if "token_ids" in inp else None
+    d = capi.route_desc(T=T, E=cfg.E, H=cfg.H, top_k=cfg.k, scoring=cfg.scoring,
+                        renormalize=cfg.renorm, routed_scaling=cfg.scaling, w_router=layer.w_router,
+                        correction_bias=layer.correction_bias, tid2eid=layer.tid2eid,
+                        vocab=0 if layer.tid2eid is None else layer.tid2eid.shape[0],
+                        token_ids=tok, zero_experts=cfg.zero_experts)
+    capi.moe_forward(layer.handle, d, cfg.act, 1.0, 1.0, inp["x"].cuda(), views["ids"], views["w"],
+                     views["out"], views["ws"], logits_out=views.get("logits"),
+                     dev_status=layer.status)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    for key, buf in bufs.items():
+        assert bool((buf[:GUARD] == 0xA5).all()), f"{key}: written before its start"
+        assert bool((buf[GUARD + parts[key][0]:] == 0xA5).all()), f"{key}: written past its end"
+    ref_r = parity.oracle_route(cfg, inp)
+    parity.assert_close(views["out"], parity.oracle_ffn(cfg, inp, ref_r["ids"], ref_r["w"]), name)
+    layer.close()
+
+
 @pytest.mark.parametrize("name", ["ragged", "t1_no_renorm"])
 def test_barrier_wait_runs_out(cuda_lib, name):
     """The few-token kernel's device-wide barrier waits are bounded.  With a 10 ms limit and
