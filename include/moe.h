@@ -65,8 +65,10 @@ typedef enum {
 } moe_scoring_t;
 typedef enum { MOE_FMT_NVFP4 = 0, MOE_FMT_MXFP4 = 1 } moe_fmt_t;
 /* Activation precision of the expert GEMMs.  BF16: W4A16 (bf16 tokens, dequantized
- * weights).  NVFP4: W4A4 -- tokens and the intermediate h are quantized to NVFP4 (per 16
- * elements, E4M3 scale, static power-of-two f32 global) before the block-scaled FP4 MMA. */
+ * weights; tokens and h enter the MMAs as f16, so their magnitudes must stay within f16's
+ * finite range, 65504).  NVFP4: W4A4 -- tokens and the intermediate h are quantized to NVFP4
+ * (per 16 elements, E4M3 scale, static power-of-two f32 global) before the block-scaled FP4
+ * MMA. */
 typedef enum { MOE_ACT_BF16 = 0, MOE_ACT_NVFP4 = 1 } moe_act_t;
 
 /* One block-quantized projection, stacked over experts (layout in the header comment). */
